@@ -1,0 +1,148 @@
+"""The CPU oracle against its pins (brute force, closed forms, hand-derived goldens,
+library routines, invariants), and mutation tests showing that a plausible
+mistake planted in the oracle makes at least one pin fail."""
+import numpy as np
+import pytest
+
+import workloads
+from oracle import moe_ref
+
+import oracle_pins as P
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin()
+
+
+def test_bruteforce_tiny_workload():
+    """Vectorised oracle == per-token brute force on the 64-token tiny layer."""
+    P.pin_bruteforce_layer()
+
+
+def test_bruteforce_ragged_shape():
+    P.pin_bruteforce_layer(shape=(128, 5, 3, 64), T=13, seed=3)
+
+
+def test_skew_calibration():
+    """The skewed long prefill leaves about 30 experts empty and one expert chosen by
+    nearly every token (at most T of the T*k assignments can go to one expert)."""
+    wl = workloads.WORKLOADS["skew16k"]
+    tok = workloads.make_tokens(wl.shape, wl.T, 0, skew=True)
+    ids, _ = moe_ref.topk_route(tok["logits"], wl.shape.k)
+    counts = moe_ref.histogram(ids, wl.shape.E)
+    assert 25 <= int((counts == 0).sum()) <= 35
+    assert counts.max() > 0.9 * wl.T
+
+
+def test_generator_statistics():
+    wl = workloads.WORKLOADS["tiny"]
+    d = workloads.make_workload(wl)
+    x = workloads.bf16_bits_to_f32(d["x_bits"])
+    assert abs(x.mean()) < 0.05 and abs(x.std() - 1) < 0.05
+    assert abs(d["logits"].std() - 1) < 0.1
+    q = moe_ref.unpack_u4(d["w13_packed"])
+    assert q.min() == 0 and q.max() == 15 and abs(q.mean() - 7.5) < 0.1
+    s = workloads.bf16_bits_to_f32(d["w13_scale"])
+    assert s.min() >= 0.0099 and s.max() <= 0.0301
+    b = workloads.bf16_bits_to_f32(d["w13_bias"]).astype(np.float64)
+    assert np.abs(b + 8 * s).max() < 0.006
+
+
+# --------------------------------------------------------------------------- #
+# mutation tests: each plants one mistake in the oracle; some pin must fail
+# --------------------------------------------------------------------------- #
+def _mutations():
+    orig = {n: getattr(moe_ref, n) for n in
+            ("unpack_u4", "dequant", "expert_swiglu", "topk_route", "expert_down",
+             "expert_weights", "stable_permutation", "round_bf16", "block_map", "exclusive_scan")}
+
+    def msb_first(p):
+        q = orig["unpack_u4"](p)
+        return q.reshape(*q.shape[:-1], -1, 8)[..., ::-1].reshape(q.shape)
+
+    def no_bias(packed, scale_bits, bias_bits):
+        return orig["dequant"](packed, scale_bits, np.zeros_like(bias_bits))
+
+    def silu_on_up(xrows, w13):
+        F = w13.shape[0] // 2
+        g, u = xrows @ w13[:F].T, xrows @ w13[F:].T
+        return moe_ref.round_bf16(moe_ref.silu(u) * g)
+
+    def ties_high(logits, k):
+        lg = np.asarray(logits, np.float32)
+        ids, w = orig["topk_route"](lg[:, ::-1], k)
+        return (lg.shape[1] - 1 - ids).astype(np.int32), w
+
+    def no_renorm(logits, k):
+        ids, w = orig["topk_route"](logits, k)
+        lg = np.asarray(logits, np.float64)
+        p = np.exp(lg - lg.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        return ids, np.take_along_axis(p, ids.astype(np.int64), 1)
+
+    def down_transposed(h, w2):
+        return h @ w2 if h.shape[1] == w2.shape[0] else h @ w2.T * 1.0001
+
+    def no_shared(wts, e):
+        w13, w2 = orig["expert_weights"](wts, e)
+        if e == wts["w13_packed"].shape[0] - 1:
+            return w13 * 0, w2 * 0
+        return w13, w2
+
+    def unstable(ids):
+        perm, inv = orig["stable_permutation"](ids)
+        flat = np.asarray(ids).ravel()
+        perm = perm.copy()
+        for e in np.unique(flat):
+            sel = np.nonzero(flat[perm] == e)[0]
+            perm[sel] = perm[sel][::-1]
+        inv = np.empty_like(perm)
+        inv[perm] = np.arange(perm.size, dtype=np.int32)
+        return perm, inv
+
+    def truncate(a):
+        a = np.asarray(a, dtype=np.float64)
+        m, e = np.frexp(a)
+        return np.ldexp(np.trunc(m * 256.0), e - 8)
+
+    def bm_no_shared(counts, offsets, T, block_n):
+        bm = orig["block_map"](counts, offsets, T, block_n)
+        return bm[bm[:, 0] < len(counts)]
+
+    def inclusive(counts):
+        c = np.asarray(counts, np.int64)
+        return np.concatenate([np.cumsum(c), [c.sum()]]).astype(np.int32)
+
+    return {
+        "nibble_msb_first": ("unpack_u4", msb_first),
+        "dequant_drops_bias": ("dequant", no_bias),
+        "silu_on_up": ("expert_swiglu", silu_on_up),
+        "ties_to_high_index": ("topk_route", ties_high),
+        "no_renormalisation": ("topk_route", no_renorm),
+        "down_transposed": ("expert_down", down_transposed),
+        "shared_expert_dropped": ("expert_weights", no_shared),
+        "unstable_scatter": ("stable_permutation", unstable),
+        "bf16_truncation": ("round_bf16", truncate),
+        "block_map_drops_shared": ("block_map", bm_no_shared),
+        "inclusive_scan": ("exclusive_scan", inclusive),
+    }
+
+
+MUTATIONS = _mutations()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, monkeypatch):
+    attr, fn = MUTATIONS[name]
+    monkeypatch.setattr(moe_ref, attr, fn)
+    failed = []
+    checks = P.ALL_PINS + [lambda: P.pin_bruteforce_layer(shape=(128, 4, 2, 64), T=9, seed=1)]
+    for pin in checks:
+        try:
+            pin()
+        except AssertionError:
+            failed.append(getattr(pin, "__name__", "brute"))
+        except Exception as ex:  # a mutation that breaks shapes is caught too
+            failed.append(f"{getattr(pin, '__name__', 'brute')}:{type(ex).__name__}")
+    assert failed, f"mutation {name} slipped through every pin"
