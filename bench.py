@@ -1,0 +1,385 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4 MoE FFN layer forward (routing + grouped GEMMs + combine).
+
+One step = one pass of the whole hot path over one batch of synthetic tokens:
+moe_route -> gate/up GEMM (+SwiGLU) -> down GEMM (+weighted combine) ->
+moe_combine.  The default workload is the 512-token prefill through the
+full-width layer (H=2048, 256 experts top-8 + 1 shared, F=512).  Weights
+(455 MB packed) exceed the 126 MB L2, so every step streams them from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload prefill512|prefill4k|decode1|decode8|skew16k|tiny]
+                  [--kernels auto|tc|simt|gemv] [--no-extra]
+
+Under torchrun each rank runs the same workload on its own GPU with its own
+tokens (weak scaling, no collective on the data path); rank 0 prints one JSON
+line.  `--impl reference` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (W4 routing+grouped GEMM) at T=512/4096; % of roofline"
+L2_BYTES = 126 * 1024 * 1024
+
+
+# --------------------------------------------------------------------------- #
+# algorithmic work (per launch / per step)
+# --------------------------------------------------------------------------- #
+def expert_bytes(shape):
+    """Packed uint4 weights + bf16 scale + bf16 bias of one expert's gate/up and down matrices."""
+    H, F = shape.H, shape.F
+    w13 = 2 * F * H // 2 + 2 * (2 * F * H // 64) * 2
+    w2 = H * F // 2 + 2 * (H * F // 64) * 2
+    return w13, w2
+
+
+def algorithmic(shape, T, n_touched):
+    w13, w2 = expert_bytes(shape)
+    H, F, k, E = shape.H, shape.F, shape.k, shape.E
+    A = T * k
+    rows = A + T
+    n = n_touched + 1
+    gate_up_bytes = n * w13 + T * H * 2 + rows * F * 2            # weights + x + h
+    down_bytes = n * w2 + rows * F * 2 + T * H * 4 * 2             # weights + h + acc read/write (L2)
+    flops_gate_up = 2.0 * rows * 2 * F * H
+    flops_down = 2.0 * rows * H * F
+    step_bytes = n * (w13 + w2) + T * H * 2 + T * E * 4 + T * H * 2
+    return {"gate_up_bytes": gate_up_bytes, "down_bytes": down_bytes, "flops_gate_up": flops_gate_up,
+            "flops_down": flops_down, "step_bytes": step_bytes, "step_flops": flops_gate_up + flops_down}
+
+
+# --------------------------------------------------------------------------- #
+# clocks
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "50"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if not self.proc:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln.strip() for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                rows.append({"sm": float(p[1]), "max": float(p[2]), "power": float(p[3]) if p[3] not in
+                             ("[N/A]", "N/A") else 0.0, "hw": p[5], "hwt": p[6], "swt": p[7], "pcap": p[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [r for r in rows if r["power"] > 300] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r["sm"] for r in busy])), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy)}
+
+
+# --------------------------------------------------------------------------- #
+# our implementation
+# --------------------------------------------------------------------------- #
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from bit_mixture_experts_gb300 import _lib, build
+    from bit_mixture_experts_gb300.layer import MoELayerW4
+
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = workloads.WORKLOADS[args.workload]
+    s = wl.shape
+    T = wl.T
+    d = workloads.make_workload(wl, seed=0, with_weights=True)
+    if rank:  # each rank its own tokens (weights are the same replica)
+        d.update(workloads.make_tokens(s, T, seed=rank, skew=wl.skew))
+    layer = MoELayerW4(s.H, s.E, s.k, s.F, d, device=dev, impl=args.kernels)
+    x = torch.from_numpy(d["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.from_numpy(d["logits"]).to(dev)
+    out = torch.empty((T, s.H), dtype=torch.bfloat16, device=dev)
+    b = layer.buffers(T)
+    stream = torch.cuda.current_stream()
+    impl, bn = layer.impl, layer.block_n
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        _lib.moe_route(logits, s.k, bn, b["topk_ids"], b["topk_w"], b["counts"], b["offsets"], b["perm"],
+                       b["inv_perm"], b["block_map"], b["num_blocks"], b["workspace"])
+        if ev is not None:
+            ev[1].record(stream)
+        w = layer.weights
+        _lib.moe_expert_gemm_w4(_lib.GATE_UP, impl, x, T, s.H, s.F, s.E, s.k, w.w13, w.s13, w.b13, b["perm"],
+                                b["topk_w"], b["block_map"], b["num_blocks"], bn, b["h"])
+        if ev is not None:
+            ev[2].record(stream)
+        _lib.moe_expert_gemm_w4(_lib.DOWN, impl, b["h"], T, s.H, s.F, s.E, s.k, w.w2, w.s2, w.b2, b["perm"],
+                                b["topk_w"], b["block_map"], b["num_blocks"], bn, b["acc"])
+        if ev is not None:
+            ev[3].record(stream)
+        _lib.moe_combine(b["acc"], out)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    touched = int((b["counts"] > 0).sum().item())
+    work = algorithmic(s, T, touched)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if work["step_bytes"] < 2 * L2_BYTES \
+        else None
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    n0 = _lib.moe_launch_count()
+    if clocks:
+        clocks.mark_start()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_end()
+    launches = _lib.moe_launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    if clocks:
+        clocks.stop()
+    seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)])
+    step_ms = seg.sum(1)
+    ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert _lib.moe_get_device_error() == 0, "device error word set"
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(d["x_bits"].view(np.int16)).pin_memory()
+        lh = torch.from_numpy(d["logits"]).pin_memory()
+        oh = torch.empty((T, s.H), dtype=torch.int16).pin_memory()
+        stage = {"x": torch.empty_like(x), "logits": torch.empty_like(logits), "out": torch.empty_like(out)}
+        for _ in range(max(1, args.warmup)):
+            layer.forward_host(xh, lh, oh, stage)
+        torch.cuda.synchronize()
+        ne = max(3, min(args.steps, 50))
+        t0 = time.perf_counter()
+        for _ in range(ne):
+            if flush is not None:
+                flush.zero_()
+            layer.forward_host(xh, lh, oh, stage)
+            torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        e2e_ms = (t1 - t0) * 1e3 / ne
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(xh.numel() * 2 + lh.numel() * 4),
+               "d2h_bytes_per_step": int(oh.numel() * 2), "ms_per_step": e2e_ms,
+               "note": "wall clock incl. pinned H2D of x+logits, layer, D2H of out, and a stream sync"}
+
+    # roofline of the dominant kernel (the gate/up GEMM)
+    gu_ms = float(seg[:, 1].mean())
+    dn_ms = float(seg[:, 2].mean())
+    peaks = load_peaks()
+    tensor_bound = T >= 2048
+    if tensor_bound:
+        achieved = work["flops_gate_up"] / (gu_ms * 1e-3) / 1e12
+        peak, unit, bound = peaks["bf16_tflops"], "TFLOP/s", "tensor"
+    else:
+        achieved = work["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
+        peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
+    roof = {"kernel": "gate/up grouped GEMM (moe_expert_gemm_w4, MOE_GATE_UP_SWIGLU)", "bound": bound,
+            "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "peak_source": peaks["source"], "traffic": None,
+            "algorithmic_per_launch": work["flops_gate_up"] if tensor_bound else work["gate_up_bytes"],
+            "launch_ms": gu_ms}
+
+    res = {
+        "metric": METRIC, "value": world * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x uint4 (fp32 accumulate)",
+        "data": "synthetic (seeded; random-init uint4 weights, bf16 scales/biases)",
+        "config": {"workload": wl.name, "desc": wl.desc, "T": T, "H": s.H, "E": s.E, "k": s.k, "F": s.F,
+                   "shared_experts": 1, "group": 64, "block_n": bn, "kernels": args.kernels,
+                   "touched_experts": touched,
+                   "l2": "L2 flushed between steps" if flush is not None else
+                   f"inputs larger than L2 ({work['step_bytes'] / 1e6:.0f} MB streamed per step)",
+                   "parallelism": f"replicas x{world} (tokens sharded, no collective)"},
+        "stages_ms": {"route": float(seg[:, 0].mean()), "gate_up": gu_ms, "down": dn_ms,
+                      "combine": float(seg[:, 3].mean())},
+        "hbm_GBps_step": work["step_bytes"] / (ms * 1e-3) / 1e9,
+        "tflops_step": work["step_flops"] / (ms * 1e-3) / 1e12,
+        "roofline": roof,
+        "gpu_launches": int(launches),
+        "e2e": e2e,
+    }
+    if clocks:
+        res["clocks"] = clocks.summary()
+    return res, d, layer
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle (reference arm and cpu_baseline)
+# --------------------------------------------------------------------------- #
+def oracle_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def time_oracle(d, n_tokens, budget_s=20.0):
+    """Time the float64 oracle on the first n_tokens of the workload (all their experts)."""
+    from oracle import moe_ref
+    wl = d["workload"]
+    T = wl.T
+    n = min(T, n_tokens)
+    toks = np.arange(n)
+    t0 = time.perf_counter()
+    moe_ref.moe_forward(d["x_bits"], d["logits"], d, wl.shape.k, tokens=toks)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": oracle_cores(), "kind": "oracle",
+            "sample": f"first {n} of the {T} tokens of {wl.name}, all their routed experts + the shared expert "
+                      f"dequantised and multiplied in float64 NumPy ({dt:.1f} s)", "seconds": dt}
+
+
+def oracle_sample_tokens(wl):
+    return {"tiny": 64, "decode1": 1, "decode8": 8, "prefill512": 16, "prefill4k": 16, "skew16k": 16}[wl.name]
+
+
+def run_reference(args):
+    wl = workloads.WORKLOADS[args.workload]
+    d = workloads.make_workload(wl, seed=0)
+    n = oracle_sample_tokens(wl)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(max(1, args.steps)):   # each step one bounded sample; stop after ~90 s of CPU work
+        vals.append(time_oracle(d, n))
+        if time.perf_counter() - t0 > 90.0:
+            break
+    wall = time.perf_counter() - t0
+    v = float(np.median([x["value"] for x in vals]))
+    cb = dict(vals[0])
+    cb["value"] = v
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+        "steps": len(vals), "warmup": 0, "ms_per_step": 1e3 * n / v, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "desc": wl.desc, "T": wl.T, "sample_tokens": n},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill512", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--kernels", default="auto", choices=["auto", "tc", "simt", "gemv"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res, d, layer = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = time_oracle(d, oracle_sample_tokens(d["workload"]))
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

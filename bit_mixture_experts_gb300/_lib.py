@@ -1,0 +1,170 @@
+"""ctypes binding of libmoe_w4.so: argument marshalling only.
+
+Every function here takes torch tensors (or plain ints), checks dtypes and
+shapes, passes raw pointers and the current CUDA stream to the C ABI of
+include/moe_w4.h, and raises MoeError on a non-zero status.  No arithmetic of
+the layer happens in Python; when the library is missing the import fails
+loudly instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe_w4.so")
+
+MOE_OK = 0
+ERRORS = {-1: "MOE_ERR_NULL", -2: "MOE_ERR_ALIGN", -3: "MOE_ERR_SHAPE", -4: "MOE_ERR_WORKSPACE",
+          -5: "MOE_ERR_CUDA", -6: "MOE_ERR_DEVICE", -7: "MOE_ERR_MODE"}
+DEVICE_ERRORS = {0: "ok", 1: "MOE_DEV_BAD_BLOCK", 2: "MOE_DEV_BAD_INDEX", 3: "MOE_DEV_TIMEOUT"}
+
+GATE_UP, DOWN = 0, 1
+IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_GEMV = 0, 1, 2, 3
+IMPLS = {"auto": IMPL_AUTO, "simt": IMPL_SIMT, "tc": IMPL_TC, "gemv": IMPL_GEMV}
+
+# Exported symbols of include/moe_w4.h (checked by the CPU tests).
+SYMBOLS = ["moe_version", "moe_launch_count", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
+           "moe_repacked_bytes", "moe_repack_w4", "moe_expert_gemm_w4", "moe_combine",
+           "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} returned {code} ({ERRORS.get(code, 'unknown')})")
+        self.code = code
+
+
+_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("w13", _vp), ("s13", _vp), ("b13", _vp), ("w2", _vp), ("s2", _vp), ("b2", _vp)]
+
+
+class Buffers(ctypes.Structure):
+    _fields_ = [("topk_ids", _vp), ("topk_w", _vp), ("counts", _vp), ("offsets", _vp), ("perm", _vp),
+                ("inv_perm", _vp), ("block_map", _vp), ("num_blocks", _vp), ("h", _vp), ("acc", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+_SIGS = {
+    "moe_version": ([], _i),
+    "moe_launch_count": ([], ctypes.c_uint64),
+    "moe_block_map_capacity": ([_i, _i, _i, _i], _i),
+    "moe_route_workspace_size": ([_i, _i, _i, _i], _sz),
+    "moe_route": ([_vp, _i, _i, _i, _i] + [_vp] * 9 + [_sz, _vp], _i),
+    "moe_repacked_bytes": ([_i, _i, _i], _sz),
+    "moe_repack_w4": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
+    "moe_expert_gemm_w4": ([_i, _i, _vp, _i, _i, _i, _i, _i] + [_vp] * 7 + [_i, _vp, _vp], _i),
+    "moe_combine": ([_vp, _vp, _i, _i, _vp], _i),
+    "moe_layer_forward": ([_vp, _vp, _vp] + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
+    "moe_layer_forward_host": ([_vp] * 6 + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
+    "moe_get_device_error": ([ctypes.POINTER(ctypes.c_int32)], _i),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise OSError(f"{path} is missing: build it with `python -m bit_mixture_experts_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def _call(name, *args):
+    rc = getattr(load(), name)(*args)
+    if rc != MOE_OK:
+        raise MoeError(name, rc)
+    return rc
+
+
+def _ptr(t):
+    """A tensor's data pointer, or a raw address given as an int."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# --------------------------------------------------------------------------- #
+# thin wrappers with the C names
+# --------------------------------------------------------------------------- #
+def moe_version() -> int:
+    return load().moe_version()
+
+
+def moe_launch_count() -> int:
+    return load().moe_launch_count()
+
+
+def moe_block_map_capacity(T, E, k, block_n) -> int:
+    return load().moe_block_map_capacity(T, E, k, block_n)
+
+
+def moe_route_workspace_size(T, E, k, block_n) -> int:
+    return load().moe_route_workspace_size(T, E, k, block_n)
+
+
+def moe_repacked_bytes(n_mat, rows, K) -> int:
+    return load().moe_repacked_bytes(n_mat, rows, K)
+
+
+def moe_route(logits, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks,
+              workspace, stream=None):
+    T, E = logits.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call("moe_route", _ptr(logits), T, E, k, block_n, _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets),
+          _ptr(perm), _ptr(inv_perm), _ptr(block_map), _ptr(num_blocks), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def moe_repack_w4(packed, scale, bias, gate_up, out, stream=None):
+    n_mat, rows, kw = packed.shape
+    _call("moe_repack_w4", _ptr(packed), _ptr(scale), _ptr(bias), n_mat, rows, kw * 8, int(gate_up), _ptr(out),
+          _stream(stream))
+
+
+def moe_expert_gemm_w4(mode, impl, act, T, H, F, E, k, w_packed, w_scale, w_bias, perm, topk_w, block_map,
+                       num_blocks, block_n, out, stream=None):
+    _call("moe_expert_gemm_w4", mode, impl, _ptr(act), T, H, F, E, k, _ptr(w_packed), _ptr(w_scale), _ptr(w_bias),
+          _ptr(perm), _ptr(topk_w), _ptr(block_map), _ptr(num_blocks), block_n, _ptr(out), _stream(stream))
+
+
+def moe_combine(acc, out, stream=None):
+    T, H = acc.shape
+    _call("moe_combine", _ptr(acc), _ptr(out), T, H, _stream(stream))
+
+
+def moe_layer_forward(x, logits, out, T, H, F, E, k, block_n, impl, weights: Weights, buffers: Buffers,
+                      stream=None):
+    _call("moe_layer_forward", _ptr(x), _ptr(logits), _ptr(out), T, H, F, E, k, block_n, impl,
+          ctypes.byref(weights), ctypes.byref(buffers), _stream(stream))
+
+
+def moe_layer_forward_host(x_host, logits_host, out_host, x_dev, logits_dev, out_dev, T, H, F, E, k, block_n, impl,
+                           weights: Weights, buffers: Buffers, stream=None):
+    _call("moe_layer_forward_host", _ptr(x_host), _ptr(logits_host), _ptr(out_host), _ptr(x_dev), _ptr(logits_dev),
+          _ptr(out_dev), T, H, F, E, k, block_n, impl, ctypes.byref(weights), ctypes.byref(buffers),
+          _stream(stream))
+
+
+def moe_get_device_error() -> int:
+    code = ctypes.c_int32(0)
+    _call("moe_get_device_error", ctypes.byref(code))
+    return code.value

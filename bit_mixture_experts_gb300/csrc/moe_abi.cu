@@ -1,0 +1,212 @@
+// extern "C" entry points of libmoe_w4.so: argument checks, the device error
+// word, and the launch sequence of the layer.  Every compute step runs in the
+// kernels of moe_route.cu, moe_gemm_simt.cu, moe_gemm_tc.cu and
+// moe_gemm_gemv.cu; nothing here touches tensor data on the host.
+#include <atomic>
+#include <mutex>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+__device__ int g_device_error = 0;
+
+// Per-device address of g_device_error, looked up once per device.
+int* device_error_ptr() {
+  static std::mutex mu;
+  static int* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+static std::atomic<uint64_t> g_launches{0};
+
+void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+// defined in the kernel files
+size_t route_workspace_bytes(int T, int E, int k);
+cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32_t* ids, float* w, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm, int32_t* nb, void* ws,
+                         cudaStream_t s);
+cudaError_t launch_gemm_simt(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const uint32_t* wq,
+                             const uint16_t* ws, const uint16_t* wb, const int32_t* perm, const float* topk_w,
+                             const int32_t* block_map, const int32_t* num_blocks, int bn, int nb_cap, void* out,
+                             cudaStream_t s);
+cudaError_t launch_combine(float* acc, uint16_t* out, int T, int H, int num_sms, cudaStream_t s);
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int T, int H, int F, int E, int k, int bn) {
+  if (T < 1 || T > (1 << 20)) return MOE_ERR_SHAPE;
+  if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return MOE_ERR_SHAPE;
+  if (H < 64 || H % 64 != 0 || F < 64 || F % 64 != 0) return MOE_ERR_SHAPE;
+  if (bn < 1 || bn > 1024) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+template <typename... P>
+int check_ptrs(P... ps) {
+  const void* arr[] = {static_cast<const void*>(ps)...};
+  for (const void* p : arr)
+    if (!p) return MOE_ERR_NULL;
+  for (const void* p : arr)
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return 0x000100; }
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_block_map_capacity(int T, int E, int k, int block_n) {
+  if (T < 1 || E < 1 || k < 1 || block_n < 1) return 0;
+  const long long A = static_cast<long long>(T) * k;
+  return static_cast<int>((A + block_n - 1) / block_n + E + (T + block_n - 1) / block_n);
+}
+
+size_t moe_route_workspace_size(int T, int E, int k, int block_n) {
+  (void)block_n;
+  if (T < 1 || E < 1 || k < 1) return 0;
+  return route_workspace_bytes(T, E, k);
+}
+
+int moe_route(const float* logits, int T, int E, int k, int block_n, int32_t* topk_ids, float* topk_w,
+              int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* block_map,
+              int32_t* num_blocks, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_shape(T, 64, 64, E, k, block_n);
+  if (rc) return rc;
+  rc = check_ptrs(logits, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks);
+  if (rc) return rc;
+  const size_t need = route_workspace_bytes(T, E, k);
+  if (need > 0) {
+    if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    rc = check_ptrs(workspace);
+    if (rc) return rc;
+  }
+  if (!device_error_ptr()) return MOE_ERR_CUDA;
+  return cuda_status(launch_route(logits, T, E, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm,
+                                  block_map, num_blocks, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,
+                       const void* w_packed, const uint16_t* w_scale, const uint16_t* w_bias, const int32_t* perm,
+                       const float* topk_w, const int32_t* block_map, const int32_t* num_blocks, int block_n,
+                       void* out, moe_stream_t stream) {
+  int rc = check_shape(T, H, F, E, k, block_n);
+  if (rc) return rc;
+  if (mode != MOE_GATE_UP_SWIGLU && mode != MOE_DOWN_COMBINE) return MOE_ERR_MODE;
+  rc = check_ptrs(act, w_packed, perm, topk_w, block_map, num_blocks, out);
+  if (rc) return rc;
+  if (!device_error_ptr()) return MOE_ERR_CUDA;
+  const int cap = moe_block_map_capacity(T, E, k, block_n);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (impl == MOE_IMPL_AUTO) impl = MOE_IMPL_SIMT;
+  switch (impl) {
+    case MOE_IMPL_SIMT:
+      if (block_n > 128) return MOE_ERR_SHAPE;
+      rc = check_ptrs(w_scale, w_bias);
+      if (rc) return rc;
+      return cuda_status(launch_gemm_simt(mode, act, T, H, F, E, k, static_cast<const uint32_t*>(w_packed), w_scale,
+                                          w_bias, perm, topk_w, block_map, num_blocks, block_n, cap, out, s));
+    default:
+      return MOE_ERR_MODE;
+  }
+}
+
+int moe_combine(float* acc, uint16_t* out, int T, int H, moe_stream_t stream) {
+  if (T < 1 || H < 64 || H % 64 != 0) return MOE_ERR_SHAPE;
+  int rc = check_ptrs(acc, out);
+  if (rc) return rc;
+  return cuda_status(launch_combine(acc, out, T, H, num_sms(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out, int T, int H, int F, int E, int k,
+                      int block_n, int impl, const moe_weights_t* w, const moe_buffers_t* b, moe_stream_t stream) {
+  if (!w || !b) return MOE_ERR_NULL;
+  int rc = moe_route(logits, T, E, k, block_n, b->topk_ids, b->topk_w, b->counts, b->offsets, b->perm, b->inv_perm,
+                     b->block_map, b->num_blocks, b->workspace, b->workspace_bytes, stream);
+  if (rc) return rc;
+  rc = moe_expert_gemm_w4(MOE_GATE_UP_SWIGLU, impl, x, T, H, F, E, k, w->w13, w->s13, w->b13, b->perm, b->topk_w,
+                          b->block_map, b->num_blocks, block_n, b->h, stream);
+  if (rc) return rc;
+  rc = moe_expert_gemm_w4(MOE_DOWN_COMBINE, impl, b->h, T, H, F, E, k, w->w2, w->s2, w->b2, b->perm, b->topk_w,
+                          b->block_map, b->num_blocks, block_n, b->acc, stream);
+  if (rc) return rc;
+  return moe_combine(b->acc, out, T, H, stream);
+}
+
+int moe_layer_forward_host(const uint16_t* x_host, const float* logits_host, uint16_t* out_host, uint16_t* x_dev,
+                           float* logits_dev, uint16_t* out_dev, int T, int H, int F, int E, int k, int block_n,
+                           int impl, const moe_weights_t* w, const moe_buffers_t* b, moe_stream_t stream) {
+  if (!x_host || !logits_host || !out_host) return MOE_ERR_NULL;
+  int rc = check_shape(T, H, F, E, k, block_n);
+  if (rc) return rc;
+  rc = check_ptrs(x_dev, logits_dev, out_dev);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t xb = static_cast<size_t>(T) * H * sizeof(uint16_t);
+  const size_t lb = static_cast<size_t>(T) * E * sizeof(float);
+  if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(logits_dev, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  rc = moe_layer_forward(x_dev, logits_dev, out_dev, T, H, F, E, k, block_n, impl, w, b, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_get_device_error(int32_t* code) {
+  if (!code) return MOE_ERR_NULL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = v;
+  return MOE_OK;
+}
+
+size_t moe_repacked_bytes(int n_mat, int rows, int K) {
+  (void)n_mat;
+  (void)rows;
+  (void)K;
+  return 0;
+}
+
+int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias, int n_mat, int rows, int K,
+                  int gate_up, void* out, moe_stream_t stream) {
+  (void)packed; (void)scale; (void)bias; (void)n_mat; (void)rows; (void)K; (void)gate_up; (void)out; (void)stream;
+  return MOE_ERR_MODE;
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+"""A W4 mixture-of-experts FFN layer driven through the C ABI.
+
+PyTorch only provides device memory and the stream; every step (routing,
+grouped GEMMs, combine) runs in libmoe_w4.so's kernels.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import _lib
+
+DEFAULT_BLOCK_N = {_lib.IMPL_SIMT: 128, _lib.IMPL_TC: 256, _lib.IMPL_GEMV: 256, _lib.IMPL_AUTO: 128}
+
+
+def _dev(a: np.ndarray, device):
+    """numpy -> torch on `device` keeping the bits (uint32 as int32, uint16 as int16)."""
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint32:
+        a = a.view(np.int32)
+    elif a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(device)
+
+
+class MoELayerW4:
+    """One layer: E routed experts (top-k) + 1 shared expert, hidden H, expert width F.
+
+    `weights` holds the canonical arrays of the workloads module (w13_packed,
+    w13_scale, w13_bias, w2_packed, w2_scale, w2_bias) as numpy arrays or torch
+    tensors already on the device.
+    """
+
+    def __init__(self, H, E, k, F, weights: dict, device="cuda", impl="auto", block_n=None):
+        import torch
+        self.H, self.E, self.k, self.F = H, E, k, F
+        self.device = torch.device(device)
+        self.impl = _lib.IMPLS[impl] if isinstance(impl, str) else int(impl)
+        self.block_n = block_n or DEFAULT_BLOCK_N[self.impl]
+        _lib.load()
+        w = {n: (v if isinstance(v, torch.Tensor) else _dev(v, self.device)) for n, v in weights.items()
+             if n.startswith(("w13_", "w2_"))}
+        self.canonical = w
+        if self.impl in (_lib.IMPL_SIMT, _lib.IMPL_AUTO):
+            self.weights = _lib.Weights(w["w13_packed"].data_ptr(), w["w13_scale"].data_ptr(),
+                                        w["w13_bias"].data_ptr(), w["w2_packed"].data_ptr(),
+                                        w["w2_scale"].data_ptr(), w["w2_bias"].data_ptr())
+            self._keep = w
+        else:
+            self.w13_r = self._repack(w["w13_packed"], w["w13_scale"], w["w13_bias"], gate_up=True)
+            self.w2_r = self._repack(w["w2_packed"], w["w2_scale"], w["w2_bias"], gate_up=False)
+            self.weights = _lib.Weights(self.w13_r.data_ptr(), None, None, self.w2_r.data_ptr(), None, None)
+        self._bufs = {}
+
+    def _repack(self, packed, scale, bias, gate_up):
+        import torch
+        n_mat, rows, kw = packed.shape
+        nbytes = _lib.moe_repacked_bytes(n_mat, rows, kw * 8)
+        out = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        _lib.moe_repack_w4(packed, scale, bias, gate_up, out)
+        return out
+
+    def buffers(self, T):
+        """Routing / intermediate buffers for T tokens (allocated once per T)."""
+        import torch
+        if T in self._bufs:
+            return self._bufs[T]
+        E, k, H, F, bn = self.E, self.k, self.H, self.F, self.block_n
+        A = T * k
+        dev = self.device
+        cap = _lib.moe_block_map_capacity(T, E, k, bn)
+        wsb = _lib.moe_route_workspace_size(T, E, k, bn)
+        t = {
+            "topk_ids": torch.empty((T, k), dtype=torch.int32, device=dev),
+            "topk_w": torch.empty((T, k), dtype=torch.float32, device=dev),
+            "counts": torch.empty(E, dtype=torch.int32, device=dev),
+            "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+            "perm": torch.empty(A, dtype=torch.int32, device=dev),
+            "inv_perm": torch.empty(A, dtype=torch.int32, device=dev),
+            "block_map": torch.empty((cap, 3), dtype=torch.int32, device=dev),
+            "num_blocks": torch.empty(1, dtype=torch.int32, device=dev),
+            "h": torch.empty((A + T, F), dtype=torch.bfloat16, device=dev),
+            "acc": torch.zeros((T, H), dtype=torch.float32, device=dev),
+            "workspace": torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev),
+        }
+        t["struct"] = _lib.Buffers(*(t[n].data_ptr() for n in ("topk_ids", "topk_w", "counts", "offsets", "perm",
+                                                                 "inv_perm", "block_map", "num_blocks", "h", "acc",
+                                                                 "workspace")), wsb)
+        self._bufs[T] = t
+        return t
+
+    def forward(self, x, logits, out=None, stream=None):
+        """x bf16 [T, H], logits fp32 [T, E] on the device -> out bf16 [T, H]."""
+        import torch
+        T = x.shape[0]
+        assert x.dtype == torch.bfloat16 and x.shape == (T, self.H) and x.is_contiguous()
+        assert logits.dtype == torch.float32 and logits.shape == (T, self.E) and logits.is_contiguous()
+        b = self.buffers(T)
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device)
+        _lib.moe_layer_forward(x, logits, out, T, self.H, self.F, self.E, self.k, self.block_n, self.impl,
+                               self.weights, b["struct"], stream)
+        return out
+
+    def forward_host(self, x_host, logits_host, out_host, stage, stream=None):
+        """Host (pinned) x, logits, out; `stage` holds device x, logits, out of the same shapes."""
+        T = x_host.shape[0]
+        b = self.buffers(T)
+        _lib.moe_layer_forward_host(x_host, logits_host, out_host, stage["x"], stage["logits"], stage["out"], T,
+                                    self.H, self.F, self.E, self.k, self.block_n, self.impl, self.weights,
+                                    b["struct"], stream)

@@ -1,0 +1,255 @@
+/*
+ * moe_w4.h -- C ABI of libmoe_w4.so: the prefill/decode forward of a
+ * mixture-of-experts FFN layer with groupwise-affine 4-bit expert weights and
+ * GPU-resident routing, for NVIDIA GB300 (sm_103a).
+ *
+ * The layer follows "Perplexity Open Sources Lily" (aitrending.vip),
+ * Technical Details: Model bullet (a router choosing 8 of 256 experts plus one
+ * shared expert) and Prefill optimizations bullet (4-bit groupwise affine
+ * weights, 64 weights per group, dequantised inside the grouped GEMM with FP32
+ * accumulation; routing histogram, prefix scan, scatter and block map kept on
+ * the GPU with no CPU synchronisation).  The Chinese section of the same page
+ * ("预填充优化") adds that each group of 64 weights shares a bfloat16 scale.
+ *
+ * Conventions for every call:
+ *  - Pointers named *_host are host pointers; every other pointer is a device
+ *    pointer owned by the caller.  The library allocates nothing.
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - All tensors are dense row-major.  Device pointers must be 16-byte aligned.
+ *  - Calls enqueue work on `stream` and return at once; no call synchronises
+ *    the host except moe_get_device_error.
+ *  - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  Argument errors
+ *    are detected on the host before anything is enqueued.  Faults found by a
+ *    kernel (a corrupt block map, an out-of-range index) are recorded in a
+ *    device error word instead of trapping; read it with moe_get_device_error.
+ *  - Behaviour for NaN or infinite logits is undefined.
+ *
+ * Sizes: T tokens, H hidden, E routed experts (the shared expert is index E of
+ * every weight array), k experts per token, F expert FFN width, A = T*k
+ * assignments, block_n rows per GEMM tile.  Limits: 1 <= k <= 32, k <= E,
+ * E <= 1024, H % 64 == 0, F % 64 == 0, 1 <= T <= 2^20.
+ */
+#ifndef MOE_W4_H
+#define MOE_W4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = -1,      /* a required pointer is NULL */
+  MOE_ERR_ALIGN = -2,     /* a device pointer is not 16-byte aligned */
+  MOE_ERR_SHAPE = -3,     /* sizes outside the limits above */
+  MOE_ERR_WORKSPACE = -4, /* workspace smaller than moe_route_workspace_size() */
+  MOE_ERR_CUDA = -5,      /* a CUDA launch or copy failed */
+  MOE_ERR_DEVICE = -6,    /* moe_get_device_error found a kernel-side fault */
+  MOE_ERR_MODE = -7       /* unknown mode or variant */
+};
+
+/* Device error word values (written by kernels, read by moe_get_device_error). */
+enum {
+  MOE_DEV_OK = 0,
+  MOE_DEV_BAD_BLOCK = 1,  /* a block-map entry outside [0, E] x [0, A+T) */
+  MOE_DEV_BAD_INDEX = 2,  /* a permutation entry outside [0, A) */
+  MOE_DEV_TIMEOUT = 3     /* a bounded device wait ran out */
+};
+
+/* GEMM modes. */
+enum {
+  MOE_GATE_UP_SWIGLU = 0, /* h = bf16(silu(x Wg^T) * (x Wu^T)) per routed row */
+  MOE_DOWN_COMBINE = 1    /* acc[t] += w * (h Wd^T), FP32 */
+};
+
+/* GEMM implementations. */
+enum {
+  MOE_IMPL_AUTO = 0,      /* tensor-core kernel for prefill, GEMV kernel for T <= 8 */
+  MOE_IMPL_SIMT = 1,      /* CUDA-core tiled kernel (canonical weight layout) */
+  MOE_IMPL_TC = 2,        /* tcgen05 kernel (repacked weight layout) */
+  MOE_IMPL_GEMV = 3       /* CUDA-core decode kernel (repacked weight layout) */
+};
+
+/* ------------------------------------------------------------------------ */
+/* Routing                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Rows of the block map that moe_route may write: ceil(A/block_n) + E + ceil(T/block_n). */
+int moe_block_map_capacity(int T, int E, int k, int block_n);
+
+/* Bytes of scratch moe_route needs (per-chunk expert counts). */
+size_t moe_route_workspace_size(int T, int E, int k, int block_n);
+
+/*
+ * moe_route -- router softmax + top-k and GPU-resident routing
+ * ("Perplexity Open Sources Lily", Technical Details, Model and Prefill
+ * optimizations bullets).
+ *
+ * logits     float32 [T, E]   router logits (read only)
+ * topk_ids   int32  [T, k]    chosen experts, by descending logit; equal
+ *                             logits go to the lower index (-0.0 == +0.0)
+ * topk_w     float32 [T, k]   exp(l_j - l_max) / sum over the k chosen
+ *                             (the softmax renormalised over the top k)
+ * counts     int32  [E]       histogram of the T*k assignments over experts
+ * offsets    int32  [E+1]     exclusive prefix scan of counts; offsets[E] = A
+ * perm       int32  [A]       assignment a = t*k + j at sorted position p,
+ *                             sorted by (expert, a): perm[p] = a
+ * inv_perm   int32  [A]       inv_perm[perm[p]] = p
+ * block_map  int32  [cap, 3]  tiles (expert, first row, rows) for every expert
+ *                             in ascending order, block_n rows per tile, then
+ *                             the shared expert (index E) over rows A..A+T-1
+ *                             (row A+t is token t); only the first
+ *                             *num_blocks rows are written
+ * num_blocks int32  [1]       number of tiles (device memory)
+ * workspace  device scratch of at least moe_route_workspace_size() bytes.
+ * block_n    1..1024.
+ */
+int moe_route(const float* logits, int T, int E, int k, int block_n,
+              int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
+              int32_t* perm, int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks,
+              void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Weights                                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Canonical weight layout (what moe_repack_w4 reads and the SIMT kernel uses):
+ *   packed uint32 [n_mat, rows, K/8]: K element 8*w+i in bits [4i, 4i+4) of word w
+ *   scale, bias   bf16   [n_mat, rows, K/64]: w = bf16(q * scale + bias)
+ * Gate/up matrices have rows = 2F (F gate rows, then F up rows) and K = H;
+ * down matrices have rows = H and K = F.  n_mat = E + 1, shared expert last.
+ */
+
+/* Bytes of the repacked layout for n_mat matrices of rows x K. */
+size_t moe_repacked_bytes(int n_mat, int rows, int K);
+
+/*
+ * moe_repack_w4 -- one-time conversion of canonical weights into the layout
+ * the tensor-core and GEMV kernels stream: per matrix, per 128-row tile, per
+ * 64-wide K group, one 4 KiB block of packed nibbles (rows laid out so that a
+ * 128-byte swizzle makes the per-row reads bank-conflict free) followed by the
+ * rows' (scale, bias) pairs.  `gate_up` = 1 interleaves gate and up rows in
+ * groups of 16 so that one tile holds 64 matching gate/up features.  Not part
+ * of the layer's timed work.  rows % 128 == 0 and K % 64 == 0.
+ */
+int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias,
+                  int n_mat, int rows, int K, int gate_up, void* out, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped expert GEMM                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * moe_expert_gemm_w4 -- grouped SwiGLU expert GEMM over 4-bit groupwise-affine
+ * weights with the dequantisation fused into the GEMM and FP32 accumulation
+ * ("Perplexity Open Sources Lily", Technical Details, Prefill optimizations
+ * bullet; itinai.com post on the Lily engine, paragraph 2: weights are expanded
+ * only on chip, never as a full bf16 copy in memory).
+ *
+ * mode MOE_GATE_UP_SWIGLU:
+ *   act  bf16 [T, H] tokens; row r of tile (e, r0, n) reads token perm[r]/k
+ *        for r < A and token r-A for r >= A (shared expert);
+ *   out  bf16 [A+T, F]: h[r] = bf16(silu(g) * u), g/u the gate/up projections
+ *        accumulated in FP32 over the bf16-expanded weights.
+ * mode MOE_DOWN_COMBINE:
+ *   act  bf16 [A+T, F] the h of the gate/up call;
+ *   out  float32 [T, H] accumulator: acc[token(r)] += w(r) * (h[r] Wd^T), with
+ *        w(r) = topk_w[perm[r]] for r < A and 1 for the shared expert.  acc
+ *        must be zero on entry (moe_combine leaves it zero).  The order of the
+ *        FP32 additions is not fixed.
+ * weights: canonical layout for MOE_IMPL_SIMT, repacked layout otherwise.
+ * block_map / num_blocks: moe_route's outputs for the same block_n.
+ * impl: MOE_IMPL_* (AUTO picks by T).  The TC kernel needs block_n <= 256
+ * and a multiple of 16; SIMT needs block_n <= 128.
+ */
+int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,
+                       const void* w_packed, const uint16_t* w_scale, const uint16_t* w_bias,
+                       const int32_t* perm, const float* topk_w,
+                       const int32_t* block_map, const int32_t* num_blocks, int block_n,
+                       void* out, moe_stream_t stream);
+
+/*
+ * moe_combine -- finish the weighted combine back to token order:
+ * out[t, c] = bf16(acc[t, c]) (round to nearest even), then acc[t, c] = 0 so
+ * the accumulator is ready for the next layer call.
+ */
+int moe_combine(float* acc, uint16_t* out, int T, int H, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Whole layer                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Device buffers of one layer call (all caller-owned; sizes for T, E, k, block_n). */
+typedef struct {
+  int32_t* topk_ids;   /* [T,k] */
+  float* topk_w;       /* [T,k] */
+  int32_t* counts;     /* [E] */
+  int32_t* offsets;    /* [E+1] */
+  int32_t* perm;       /* [A] */
+  int32_t* inv_perm;   /* [A] */
+  int32_t* block_map;  /* [moe_block_map_capacity, 3] */
+  int32_t* num_blocks; /* [1] */
+  uint16_t* h;         /* bf16 [A+T, F] */
+  float* acc;          /* [T, H], zero on the first call; left zero by every call */
+  void* workspace;     /* moe_route_workspace_size bytes */
+  size_t workspace_bytes;
+} moe_buffers_t;
+
+/* Weights of one layer: gate/up and down matrices of E+1 experts. */
+typedef struct {
+  const void* w13;        /* packed (canonical or repacked, matching impl) */
+  const uint16_t* s13;    /* canonical scale (SIMT only, else NULL) */
+  const uint16_t* b13;    /* canonical bias (SIMT only, else NULL) */
+  const void* w2;
+  const uint16_t* s2;
+  const uint16_t* b2;
+} moe_weights_t;
+
+/*
+ * moe_layer_forward -- the whole hot path on one stream with no host sync:
+ * moe_route, gate/up GEMM, down GEMM, moe_combine.  x bf16 [T,H], logits
+ * float32 [T,E], out bf16 [T,H] are device pointers.
+ */
+int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out,
+                      int T, int H, int F, int E, int k, int block_n, int impl,
+                      const moe_weights_t* weights, const moe_buffers_t* buffers,
+                      moe_stream_t stream);
+
+/*
+ * moe_layer_forward_host -- the same with x_host, logits_host and out_host in
+ * host memory (pinned for asynchronous copies): copies the inputs to the
+ * device staging buffers x_dev / logits_dev, runs the layer into out_dev and
+ * copies the result back, all on `stream`.  Returns after enqueueing; the
+ * caller synchronises the stream before reading out_host.
+ */
+int moe_layer_forward_host(const uint16_t* x_host, const float* logits_host, uint16_t* out_host,
+                           uint16_t* x_dev, float* logits_dev, uint16_t* out_dev,
+                           int T, int H, int F, int E, int k, int block_n, int impl,
+                           const moe_weights_t* weights, const moe_buffers_t* buffers,
+                           moe_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronises the current device, returns the device error word in *code and
+ * clears it.  Returns MOE_ERR_CUDA if the synchronisation itself failed. */
+int moe_get_device_error(int32_t* code);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int moe_version(void);
+
+/* Number of kernels this process has launched through the library so far
+ * (all devices).  Used to count launches inside a timed region. */
+uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_W4_H */

@@ -1,0 +1,86 @@
+"""The C-ABI library on the CPU: it loads, exports every entry point that
+include/moe_w4.h declares, and its host-only paths (sizes, argument checks
+that fail before any CUDA call) behave as documented.  No compute runs."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from oracle import moe_ref
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_mixture_experts_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    from bit_mixture_experts_gb300 import _lib
+    decl = declared_symbols()
+    assert len(decl) >= 11
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert set(decl) == set(_lib.SYMBOLS)
+
+
+def test_version(lib):
+    assert lib.moe_version() == 0x000100
+
+
+@pytest.mark.parametrize("T,E,k,bn", [(1, 16, 2, 128), (512, 256, 8, 128), (4096, 256, 8, 256), (7, 3, 3, 2)])
+def test_block_map_capacity_matches_oracle(lib, T, E, k, bn):
+    assert lib.moe_block_map_capacity(T, E, k, bn) == moe_ref.block_map_capacity(T, E, k, bn)
+
+
+def test_workspace_size(lib):
+    assert lib.moe_route_workspace_size(1, 256, 8, 128) == 0          # single-CTA path needs none
+    assert lib.moe_route_workspace_size(4096, 256, 8, 128) > 0
+    assert lib.moe_route_workspace_size(4096, 256, 8, 128) % 16 == 0
+
+
+def _route(lib, T=8, E=16, k=2, bn=128, ptr=16, ws=0):
+    p = ctypes.c_void_p(ptr) if ptr is not None else None
+    return lib.moe_route(p, T, E, k, bn, p, p, p, p, p, p, p, p, p, ws, None)
+
+
+def test_route_argument_errors(lib):
+    assert _route(lib, T=0) == -3
+    assert _route(lib, k=17, E=16) == -3
+    assert _route(lib, k=33, E=64) == -3
+    assert _route(lib, E=1025) == -3
+    assert _route(lib, bn=0) == -3
+    assert _route(lib, ptr=None) == -1
+    assert _route(lib, ptr=8) == -2
+    assert _route(lib, T=4096, E=256, k=8, ptr=16, ws=0) == -4
+
+
+def test_gemm_argument_errors(lib):
+    p = ctypes.c_void_p(256)
+    args = lambda mode, impl, H, F, bn, ptr=p: lib.moe_expert_gemm_w4(
+        mode, impl, ptr, 16, H, F, 8, 2, ptr, ptr, ptr, ptr, ptr, ptr, ptr, bn, ptr, None)
+    assert args(0, 1, 100, 64, 128) == -3       # H % 64
+    assert args(0, 1, 128, 96, 128) == -3       # F % 64
+    assert args(5, 1, 128, 64, 128) == -7       # mode
+    assert args(0, 1, 128, 64, 128, ptr=None) == -1
+    assert args(0, 1, 128, 64, 128, ptr=ctypes.c_void_p(260)) == -2
+
+
+def test_combine_argument_errors(lib):
+    assert lib.moe_combine(ctypes.c_void_p(16), ctypes.c_void_p(16), 4, 100, None) == -3
+    assert lib.moe_combine(None, ctypes.c_void_p(16), 4, 128, None) == -1
+    assert lib.moe_combine(ctypes.c_void_p(20), ctypes.c_void_p(16), 4, 128, None) == -2
