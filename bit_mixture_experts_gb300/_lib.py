@@ -26,7 +26,7 @@ IMPLS = {"auto": IMPL_AUTO, "simt": IMPL_SIMT, "tc": IMPL_TC, "gemv": IMPL_GEMV}
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
 SYMBOLS = ["moe_version", "moe_launch_count", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
            "moe_repacked_bytes", "moe_repack_w4", "moe_expert_gemm_w4", "moe_combine",
-           "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error"]
+           "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns"]
 
 
 class MoeError(RuntimeError):
@@ -61,6 +61,7 @@ _SIGS = {
     "moe_layer_forward": ([_vp, _vp, _vp] + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
     "moe_layer_forward_host": ([_vp] * 6 + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
     "moe_get_device_error": ([ctypes.POINTER(ctypes.c_int32)], _i),
+    "moe_set_wait_limit_ns": ([ctypes.c_uint64], None),
 }
 
 _lib = None
@@ -162,6 +163,10 @@ def moe_layer_forward_host(x_host, logits_host, out_host, x_dev, logits_dev, out
     _call("moe_layer_forward_host", _ptr(x_host), _ptr(logits_host), _ptr(out_host), _ptr(x_dev), _ptr(logits_dev),
           _ptr(out_dev), T, H, F, E, k, block_n, impl, ctypes.byref(weights), ctypes.byref(buffers),
           _stream(stream))
+
+
+def moe_set_wait_limit_ns(ns: int) -> None:
+    load().moe_set_wait_limit_ns(int(ns))
 
 
 def moe_get_device_error() -> int:

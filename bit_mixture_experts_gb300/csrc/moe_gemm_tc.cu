@@ -1,0 +1,535 @@
+// Tensor-core grouped expert GEMM over groupwise-affine 4-bit weights for
+// sm_103a (tcgen05 + TMEM), with the dequantisation fused into the GEMM.
+//
+// "Perplexity Open Sources Lily" (aitrending.vip), Technical Details,
+// Prefill optimizations bullet: 4-bit weights in groups of 64 are expanded
+// inside the grouped GEMM and accumulated in FP32; the itinai.com post on the
+// same engine (paragraph 2) adds that the expanded bf16 weights never exist as
+// a full copy in memory.  The pages' Metal kernel expands them in threadgroup
+// memory with 32-row tiles and four simdgroups; on GB300 the expanded tile goes
+// to tensor memory instead, where the MMA reads it directly, so shared-memory
+// bandwidth is left to the activations:
+//
+//   D[m, n] = sum_k W[m, k] * X[n, k]      (swap-AB: weight rows on M, tokens on N)
+//
+//   M = 128 weight rows of one expert (one "M-tile"), N = the tile's token
+//   rows rounded up to 16 (<= 256), K stepped 64 at a time (one quant group).
+//
+// Roles (512 threads, one CTA per SM, persistent over (block-map tile, M-tile)):
+//   warp 0      bulk-copies the packed 4-bit block of each K step into smem
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (A from TMEM, B from smem)
+//   warps 2-3   gather the tile's token rows with cp.async into 128B-swizzled smem
+//   warps 4-11  two dequant warpgroups (alternate K steps): nibbles -> bf16
+//               w = bf16(q*scale + bias) with one fma.rn.bf16x2 per pair,
+//               written to TMEM with tcgen05.st
+//   warps 12-15 epilogue: tcgen05.ld of the FP32 accumulators, then
+//               gate/up: h = bf16(silu(g) * u) stored to h[row, f]
+//               down:    acc[token] += w * y with FP32 reductions
+//
+// Every mbarrier wait is bounded by a time limit; on expiry the kernel records
+// MOE_DEV_TIMEOUT in the device error word, every role leaves its loop, copies
+// in flight are drained, TMEM is freed and the kernel returns.
+#include "moe_common.cuh"
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int TC_M = 128;           // weight rows per M-tile
+constexpr int KG = 64;              // K per pipeline stage (= one quant group)
+constexpr int NST = 4;              // pipeline stages
+constexpr int NMAX = 256;           // max token rows per tile
+constexpr int B_STAGE = NMAX * 128; // bytes of one activation stage (rows x 64 bf16)
+constexpr int W_PACKED = TC_M * 32; // packed nibbles of one M-tile x K group
+constexpr int W_STAGE = W_PACKED + TC_M * 4;  // + (scale, bias) per row
+constexpr int TMEM_COLS = 512;
+constexpr int TMEM_A0 = 256;        // first TMEM column of the A stages (D uses 0..255)
+constexpr int NTHREADS = 512;
+constexpr int GATHER_T = 64;        // threads of the gather warps
+constexpr int LAG = 2;              // cp.async groups kept in flight per gather thread
+
+// smem layout (offsets from a 1024-byte aligned base)
+constexpr int OFF_B = 0;
+constexpr int OFF_W = OFF_B + NST * B_STAGE;
+constexpr int OFF_BAR = OFF_W + NST * W_STAGE;
+constexpr int NBAR = 5 * NST + 3;
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+
+static_assert(OFF_W % 1024 == 0, "B stages must stay 1024-byte aligned");
+static_assert(W_STAGE % 16 == 0, "bulk copies move multiples of 16 bytes");
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t wfull(int s) const { return base + 8 * s; }
+  __device__ uint32_t wempty(int s) const { return base + 8 * (NST + s); }
+  __device__ uint32_t afull(int s) const { return base + 8 * (2 * NST + s); }
+  __device__ uint32_t bfull(int s) const { return base + 8 * (3 * NST + s); }
+  __device__ uint32_t empty(int s) const { return base + 8 * (4 * NST + s); }
+  __device__ uint32_t dfull() const { return base + 8 * (5 * NST); }
+  __device__ uint32_t dempty() const { return base + 8 * (5 * NST + 1); }
+  __device__ uint32_t fin() const { return base + 8 * (5 * NST + 2); }
+};
+
+struct TcParams {
+  const uint16_t* act;
+  const uint8_t* w;
+  const int32_t* perm;
+  const float* topk_w;
+  const int32_t* block_map;
+  const int32_t* num_blocks;
+  void* out;
+  int* err;
+  unsigned long long wait_ns;
+  int T, H, F, E, k, bn, cap;
+};
+
+// Bounded wait on phase `parity` of `bar`.  Returns false on timeout or when
+// another role has already given up (s_abort).  Warp-uniform when called by
+// all lanes of a warp (the decision uses lane 0's clock).
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
+                                          unsigned long long limit) {
+  const unsigned long long t0 = ptx::globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    const bool done = ptx::mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    if ((i & 15) == 15) {
+      int give_up = *s_abort;
+      if (!give_up && ptx::globaltimer() - t0 > limit) give_up = 2;
+      give_up = __shfl_sync(0xffffffffu, give_up, 0);
+      if (give_up) {
+        if (give_up == 2 && (threadIdx.x & 31) == 0) {
+          set_device_error(err, MOE_DEV_TIMEOUT);
+          *s_abort = 1;
+        }
+        return false;
+      }
+    }
+  }
+}
+
+// Single-thread variant.
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
+                                         unsigned long long limit) {
+  const unsigned long long t0 = ptx::globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 15) == 15) {
+      if (*s_abort) return false;
+      if (ptx::globaltimer() - t0 > limit) {
+        set_device_error(err, MOE_DEV_TIMEOUT);
+        *s_abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Wait that ignores s_abort (used to drain copies already in flight).
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
+  const unsigned long long t0 = ptx::globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer() - t0 > limit) return;
+  }
+}
+
+// Block-map entry of unit u; false for a malformed entry (the same decision
+// in every role, so all roles skip it together).
+__device__ __forceinline__ bool unit_tile(const TcParams& p, int u, int MT, Tile* t, int* mt) {
+  const int b = u / MT;
+  *mt = u - b * MT;
+  t->expert = __ldg(p.block_map + 3 * b);
+  t->row0 = __ldg(p.block_map + 3 * b + 1);
+  t->rows = __ldg(p.block_map + 3 * b + 2);
+  const int A = p.T * p.k;
+  bool ok = t->expert >= 0 && t->expert <= p.E && t->rows >= 1 && t->rows <= p.bn && t->row0 >= 0;
+  if (ok) ok = t->expert < p.E ? (t->row0 + t->rows <= A) : (t->row0 >= A && t->row0 + t->rows <= A + p.T);
+  return ok;
+}
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+}  // namespace
+
+template <int MODE>
+__global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const Bars bars{sbase + OFF_BAR};
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = MODE == 0 ? p.H : p.F;
+  const int KT = K / KG;
+  const int MT = MODE == 0 ? (2 * p.F) / TC_M : p.H / TC_M;
+  const int A = p.T * p.k;
+  int nb = __ldg(p.num_blocks);
+  if (nb < 0 || nb > p.cap) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(p.err, MOE_DEV_BAD_BLOCK);
+    nb = nb < 0 ? 0 : p.cap;
+  }
+  const int units = nb * MT;
+
+  if (threadIdx.x == 0) {
+    *s_abort = 0;
+    for (int s = 0; s < NST; ++s) {
+      ptx::mbar_init(bars.wfull(s), 1);
+      ptx::mbar_init(bars.wempty(s), 4);
+      ptx::mbar_init(bars.afull(s), 4);
+      ptx::mbar_init(bars.bfull(s), GATHER_T);
+      ptx::mbar_init(bars.empty(s), 1);
+    }
+    ptx::mbar_init(bars.dfull(), 1);
+    ptx::mbar_init(bars.dempty(), 4);
+    ptx::mbar_init(bars.fin(), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(s_tmem), TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const unsigned long long lim = p.wait_ns;
+  int prod_it = 0;  // bulk copies issued by the producer (warp 0, lane 0)
+
+  if (warp == 0) {
+    // ------------------------------------------------ packed-weight producer
+    if (lane == 0) {
+      int& it = prod_it;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        Tile t;
+        int mt;
+        if (!unit_tile(p, u, MT, &t, &mt)) continue;
+        const uint8_t* src = p.w + (static_cast<size_t>(t.expert) * MT + mt) * KT * static_cast<size_t>(W_STAGE);
+        for (int kg = 0; kg < KT; ++kg, ++it) {
+          const int s = it % NST, r = it / NST;
+          if (r > 0 && !wait_one(bars.wempty(s), (r - 1) & 1, s_abort, p.err, lim)) goto producer_done;
+          ptx::mbar_arrive_expect_tx(bars.wfull(s), W_STAGE);
+          ptx::bulk_g2s(sbase + OFF_W + s * W_STAGE, src + static_cast<size_t>(kg) * W_STAGE, W_STAGE,
+                        bars.wfull(s));
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int it = 0, ui = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        Tile t;
+        int mt;
+        if (!unit_tile(p, u, MT, &t, &mt)) continue;
+        const uint32_t idesc = ptx::idesc_bf16_f32(TC_M, round16(t.rows));
+        if (ui > 0 && !wait_one(bars.dempty(), (ui - 1) & 1, s_abort, p.err, lim)) goto mma_done;
+        ptx::tc_fence_after();
+        for (int kg = 0; kg < KT; ++kg, ++it) {
+          const int s = it % NST, r = it / NST;
+          if (!wait_one(bars.afull(s), r & 1, s_abort, p.err, lim)) goto mma_done;
+          if (!wait_one(bars.bfull(s), r & 1, s_abort, p.err, lim)) goto mma_done;
+          ptx::tc_fence_after();
+          const uint32_t a_tmem = tmem + TMEM_A0 + 32 * s;
+          const uint64_t bdesc = ptx::smem_desc_sw128(sbase + OFF_B + s * B_STAGE);
+#pragma unroll
+          for (int j = 0; j < KG / 16; ++j)
+            ptx::mma_ts(tmem, a_tmem + 8 * j, bdesc + 2 * j, idesc, (kg | j) != 0);
+          ptx::mma_commit(bars.empty(s));
+        }
+        ptx::mma_commit(bars.dfull());
+        ++ui;
+      }
+    mma_done:
+      ptx::mma_commit(bars.fin());
+      wait_drain(bars.fin(), 0, lim);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------ activation gather
+    const int gt = threadIdx.x - 64;  // 0..63
+    const int chunk = gt & 7, row_a = gt >> 3;
+    int it = 0;
+    bool aborted = false;
+    for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
+      Tile t;
+      int mt;
+      if (!unit_tile(p, u, MT, &t, &mt)) continue;
+      // this thread's rows: i = row_a + 8*j
+      int src_row[NMAX / 8];
+#pragma unroll
+      for (int j = 0; j < NMAX / 8; ++j) {
+        const int i = row_a + 8 * j;
+        int sr = -1;
+        if (i < t.rows) {
+          const int r = t.row0 + i;
+          if (MODE == 0) {
+            if (r < A) {
+              const int a = __ldg(p.perm + r);
+              if (a >= 0 && a < A) sr = a / p.k;
+              else set_device_error(p.err, MOE_DEV_BAD_INDEX);
+            } else {
+              sr = r - A;
+            }
+          } else {
+            sr = r;
+          }
+        }
+        src_row[j] = sr;
+      }
+      for (int kg = 0; kg < KT; ++kg, ++it) {
+        const int s = it % NST, r = it / NST;
+        if (r > 0 && !wait_warp(bars.empty(s), (r - 1) & 1, s_abort, p.err, lim)) {
+          aborted = true;
+          break;
+        }
+        const uint32_t dst0 = sbase + OFF_B + s * B_STAGE;
+#pragma unroll
+        for (int j = 0; j < NMAX / 8; ++j) {
+          const int i = row_a + 8 * j;
+          if (src_row[j] >= 0) {
+            const uint16_t* src = p.act + static_cast<size_t>(src_row[j]) * K + kg * KG + chunk * 8;
+            const uint32_t dst = dst0 + (i >> 3) * 1024 + (i & 7) * 128 + ((chunk ^ (i & 7)) << 4);
+            ptx::cp_async_16(dst, src);
+          }
+        }
+        ptx::cp_async_commit();
+        if (it >= LAG) {
+          ptx::cp_async_wait<LAG>();
+          ptx::fence_proxy_async_smem();
+          ptx::mbar_arrive(bars.bfull((it - LAG) % NST));
+        }
+      }
+    }
+    ptx::cp_async_wait_all();
+    if (!aborted && !*s_abort) {
+      ptx::fence_proxy_async_smem();
+      for (int t = it - LAG < 0 ? 0 : it - LAG; t < it; ++t) ptx::mbar_arrive(bars.bfull(t % NST));
+    }
+  } else if (warp < 12) {
+    // ------------------------------------------------ dequant (two warpgroups)
+    const int wg = (warp - 4) >> 2;
+    const int q = warp & 3;
+    const int L = 32 * q + lane;  // weight row within the M-tile = TMEM lane
+    int it = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      Tile t;
+      int mt;
+      if (!unit_tile(p, u, MT, &t, &mt)) continue;
+      for (int kg = 0; kg < KT; ++kg, ++it) {
+        if ((it & 1) != wg) continue;
+        const int s = it % NST, r = it / NST;
+        if (!wait_warp(bars.wfull(s), r & 1, s_abort, p.err, lim)) goto dequant_done;
+        const uint8_t* ws = smem + OFF_W + s * W_STAGE;
+        const uint4 p0 = *reinterpret_cast<const uint4*>(ws + L * 16);
+        const uint4 p1 = *reinterpret_cast<const uint4*>(ws + 2048 + L * 16);
+        const uint32_t sb = *reinterpret_cast<const uint32_t*>(ws + W_PACKED + L * 4);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bars.wempty(s));
+        if (r > 0 && !wait_warp(bars.empty(s), (r - 1) & 1, s_abort, p.err, lim)) goto dequant_done;
+        {
+          const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
+          const uint32_t b2 = (sb >> 16) * 0x10001u;
+          constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
+          uint32_t v[32];
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              // nibbles of K elements 8w+2j (low half) and 8w+2j+1 (high half): 128+q exactly
+              const uint32_t x = ((words[w] >> (4 * j)) & 0x000f000fu) | MAGIC;
+              v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
+            }
+          }
+          ptx::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + TMEM_A0 + 32 * s, v);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bars.afull(s));
+      }
+    }
+  dequant_done:;
+  } else {
+    // ------------------------------------------------ epilogue
+    const int q = warp & 3;
+    int ui = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      Tile t;
+      int mt;
+      if (!unit_tile(p, u, MT, &t, &mt)) {
+        if (threadIdx.x == 12 * 32) set_device_error(p.err, MOE_DEV_BAD_BLOCK);
+        continue;
+      }
+      if (!wait_warp(bars.dfull(), ui & 1, s_abort, p.err, lim)) break;
+      ptx::tc_fence_after();
+      const int N = round16(t.rows);
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+        ptx::tmem_wait_ld();
+        if (MODE == 0) {
+          const int f = 64 * mt + 16 * q + (lane & 15);
+          uint16_t* h = static_cast<uint16_t*>(p.out);
+          const bool lo = lane < 16;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t send = lo ? v[16 + j] : v[j];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const float g = __uint_as_float(lo ? v[j] : recv);
+            const float uu = __uint_as_float(lo ? recv : v[16 + j]);
+            const int n = c0 + j + (lo ? 0 : 16);
+            if (n < t.rows) h[static_cast<size_t>(t.row0 + n) * p.F + f] = float_to_bf16_bits(silu(g) * uu);
+          }
+        } else {
+          const int ch = TC_M * mt + 32 * q + lane;
+          float* acc = static_cast<float*>(p.out);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int n = c0 + j;
+            if (n < t.rows) {
+              const int r = t.row0 + n;
+              int tok = r - A;
+              float wt = 1.0f;
+              if (r < A) {
+                const int a = __ldg(p.perm + r);
+                const bool ok = a >= 0 && a < A;
+                if (!ok) set_device_error(p.err, MOE_DEV_BAD_INDEX);
+                tok = ok ? a / p.k : -1;
+                wt = ok ? __ldg(p.topk_w + a) : 0.0f;
+              }
+              if (tok >= 0) atomicAdd(acc + static_cast<size_t>(tok) * p.H + ch, wt * __uint_as_float(v[j]));
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bars.dempty());
+      ++ui;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0 && *s_abort) {
+    // after a timeout some bulk copies may never have been consumed: let them land before the CTA exits
+    for (int t = prod_it - NST < 0 ? 0 : prod_it - NST; t < prod_it; ++t)
+      wait_drain(bars.wfull(t % NST), (t / NST) & 1, lim);
+  }
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------------------
+// weight repack: canonical -> per (matrix, M-tile, K group) blocks of
+// [2 halves][128 rows][4 words] packed nibbles + [128 rows] (scale, bias).
+// Within a word the nibbles are reordered so that (word >> 4j) & 0x000f000f
+// yields K elements 2j (low half) and 2j+1 (high half) of that word's eight.
+// Gate/up tiles hold 64 features: per 32-row quadrant, 16 gate rows followed
+// by the 16 up rows of the same features.
+// --------------------------------------------------------------------------
+__global__ void repack_kernel(const uint32_t* __restrict__ packed, const uint16_t* __restrict__ scale,
+                              const uint16_t* __restrict__ bias, int n_mat, int rows, int K, int gate_up,
+                              uint8_t* __restrict__ out) {
+  const int MT = rows / TC_M, KT = K / KG;
+  const size_t total = static_cast<size_t>(n_mat) * MT * KT * TC_M;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int L = static_cast<int>(idx % TC_M);
+    size_t rest = idx / TC_M;
+    const int kg = static_cast<int>(rest % KT);
+    rest /= KT;
+    const int mt = static_cast<int>(rest % MT);
+    const int mat = static_cast<int>(rest / MT);
+    int row;
+    if (gate_up) {
+      const int q = L >> 5, i = L & 31;
+      const int f = 64 * mt + 16 * q + (i & 15);
+      row = i < 16 ? f : rows / 2 + f;
+    } else {
+      row = TC_M * mt + L;
+    }
+    const size_t crow = static_cast<size_t>(mat) * rows + row;
+    uint8_t* blk = out + ((static_cast<size_t>(mat) * MT + mt) * KT + kg) * W_STAGE;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const uint32_t in = packed[crow * (K / 8) + kg * 8 + w];
+      uint32_t o = 0;
+#pragma unroll
+      for (int slot = 0; slot < 8; ++slot) {
+        const int src = slot < 4 ? 2 * slot : 2 * (slot - 4) + 1;
+        o |= ((in >> (4 * src)) & 0xfu) << (4 * slot);
+      }
+      *reinterpret_cast<uint32_t*>(blk + (w >> 2) * 2048 + L * 16 + (w & 3) * 4) = o;
+    }
+    const uint32_t sb = static_cast<uint32_t>(scale[crow * (K / 64) + kg]) |
+                        (static_cast<uint32_t>(bias[crow * (K / 64) + kg]) << 16);
+    *reinterpret_cast<uint32_t*>(blk + W_PACKED + L * 4) = sb;
+  }
+}
+
+size_t repacked_bytes(int n_mat, int rows, int K) {
+  return static_cast<size_t>(n_mat) * (rows / TC_M) * (K / KG) * W_STAGE;
+}
+
+cudaError_t launch_repack(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias, int n_mat, int rows,
+                          int K, int gate_up, void* out, cudaStream_t s) {
+  const size_t total = static_cast<size_t>(n_mat) * (rows / TC_M) * (K / KG) * TC_M;
+  size_t blocks = (total + 255) / 256;
+  if (blocks > 65535) blocks = 65535;
+  repack_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(packed, scale, bias, n_mat, rows, K, gate_up,
+                                                              static_cast<uint8_t*>(out));
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+static unsigned long long g_wait_ns = 1000000000ull;
+
+void set_wait_limit_ns(unsigned long long ns) { g_wait_ns = ns; }
+
+cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
+                           const int32_t* perm, const float* topk_w, const int32_t* block_map,
+                           const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s) {
+  static bool attr_set[2] = {false, false};
+  TcParams prm;
+  prm.act = act;
+  prm.w = static_cast<const uint8_t*>(w);
+  prm.perm = perm;
+  prm.topk_w = topk_w;
+  prm.block_map = block_map;
+  prm.num_blocks = num_blocks;
+  prm.out = out;
+  prm.err = device_error_ptr();
+  prm.wait_ns = g_wait_ns;
+  prm.T = T;
+  prm.H = H;
+  prm.F = F;
+  prm.E = E;
+  prm.k = k;
+  prm.bn = bn;
+  prm.cap = cap;
+  if (mode == MOE_GATE_UP_SWIGLU) {
+    if (!attr_set[0]) {
+      cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      attr_set[0] = true;
+    }
+    gemm_tc_kernel<0><<<num_sms, NTHREADS, SMEM_BYTES, s>>>(prm);
+  } else {
+    if (!attr_set[1]) {
+      cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      attr_set[1] = true;
+    }
+    gemm_tc_kernel<1><<<num_sms, NTHREADS, SMEM_BYTES, s>>>(prm);
+  }
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -9,7 +9,7 @@ import numpy as np
 
 from . import _lib
 
-DEFAULT_BLOCK_N = {_lib.IMPL_SIMT: 128, _lib.IMPL_TC: 256, _lib.IMPL_GEMV: 256, _lib.IMPL_AUTO: 128}
+DEFAULT_BLOCK_N = {_lib.IMPL_SIMT: 128, _lib.IMPL_TC: 256, _lib.IMPL_GEMV: 256, _lib.IMPL_AUTO: 256}
 
 
 def _dev(a: np.ndarray, device):
@@ -41,7 +41,7 @@ class MoELayerW4:
         w = {n: (v if isinstance(v, torch.Tensor) else _dev(v, self.device)) for n, v in weights.items()
              if n.startswith(("w13_", "w2_"))}
         self.canonical = w
-        if self.impl in (_lib.IMPL_SIMT, _lib.IMPL_AUTO):
+        if self.impl == _lib.IMPL_SIMT:
             self.weights = _lib.Weights(w["w13_packed"].data_ptr(), w["w13_scale"].data_ptr(),
                                         w["w13_bias"].data_ptr(), w["w2_packed"].data_ptr(),
                                         w["w2_scale"].data_ptr(), w["w2_bias"].data_ptr())

@@ -131,12 +131,14 @@ size_t moe_repacked_bytes(int n_mat, int rows, int K);
 
 /*
  * moe_repack_w4 -- one-time conversion of canonical weights into the layout
- * the tensor-core and GEMV kernels stream: per matrix, per 128-row tile, per
- * 64-wide K group, one 4 KiB block of packed nibbles (rows laid out so that a
- * 128-byte swizzle makes the per-row reads bank-conflict free) followed by the
- * rows' (scale, bias) pairs.  `gate_up` = 1 interleaves gate and up rows in
- * groups of 16 so that one tile holds 64 matching gate/up features.  Not part
- * of the layer's timed work.  rows % 128 == 0 and K % 64 == 0.
+ * the tensor-core kernel streams (not part of the layer's timed work).  Per
+ * matrix, per 128-row tile, per 64-wide K group, one contiguous 4608-byte
+ * block: [2 halves][128 rows][16 bytes] of packed nibbles (half h holds K
+ * elements 32h..32h+31 of the group; within each word the nibbles are ordered
+ * so that (word >> 4j) & 0x000f000f holds elements 2j and 2j+1 of its eight)
+ * followed by [128 rows] x (scale bf16, bias bf16).  With gate_up = 1 a tile
+ * holds 64 features: in each 32-row quarter, 16 gate rows then the 16 up rows
+ * of the same features (rows = 2F).  Needs rows % 128 == 0 and K % 64 == 0.
  */
 int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias,
                   int n_mat, int rows, int K, int gate_up, void* out, moe_stream_t stream);
@@ -166,7 +168,7 @@ int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t*
  * weights: canonical layout for MOE_IMPL_SIMT, repacked layout otherwise.
  * block_map / num_blocks: moe_route's outputs for the same block_n.
  * impl: MOE_IMPL_* (AUTO picks by T).  The TC kernel needs block_n <= 256
- * and a multiple of 16; SIMT needs block_n <= 128.
+ * and H % 128 == 0; SIMT needs block_n <= 128.
  */
 int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,
                        const void* w_packed, const uint16_t* w_scale, const uint16_t* w_bias,
@@ -241,6 +243,11 @@ int moe_layer_forward_host(const uint16_t* x_host, const float* logits_host, uin
 /* Synchronises the current device, returns the device error word in *code and
  * clears it.  Returns MOE_ERR_CUDA if the synchronisation itself failed. */
 int moe_get_device_error(int32_t* code);
+
+/* Time limit of every bounded wait inside the tensor-core kernel (default
+ * 1 s).  When a wait runs out the kernel records MOE_DEV_TIMEOUT, drains its
+ * copies in flight, frees its tensor memory and returns.  Test hook. */
+void moe_set_wait_limit_ns(uint64_t ns);
 
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int moe_version(void);

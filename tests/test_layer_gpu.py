@@ -10,7 +10,7 @@ import gpu_util as G
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["simt"]
+IMPLS = ["tc", "simt"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,6 +53,16 @@ def test_layer_small(spec, impl):
     G.assert_close(got, ref, f"layer {spec} {impl}")
 
 
+@pytest.mark.parametrize("block_n", [16, 64, 128, 200, 256])
+def test_layer_tc_block_sizes(block_n):
+    """The tensor-core kernel with every tile height it supports (N = rows rounded up to 16)."""
+    spec = (700, 256, 16, 4, 128, False)
+    d = G.workload(spec)
+    (got,), _ = run_layer(d, "tc", block_n=block_n)
+    ref = moe_ref.moe_forward(d["x_bits"], d["logits"], d, spec[3])["out"]
+    G.assert_close(got, ref, f"tc block_n={block_n}")
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_layer_repeatable(impl):
     """Two calls in a row give the same result (the accumulator is left zero)."""
@@ -79,3 +89,38 @@ def test_layer_full_size_sampled(name, impl):
     ref = moe_ref.moe_forward(d["x_bits"], d["logits"], d, d["workload"].shape.k, tokens=toks)["out"]
     G.assert_close(got[toks], ref, f"{name} sampled tokens {impl}")
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_gate_up_intermediate(impl):
+    """The gate/up GEMM alone: h = bf16(silu(g) u) per permuted row against the oracle's h."""
+    import torch
+    from bit_mixture_experts_gb300 import _lib
+    from bit_mixture_experts_gb300.layer import MoELayerW4
+    spec = (200, 256, 8, 2, 128, False)
+    d = G.workload(spec)
+    T, H, E, k, F = spec[:5]
+    layer = MoELayerW4(H, E, k, F, d, impl=impl)
+    x, logits = G.to_dev_inputs(d)
+    b = layer.buffers(T)
+    w = layer.weights
+    bn = layer.block_n
+    _lib.moe_route(logits, k, bn, b["topk_ids"], b["topk_w"], b["counts"], b["offsets"], b["perm"],
+                   b["inv_perm"], b["block_map"], b["num_blocks"], b["workspace"])
+    b["h"].zero_()
+    _lib.moe_expert_gemm_w4(_lib.GATE_UP, layer.impl, x, T, H, F, E, k, w.w13, w.s13, w.b13, b["perm"],
+                            b["topk_w"], b["block_map"], b["num_blocks"], bn, b["h"])
+    torch.cuda.synchronize()
+    assert _lib.moe_get_device_error() == 0
+    got = G.bf16_to_f64(b["h"])
+    perm = b["perm"].cpu().numpy()
+    ref = moe_ref.moe_forward(d["x_bits"], d["logits"], d, k, want_h=True)
+    ids = ref["topk_ids"].ravel()
+    A = T * k
+    want = np.zeros((A + T, F))
+    for r in range(A):
+        a = int(perm[r])
+        want[r] = ref["h"][(a // k, int(ids[a]))]
+    for t in range(T):
+        want[A + t] = ref["h"][(t, E)]
+    G.assert_close(got, want, f"h {impl}")
