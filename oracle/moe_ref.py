@@ -162,12 +162,24 @@ def silu(g):
     return g / (1.0 + np.exp(-g))
 
 
-def expert_swiglu(xrows, w13) -> np.ndarray:
-    """h = bf16(silu(x Wg^T) * (x Wu^T)); w13 holds the F gate rows then the F up rows."""
+def expert_swiglu_exact(xrows, w13) -> np.ndarray:
+    """silu(x Wg^T) * (x Wu^T) before rounding; w13 holds the F gate rows then the F up rows."""
     F = w13.shape[0] // 2
     g = xrows @ w13[:F].T
     u = xrows @ w13[F:].T
-    return round_bf16(silu(g) * u)
+    return silu(g) * u
+
+
+def expert_swiglu(xrows, w13) -> np.ndarray:
+    """h = bf16(silu(x Wg^T) * (x Wu^T))."""
+    return round_bf16(expert_swiglu_exact(xrows, w13))
+
+
+def bf16_floor_ceil(a):
+    """The two bf16 values enclosing a (equal when a is a bf16 value)."""
+    a = np.asarray(a, dtype=np.float64)
+    m, e = np.frexp(a)
+    return np.ldexp(np.floor(m * 256.0), e - 8), np.ldexp(np.ceil(m * 256.0), e - 8)
 
 
 def expert_down(h, w2) -> np.ndarray:
@@ -181,14 +193,18 @@ def expert_weights(wts: dict, e: int):
     return w13, w2
 
 
-def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = False) -> dict:
+def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = False, h_given=None) -> dict:
     """The layer: out[t] = bf16( sum_j w[t,j] * y_{e_j}(x_t) + y_shared(x_t) ).
 
     ``tokens`` restricts the computation to a subset of token indices (routing
     of a token depends on its own logits only), which is how full-size
     workloads are checked on sampled outputs.  With ``want_h`` the bf16
     intermediate h of every (token, routed expert) and of the shared expert is
-    returned as well, keyed by (t, e).
+    returned as well, keyed by (t, e), together with its unrounded value
+    (key "h_exact").  ``h_given(t, e)``, when set, supplies h instead of the
+    gate/up projection: the down projection and combine are then evaluated
+    exactly on that h (used to check a rounding of h that differs from
+    round-to-nearest on values next to a rounding midpoint).
     """
     logits = np.asarray(logits, dtype=np.float32)
     T, E = logits.shape
@@ -197,7 +213,7 @@ def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = F
     x = bf16_value(np.asarray(x_bits)[sel])
     n, H = x.shape
     acc = np.zeros((n, H), dtype=np.float64)
-    hs = {}
+    hs, hx = {}, {}
     for e in sorted(set(np.unique(ids).tolist()) | {E}):
         if e == E:
             rows, wt = np.arange(n), np.ones(n)
@@ -205,13 +221,19 @@ def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = F
             rows, cols = np.nonzero(ids == e)
             wt = w[rows, cols]
         w13, w2 = expert_weights(wts, e)
-        h = expert_swiglu(x[rows], w13)
+        if h_given is not None:
+            h = np.stack([np.asarray(h_given(int(sel[r]), int(e)), dtype=np.float64) for r in rows])
+        else:
+            v = expert_swiglu_exact(x[rows], w13)
+            h = round_bf16(v)
+            if want_h:
+                for i, r in enumerate(rows):
+                    hs[(int(sel[r]), int(e))] = h[i]
+                    hx[(int(sel[r]), int(e))] = v[i]
         y = expert_down(h, w2)
         acc[rows] += wt[:, None] * y
-        if want_h:
-            for i, r in enumerate(rows):
-                hs[(int(sel[r]), int(e))] = h[i]
     res = {"out": round_bf16(acc), "topk_ids": ids, "topk_w": w, "tokens": sel}
     if want_h:
         res["h"] = hs
+        res["h_exact"] = hx
     return res

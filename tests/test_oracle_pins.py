@@ -24,6 +24,32 @@ def test_bruteforce_ragged_shape():
     P.pin_bruteforce_layer(shape=(128, 5, 3, 64), T=13, seed=3)
 
 
+def test_bf16_floor_ceil():
+    r = np.random.default_rng(11)
+    a = r.standard_normal(5000) * 10.0 ** r.integers(-3, 3, 5000)
+    lo, hi = moe_ref.bf16_floor_ceil(a)
+    rn = moe_ref.round_bf16(a)
+    assert np.all(lo <= a) and np.all(a <= hi)
+    assert np.all((rn == lo) | (rn == hi))
+    assert np.array_equal(moe_ref.round_bf16(lo), lo) and np.array_equal(moe_ref.round_bf16(hi), hi)
+    # adjacent: nothing representable strictly between
+    mid = 0.5 * (lo + hi)
+    assert np.all((lo == hi) | ((moe_ref.round_bf16(mid) == lo) | (moe_ref.round_bf16(mid) == hi)))
+    b = moe_ref.round_bf16(a)
+    lo2, hi2 = moe_ref.bf16_floor_ceil(b)
+    assert np.array_equal(lo2, b) and np.array_equal(hi2, b)
+
+
+def test_given_h_reproduces_layer():
+    """Evaluating down + combine on the oracle's own h reproduces the layer output."""
+    d = workloads.make_workload(workloads.custom(9, 128, 4, 2, 64), 2)
+    ref = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, want_h=True)
+    again = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, h_given=lambda t, e: ref["h"][(t, e)])
+    assert np.array_equal(ref["out"], again["out"])
+    for key, h in ref["h"].items():
+        assert np.array_equal(h, moe_ref.round_bf16(ref["h_exact"][key]))
+
+
 def test_skew_calibration():
     """The skewed long prefill leaves about 30 experts empty and one expert chosen by
     nearly every token (at most T of the T*k assignments can go to one expert)."""
@@ -54,7 +80,7 @@ def test_generator_statistics():
 # --------------------------------------------------------------------------- #
 def _mutations():
     orig = {n: getattr(moe_ref, n) for n in
-            ("unpack_u4", "dequant", "expert_swiglu", "topk_route", "expert_down",
+            ("unpack_u4", "dequant", "expert_swiglu_exact", "topk_route", "expert_down",
              "expert_weights", "stable_permutation", "round_bf16", "block_map", "exclusive_scan")}
 
     def msb_first(p):
@@ -67,7 +93,7 @@ def _mutations():
     def silu_on_up(xrows, w13):
         F = w13.shape[0] // 2
         g, u = xrows @ w13[:F].T, xrows @ w13[F:].T
-        return moe_ref.round_bf16(moe_ref.silu(u) * g)
+        return moe_ref.silu(u) * g
 
     def ties_high(logits, k):
         lg = np.asarray(logits, np.float32)
@@ -117,7 +143,7 @@ def _mutations():
     return {
         "nibble_msb_first": ("unpack_u4", msb_first),
         "dequant_drops_bias": ("dequant", no_bias),
-        "silu_on_up": ("expert_swiglu", silu_on_up),
+        "silu_on_up": ("expert_swiglu_exact", silu_on_up),
         "ties_to_high_index": ("topk_route", ties_high),
         "no_renormalisation": ("topk_route", no_renorm),
         "down_transposed": ("expert_down", down_transposed),
