@@ -140,7 +140,7 @@ def run_ours(args, rank, world, local_rank):
     d = workloads.make_workload(wl, seed=0, with_weights=True)
     if rank:  # each rank its own tokens (weights are the same replica)
         d.update(workloads.make_tokens(s, T, seed=rank, skew=wl.skew))
-    layer = MoELayerW4(s.H, s.E, s.k, s.F, d, device=dev, impl=args.kernels)
+    layer = MoELayerW4(s.H, s.E, s.k, s.F, d, device=dev, impl=args.kernels, block_n=args.block_n)
     x = torch.from_numpy(d["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
     logits = torch.from_numpy(d["logits"]).to(dev)
     out = torch.empty((T, s.H), dtype=torch.bfloat16, device=dev)
@@ -351,6 +351,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill512", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--kernels", default="auto", choices=["auto", "tc", "simt", "gemv"])
+    ap.add_argument("--block-n", type=int, default=None, help="rows per GEMM tile (default: per kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true")

@@ -29,6 +29,9 @@
 // Every mbarrier wait is bounded by a time limit; on expiry the kernel records
 // MOE_DEV_TIMEOUT in the device error word, every role leaves its loop, copies
 // in flight are drained, TMEM is freed and the kernel returns.
+#include <cuda.h>
+#include <string.h>
+
 #include "moe_common.cuh"
 #include "moe_ptx.cuh"
 
@@ -38,39 +41,33 @@ namespace {
 
 constexpr int TC_M = 128;           // weight rows per M-tile
 constexpr int KG = 64;              // K per pipeline stage (= one quant group)
-constexpr int NST = 4;              // pipeline stages
-constexpr int NMAX = 256;           // max token rows per tile
-constexpr int B_STAGE = NMAX * 128; // bytes of one activation stage (rows x 64 bf16)
+constexpr int NW = 12;              // packed-weight ring (smem)
+constexpr int NA = 8;               // dequantised-weight ring (TMEM, 32 columns each)
+constexpr int NBMAX = 16;           // activation ring (smem), run-time depth <= NBMAX
 constexpr int W_PACKED = TC_M * 32; // packed nibbles of one M-tile x K group
 constexpr int W_STAGE = W_PACKED + TC_M * 4;  // + (scale, bias) per row
 constexpr int TMEM_COLS = 512;
-constexpr int TMEM_A0 = 256;        // first TMEM column of the A stages (D uses 0..255)
+constexpr int TMEM_A0 = 256;        // A ring columns 256..511; D uses 0..255
 constexpr int NTHREADS = 512;
-constexpr int GATHER_T = 64;        // threads of the gather warps
-constexpr int LAG = 2;              // cp.async groups kept in flight per gather thread
+constexpr int GATHER_T = 64;        // threads of the gather warps (gate/up mode)
 
-// smem layout (offsets from a 1024-byte aligned base)
-constexpr int OFF_B = 0;
-constexpr int OFF_W = OFF_B + NST * B_STAGE;
-constexpr int OFF_BAR = OFF_W + NST * W_STAGE;
-constexpr int NBAR = 5 * NST + 3;
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+// barrier indices
+constexpr int BAR_WFULL = 0;
+constexpr int BAR_WEMPTY = BAR_WFULL + NW;
+constexpr int BAR_AFULL = BAR_WEMPTY + NW;
+constexpr int BAR_AEMPTY = BAR_AFULL + NA;
+constexpr int BAR_BFULL = BAR_AEMPTY + NA;
+constexpr int BAR_BEMPTY = BAR_BFULL + NBMAX;
+constexpr int BAR_DFULL = BAR_BEMPTY + NBMAX;
+constexpr int BAR_DEMPTY = BAR_DFULL + 2;
+constexpr int BAR_FIN = BAR_DEMPTY + 2;
+constexpr int NBAR = BAR_FIN + 1;
 
-static_assert(OFF_W % 1024 == 0, "B stages must stay 1024-byte aligned");
+// smem layout (offsets from a 1024-byte aligned base): B ring | W ring | barriers | misc
+constexpr int W_RING_BYTES = NW * W_STAGE;
+constexpr int TAIL_BYTES = W_RING_BYTES + NBAR * 8 + 16;
+
 static_assert(W_STAGE % 16 == 0, "bulk copies move multiples of 16 bytes");
-
-struct Bars {
-  uint32_t base;
-  __device__ uint32_t wfull(int s) const { return base + 8 * s; }
-  __device__ uint32_t wempty(int s) const { return base + 8 * (NST + s); }
-  __device__ uint32_t afull(int s) const { return base + 8 * (2 * NST + s); }
-  __device__ uint32_t bfull(int s) const { return base + 8 * (3 * NST + s); }
-  __device__ uint32_t empty(int s) const { return base + 8 * (4 * NST + s); }
-  __device__ uint32_t dfull() const { return base + 8 * (5 * NST); }
-  __device__ uint32_t dempty() const { return base + 8 * (5 * NST + 1); }
-  __device__ uint32_t fin() const { return base + 8 * (5 * NST + 2); }
-};
 
 struct TcParams {
   const uint16_t* act;
@@ -83,6 +80,10 @@ struct TcParams {
   int* err;
   unsigned long long wait_ns;
   int T, H, F, E, k, bn, cap;
+  int nb;       // activation ring depth
+  int sb;       // bytes of one activation stage (boxr rows x 128 bytes)
+  int nd;       // accumulator buffers (2 when tiles have <= 128 rows)
+  int lag;      // cp.async groups each gather thread keeps in flight
 };
 
 // Bounded wait on phase `parity` of `bar`.  Returns false on timeout or when
@@ -152,21 +153,32 @@ __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
 }  // namespace
 
+// Rings (each with full/empty mbarriers, stage index = running K-step count
+// `it` modulo the ring depth):
+//   W  packed 4-bit blocks, smem, bulk copy -> dequant warps
+//   A  dequantised bf16 weights, TMEM, dequant warps -> MMA
+//   B  activation rows (128B-swizzled, K-major), smem, gather/TMA -> MMA
+//   D  FP32 accumulators, TMEM, MMA -> epilogue (1 or 2 buffers)
 template <int MODE>
-__global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) {
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmap_act) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
-  const Bars bars{sbase + OFF_BAR};
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 4);
+  const int NB = p.nb, SB = p.sb, ND = p.nd;
+  const uint32_t off_w = static_cast<uint32_t>(NB * SB);
+  const uint32_t bar0 = sbase + off_w + W_RING_BYTES;
+  auto bar = [bar0](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + off_w + W_RING_BYTES + NBAR * 8);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + off_w + W_RING_BYTES + NBAR * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = MODE == 0 ? p.H : p.F;
   const int KT = K / KG;
   const int MT = MODE == 0 ? (2 * p.F) / TC_M : p.H / TC_M;
   const int A = p.T * p.k;
+  const int DCOLS = ND == 2 ? 128 : 256;
   int nb = __ldg(p.num_blocks);
   if (nb < 0 || nb > p.cap) {
     if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(p.err, MOE_DEV_BAD_BLOCK);
@@ -176,16 +188,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) 
 
   if (threadIdx.x == 0) {
     *s_abort = 0;
-    for (int s = 0; s < NST; ++s) {
-      ptx::mbar_init(bars.wfull(s), 1);
-      ptx::mbar_init(bars.wempty(s), 4);
-      ptx::mbar_init(bars.afull(s), 4);
-      ptx::mbar_init(bars.bfull(s), GATHER_T);
-      ptx::mbar_init(bars.empty(s), 1);
+    for (int s = 0; s < NW; ++s) {
+      ptx::mbar_init(bar(BAR_WFULL + s), 1);
+      ptx::mbar_init(bar(BAR_WEMPTY + s), 4);
     }
-    ptx::mbar_init(bars.dfull(), 1);
-    ptx::mbar_init(bars.dempty(), 4);
-    ptx::mbar_init(bars.fin(), 1);
+    for (int s = 0; s < NA; ++s) {
+      ptx::mbar_init(bar(BAR_AFULL + s), 4);
+      ptx::mbar_init(bar(BAR_AEMPTY + s), 1);
+    }
+    for (int s = 0; s < NBMAX; ++s) {
+      ptx::mbar_init(bar(BAR_BFULL + s), MODE == 0 ? GATHER_T : 1);
+      ptx::mbar_init(bar(BAR_BEMPTY + s), 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      ptx::mbar_init(bar(BAR_DFULL + d), 1);
+      ptx::mbar_init(bar(BAR_DEMPTY + d), 4);
+    }
+    ptx::mbar_init(bar(BAR_FIN), 1);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -197,23 +216,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) 
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const unsigned long long lim = p.wait_ns;
-  int prod_it = 0;  // bulk copies issued by the producer (warp 0, lane 0)
+  int prod_w = 0, prod_b = 0;  // bulk/tensor copies issued (for the drain after a timeout)
 
   if (warp == 0) {
     // ------------------------------------------------ packed-weight producer
     if (lane == 0) {
-      int& it = prod_it;
+      int& it = prod_w;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         Tile t;
         int mt;
         if (!unit_tile(p, u, MT, &t, &mt)) continue;
         const uint8_t* src = p.w + (static_cast<size_t>(t.expert) * MT + mt) * KT * static_cast<size_t>(W_STAGE);
         for (int kg = 0; kg < KT; ++kg, ++it) {
-          const int s = it % NST, r = it / NST;
-          if (r > 0 && !wait_one(bars.wempty(s), (r - 1) & 1, s_abort, p.err, lim)) goto producer_done;
-          ptx::mbar_arrive_expect_tx(bars.wfull(s), W_STAGE);
-          ptx::bulk_g2s(sbase + OFF_W + s * W_STAGE, src + static_cast<size_t>(kg) * W_STAGE, W_STAGE,
-                        bars.wfull(s));
+          const int s = it % NW, r = it / NW;
+          if (r > 0 && !wait_one(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto producer_done;
+          ptx::mbar_arrive_expect_tx(bar(BAR_WFULL + s), W_STAGE);
+          ptx::bulk_g2s(sbase + off_w + s * W_STAGE, src + static_cast<size_t>(kg) * W_STAGE, W_STAGE,
+                        bar(BAR_WFULL + s));
         }
       }
     producer_done:;
@@ -227,46 +246,67 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) 
         int mt;
         if (!unit_tile(p, u, MT, &t, &mt)) continue;
         const uint32_t idesc = ptx::idesc_bf16_f32(TC_M, round16(t.rows));
-        if (ui > 0 && !wait_one(bars.dempty(), (ui - 1) & 1, s_abort, p.err, lim)) goto mma_done;
+        const int d = ui % ND, rd = ui / ND;
+        if (rd > 0 && !wait_one(bar(BAR_DEMPTY + d), (rd - 1) & 1, s_abort, p.err, lim)) goto mma_done;
         ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + d * DCOLS;
         for (int kg = 0; kg < KT; ++kg, ++it) {
-          const int s = it % NST, r = it / NST;
-          if (!wait_one(bars.afull(s), r & 1, s_abort, p.err, lim)) goto mma_done;
-          if (!wait_one(bars.bfull(s), r & 1, s_abort, p.err, lim)) goto mma_done;
+          const int sa = it % NA, sb = it % NB;
+          if (!wait_one(bar(BAR_AFULL + sa), (it / NA) & 1, s_abort, p.err, lim)) goto mma_done;
+          if (!wait_one(bar(BAR_BFULL + sb), (it / NB) & 1, s_abort, p.err, lim)) goto mma_done;
           ptx::tc_fence_after();
-          const uint32_t a_tmem = tmem + TMEM_A0 + 32 * s;
-          const uint64_t bdesc = ptx::smem_desc_sw128(sbase + OFF_B + s * B_STAGE);
+          const uint32_t a_tmem = tmem + TMEM_A0 + 32 * sa;
+          const uint64_t bdesc = ptx::smem_desc_sw128(sbase + sb * SB);
 #pragma unroll
           for (int j = 0; j < KG / 16; ++j)
-            ptx::mma_ts(tmem, a_tmem + 8 * j, bdesc + 2 * j, idesc, (kg | j) != 0);
-          ptx::mma_commit(bars.empty(s));
+            ptx::mma_ts(d_tmem, a_tmem + 8 * j, bdesc + 2 * j, idesc, (kg | j) != 0);
+          ptx::mma_commit(bar(BAR_AEMPTY + sa));
+          ptx::mma_commit(bar(BAR_BEMPTY + sb));
         }
-        ptx::mma_commit(bars.dfull());
+        ptx::mma_commit(bar(BAR_DFULL + d));
         ++ui;
       }
     mma_done:
-      ptx::mma_commit(bars.fin());
-      wait_drain(bars.fin(), 0, lim);
+      ptx::mma_commit(bar(BAR_FIN));
+      wait_drain(bar(BAR_FIN), 0, lim);
     }
   } else if (warp < 4) {
-    // ------------------------------------------------ activation gather
-    const int gt = threadIdx.x - 64;  // 0..63
-    const int chunk = gt & 7, row_a = gt >> 3;
-    int it = 0;
-    bool aborted = false;
-    for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
-      Tile t;
-      int mt;
-      if (!unit_tile(p, u, MT, &t, &mt)) continue;
-      // this thread's rows: i = row_a + 8*j
-      int src_row[NMAX / 8];
+    if (MODE == 1) {
+      // ------------------------------------------------ activation producer (TMA, contiguous rows)
+      if (warp == 2 && lane == 0) {
+        int& it = prod_b;
+        const uint32_t bytes = static_cast<uint32_t>(SB);
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+          Tile t;
+          int mt;
+          if (!unit_tile(p, u, MT, &t, &mt)) continue;
+          for (int kg = 0; kg < KT; ++kg, ++it) {
+            const int s = it % NB, r = it / NB;
+            if (r > 0 && !wait_one(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto bprod_done;
+            ptx::mbar_arrive_expect_tx(bar(BAR_BFULL + s), bytes);
+            ptx::tma_load_2d(sbase + s * SB, &tmap_act, kg * KG, t.row0, bar(BAR_BFULL + s));
+          }
+        }
+      bprod_done:;
+      }
+    } else {
+      // ------------------------------------------------ activation gather (cp.async, token rows)
+      const int gt = threadIdx.x - 64;  // 0..63
+      const int chunk = gt & 7, row_a = gt >> 3;
+      const int lag = p.lag;
+      int it = 0;
+      bool aborted = false;
+      for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
+        Tile t;
+        int mt;
+        if (!unit_tile(p, u, MT, &t, &mt)) continue;
+        int src_row[256 / 8];
 #pragma unroll
-      for (int j = 0; j < NMAX / 8; ++j) {
-        const int i = row_a + 8 * j;
-        int sr = -1;
-        if (i < t.rows) {
-          const int r = t.row0 + i;
-          if (MODE == 0) {
+        for (int j = 0; j < 256 / 8; ++j) {
+          const int i = row_a + 8 * j;
+          int sr = -1;
+          if (i < t.rows) {
+            const int r = t.row0 + i;
             if (r < A) {
               const int a = __ldg(p.perm + r);
               if (a >= 0 && a < A) sr = a / p.k;
@@ -274,43 +314,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) 
             } else {
               sr = r - A;
             }
-          } else {
-            sr = r;
           }
+          src_row[j] = sr;
         }
-        src_row[j] = sr;
-      }
-      for (int kg = 0; kg < KT; ++kg, ++it) {
-        const int s = it % NST, r = it / NST;
-        if (r > 0 && !wait_warp(bars.empty(s), (r - 1) & 1, s_abort, p.err, lim)) {
-          aborted = true;
-          break;
-        }
-        const uint32_t dst0 = sbase + OFF_B + s * B_STAGE;
+        for (int kg = 0; kg < KT; ++kg, ++it) {
+          const int s = it % NB, r = it / NB;
+          if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t dst0 = sbase + s * SB;
 #pragma unroll
-        for (int j = 0; j < NMAX / 8; ++j) {
-          const int i = row_a + 8 * j;
-          if (src_row[j] >= 0) {
-            const uint16_t* src = p.act + static_cast<size_t>(src_row[j]) * K + kg * KG + chunk * 8;
-            const uint32_t dst = dst0 + (i >> 3) * 1024 + (i & 7) * 128 + ((chunk ^ (i & 7)) << 4);
-            ptx::cp_async_16(dst, src);
+          for (int j = 0; j < 256 / 8; ++j) {
+            const int i = row_a + 8 * j;
+            if (src_row[j] >= 0) {
+              const uint16_t* src = p.act + static_cast<size_t>(src_row[j]) * K + kg * KG + chunk * 8;
+              const uint32_t dst = dst0 + (i >> 3) * 1024 + (i & 7) * 128 + ((chunk ^ (i & 7)) << 4);
+              ptx::cp_async_16(dst, src);
+            }
+          }
+          ptx::cp_async_commit();
+          if (it >= lag) {
+            ptx::cp_async_wait_n(lag);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(bar(BAR_BFULL + (it - lag) % NB));
           }
         }
-        ptx::cp_async_commit();
-        if (it >= LAG) {
-          ptx::cp_async_wait<LAG>();
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(bars.bfull((it - LAG) % NST));
-        }
       }
-    }
-    ptx::cp_async_wait_all();
-    if (!aborted && !*s_abort) {
-      ptx::fence_proxy_async_smem();
-      for (int t = it - LAG < 0 ? 0 : it - LAG; t < it; ++t) ptx::mbar_arrive(bars.bfull(t % NST));
+      ptx::cp_async_wait_all();
+      if (!aborted && !*s_abort) {
+        ptx::fence_proxy_async_smem();
+        for (int t = it - lag < 0 ? 0 : it - lag; t < it; ++t) ptx::mbar_arrive(bar(BAR_BFULL + t % NB));
+      }
     }
   } else if (warp < 12) {
-    // ------------------------------------------------ dequant (two warpgroups)
+    // ------------------------------------------------ dequant (two warpgroups, alternate K steps)
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int L = 32 * q + lane;  // weight row within the M-tile = TMEM lane
@@ -321,19 +359,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) 
       if (!unit_tile(p, u, MT, &t, &mt)) continue;
       for (int kg = 0; kg < KT; ++kg, ++it) {
         if ((it & 1) != wg) continue;
-        const int s = it % NST, r = it / NST;
-        if (!wait_warp(bars.wfull(s), r & 1, s_abort, p.err, lim)) goto dequant_done;
-        const uint8_t* ws = smem + OFF_W + s * W_STAGE;
+        const int sw = it % NW, sa = it % NA;
+        if (!wait_warp(bar(BAR_WFULL + sw), (it / NW) & 1, s_abort, p.err, lim)) goto dequant_done;
+        const uint8_t* ws = smem + off_w + sw * W_STAGE;
         const uint4 p0 = *reinterpret_cast<const uint4*>(ws + L * 16);
         const uint4 p1 = *reinterpret_cast<const uint4*>(ws + 2048 + L * 16);
-        const uint32_t sb = *reinterpret_cast<const uint32_t*>(ws + W_PACKED + L * 4);
+        const uint32_t sbw = *reinterpret_cast<const uint32_t*>(ws + W_PACKED + L * 4);
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars.wempty(s));
-        if (r > 0 && !wait_warp(bars.empty(s), (r - 1) & 1, s_abort, p.err, lim)) goto dequant_done;
+        if (lane == 0) ptx::mbar_arrive(bar(BAR_WEMPTY + sw));
+        if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
+          goto dequant_done;
         {
           const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-          const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
-          const uint32_t b2 = (sb >> 16) * 0x10001u;
+          const uint32_t s2 = (sbw & 0xffffu) * 0x10001u;
+          const uint32_t b2 = (sbw >> 16) * 0x10001u;
           constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
           uint32_t v[32];
 #pragma unroll
@@ -345,12 +384,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) 
               v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
             }
           }
-          ptx::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + TMEM_A0 + 32 * s, v);
+          ptx::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + TMEM_A0 + 32 * sa, v);
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bars.afull(s));
+        if (lane == 0) ptx::mbar_arrive(bar(BAR_AFULL + sa));
       }
     }
   dequant_done:;
@@ -365,14 +404,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) 
         if (threadIdx.x == 12 * 32) set_device_error(p.err, MOE_DEV_BAD_BLOCK);
         continue;
       }
-      if (!wait_warp(bars.dfull(), ui & 1, s_abort, p.err, lim)) break;
+      const int d = ui % ND;
+      if (!wait_warp(bar(BAR_DFULL + d), (ui / ND) & 1, s_abort, p.err, lim)) break;
       ptx::tc_fence_after();
       const int N = round16(t.rows);
       for (int c0 = 0; c0 < N; c0 += 32) {
         uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
-        ptx::tmem_wait_ld();
+        ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + d * DCOLS + c0, v);
         if (MODE == 0) {
+          ptx::tmem_wait_ld();
           const int f = 64 * mt + 16 * q + (lane & 15);
           uint16_t* h = static_cast<uint16_t*>(p.out);
           const bool lo = lane < 16;
@@ -386,40 +426,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) gemm_tc_kernel(const TcParams p) 
             if (n < t.rows) h[static_cast<size_t>(t.row0 + n) * p.F + f] = float_to_bf16_bits(silu(g) * uu);
           }
         } else {
+          // token and combine weight of column c0 + lane, loaded once and broadcast
+          int tok = -1;
+          float wt = 0.f;
+          const int n_l = c0 + lane;
+          if (n_l < t.rows) {
+            const int r = t.row0 + n_l;
+            if (r < A) {
+              const int a = __ldg(p.perm + r);
+              if (a >= 0 && a < A) {
+                tok = a / p.k;
+                wt = __ldg(p.topk_w + a);
+              } else {
+                set_device_error(p.err, MOE_DEV_BAD_INDEX);
+              }
+            } else {
+              tok = r - A;
+              wt = 1.0f;
+            }
+          }
+          ptx::tmem_wait_ld();
           const int ch = TC_M * mt + 32 * q + lane;
           float* acc = static_cast<float*>(p.out);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int n = c0 + j;
-            if (n < t.rows) {
-              const int r = t.row0 + n;
-              int tok = r - A;
-              float wt = 1.0f;
-              if (r < A) {
-                const int a = __ldg(p.perm + r);
-                const bool ok = a >= 0 && a < A;
-                if (!ok) set_device_error(p.err, MOE_DEV_BAD_INDEX);
-                tok = ok ? a / p.k : -1;
-                wt = ok ? __ldg(p.topk_w + a) : 0.0f;
-              }
-              if (tok >= 0) atomicAdd(acc + static_cast<size_t>(tok) * p.H + ch, wt * __uint_as_float(v[j]));
-            }
+            const int tj = __shfl_sync(0xffffffffu, tok, j);
+            const float wj = __shfl_sync(0xffffffffu, wt, j);
+            if (tj >= 0) atomicAdd(acc + static_cast<size_t>(tj) * p.H + ch, wj * __uint_as_float(v[j]));
           }
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bars.dempty());
+      if (lane == 0) ptx::mbar_arrive(bar(BAR_DEMPTY + d));
       ++ui;
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0 && lane == 0 && *s_abort) {
-    // after a timeout some bulk copies may never have been consumed: let them land before the CTA exits
-    for (int t = prod_it - NST < 0 ? 0 : prod_it - NST; t < prod_it; ++t)
-      wait_drain(bars.wfull(t % NST), (t / NST) & 1, lim);
+  if (*s_abort) {
+    // after a timeout some copies may never have been consumed: let them land before the CTA exits
+    if (warp == 0 && lane == 0)
+      for (int t = prod_w - NW < 0 ? 0 : prod_w - NW; t < prod_w; ++t)
+        wait_drain(bar(BAR_WFULL + t % NW), (t / NW) & 1, lim);
+    if (MODE == 1 && warp == 2 && lane == 0)
+      for (int t = prod_b - NB < 0 ? 0 : prod_b - NB; t < prod_b; ++t)
+        wait_drain(bar(BAR_BFULL + t % NB), (t / NB) & 1, lim);
   }
   if (warp == 1) {
     ptx::tc_fence_after();
@@ -494,10 +547,43 @@ static unsigned long long g_wait_ns = 1000000000ull;
 
 void set_wait_limit_ns(unsigned long long ns) { g_wait_ns = ns; }
 
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+int max_dyn_smem() {
+  static int v = 0;
+  if (!v) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (v <= 0) v = 232448;
+  }
+  return v;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                            const int32_t* perm, const float* topk_w, const int32_t* block_map,
                            const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s) {
-  static bool attr_set[2] = {false, false};
   TcParams prm;
   prm.act = act;
   prm.w = static_cast<const uint8_t*>(w);
@@ -515,18 +601,38 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   prm.k = k;
   prm.bn = bn;
   prm.cap = cap;
+  const int boxr = (bn + 15) & ~15;
+  prm.sb = boxr * 128;
+  const int budget = max_dyn_smem() - TAIL_BYTES - 1024;
+  int nbs = budget / prm.sb;
+  if (nbs > NBMAX) nbs = NBMAX;
+  if (nbs < 3) return cudaErrorInvalidValue;
+  prm.nb = nbs;
+  prm.nd = boxr <= 128 ? 2 : 1;
+  prm.lag = nbs - 1 < 6 ? nbs - 1 : 6;
+  const int smem = nbs * prm.sb + TAIL_BYTES + 1024;
+
+  CUtensorMap tmap;
+  memset(&tmap, 0, sizeof(tmap));
+  if (mode == MOE_DOWN_COMBINE) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int A = T * k;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(F), static_cast<cuuint64_t>(A + T)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(F) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(boxr)};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(act), gdim, gstride, box,
+                     estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   if (mode == MOE_GATE_UP_SWIGLU) {
-    if (!attr_set[0]) {
-      cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-      attr_set[0] = true;
-    }
-    gemm_tc_kernel<0><<<num_sms, NTHREADS, SMEM_BYTES, s>>>(prm);
+    cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    gemm_tc_kernel<0><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
   } else {
-    if (!attr_set[1]) {
-      cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-      attr_set[1] = true;
-    }
-    gemm_tc_kernel<1><<<num_sms, NTHREADS, SMEM_BYTES, s>>>(prm);
+    cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    gemm_tc_kernel<1><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
   }
   note_launches(1);
   return cudaGetLastError();
