@@ -24,7 +24,7 @@ IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_GEMV = 0, 1, 2, 3
 IMPLS = {"auto": IMPL_AUTO, "simt": IMPL_SIMT, "tc": IMPL_TC, "gemv": IMPL_GEMV}
 
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
-SYMBOLS = ["moe_version", "moe_launch_count", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
+SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
            "moe_repacked_bytes", "moe_repack_w4", "moe_expert_gemm_w4", "moe_combine",
            "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns"]
 
@@ -54,6 +54,7 @@ _SIGS = {
     "moe_block_map_capacity": ([_i, _i, _i, _i], _i),
     "moe_route_workspace_size": ([_i, _i, _i, _i], _sz),
     "moe_route": ([_vp, _i, _i, _i, _i] + [_vp] * 9 + [_sz, _vp], _i),
+    "moe_route_noalloc": ([_vp, _i, _i, _i, _i] + [_vp] * 9, _i),
     "moe_repacked_bytes": ([_i, _i, _i], _sz),
     "moe_repack_w4": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
     "moe_expert_gemm_w4": ([_i, _i, _vp, _i, _i, _i, _i, _i] + [_vp] * 7 + [_i, _vp, _vp], _i),
@@ -133,6 +134,14 @@ def moe_route(logits, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_p
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _call("moe_route", _ptr(logits), T, E, k, block_n, _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets),
           _ptr(perm), _ptr(inv_perm), _ptr(block_map), _ptr(num_blocks), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def moe_route_noalloc(logits, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks,
+                      stream=None):
+    """moe_route with the library's own fixed scratch instead of a workspace (no allocation)."""
+    T, E = logits.shape
+    _call("moe_route_noalloc", _ptr(logits), T, E, k, block_n, _ptr(topk_ids), _ptr(topk_w), _ptr(counts),
+          _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(block_map), _ptr(num_blocks), _stream(stream))
 
 
 def moe_repack_w4(packed, scale, bias, gate_up, out, stream=None):

@@ -417,3 +417,65 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
 }
 
 }  // namespace moe
+
+// --------------------------------------------------------------------------
+// moe_route_noalloc: the same routing with its per-chunk counts kept in a
+// fixed device array owned by this library, for callers that are not allowed
+// to allocate device memory (see include/moe_w4.h).
+// --------------------------------------------------------------------------
+#include <mutex>
+
+// 256 chunks x 256 experts of int32 counts: every T this library accepts (at
+// most 256 chunks) with up to 256 routed experts.  Resident on each device
+// that loads the library until the process exits.
+static __device__ __align__(256) int32_t moe_route_scratch[256 * 256];
+
+namespace {
+
+constexpr size_t kRouteScratchBytes = sizeof(int32_t) * 256 * 256;
+
+// Device address of moe_route_scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in for the device symbol).
+void* route_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, moe_route_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int moe_route_noalloc(const float* logits, int T, int E, int k, int block_n, int32_t* topk_ids,
+                                 float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                 int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks,
+                                 moe_stream_t stream) {
+  if (T < 1 || T > (1 << 20) || E < 1 || E > 1024 || k < 1 || k > 32 || k > E || block_n < 1 || block_n > 1024)
+    return MOE_ERR_SHAPE;
+  const void* ptrs[] = {logits, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks};
+  for (const void* q : ptrs)
+    if (!q) return MOE_ERR_NULL;
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MOE_ERR_ALIGN;
+  const size_t need = moe::route_workspace_bytes(T, E, k);
+  if (need > kRouteScratchBytes) return MOE_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (need > 0) {
+    scratch = route_scratch_address();
+    if (!scratch) return MOE_ERR_CUDA;
+  }
+  if (!moe::device_error_ptr()) return MOE_ERR_CUDA;
+  const cudaError_t e = moe::launch_route(logits, T, E, k, block_n, topk_ids, topk_w, counts, offsets, perm,
+                                          inv_perm, block_map, num_blocks, scratch,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+

@@ -114,6 +114,34 @@ int moe_route(const float* logits, int T, int E, int k, int block_n,
               int32_t* perm, int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks,
               void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/*
+ * moe_route_noalloc -- moe_route for callers that may not allocate device
+ * memory: code handed only its input and output buffers by a host engine
+ * whose allocator owns the whole device (a serving process that reserves
+ * memory up front), or code on a latency path where cudaMalloc's implicit
+ * device-wide synchronisation is not acceptable.  The pages describe no such
+ * entry point; it has no counterpart there.
+ *
+ * Same arguments, outputs and limits as moe_route, without the workspace:
+ * the per-chunk expert counts live in one fixed 256 KiB device array of the
+ * library (256 chunks x 256 experts of int32), held on every GPU that loads
+ * the library until the process exits.  That covers every T for E <= 256;
+ * a call whose counts need more than 256 KiB (moe_route_workspace_size
+ * reports the need) returns MOE_ERR_WORKSPACE before enqueueing anything.
+ * For T*k <= 1024 no scratch is used.  Nothing is allocated or freed.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  The routing kernels overwrite every scratch
+ * entry before reading it, so nothing needs clearing between calls, but all
+ * calls share the one array: calls that can overlap on the GPU (different
+ * streams, or different host threads) race and must be serialised by the
+ * caller.
+ */
+int moe_route_noalloc(const float* logits, int T, int E, int k, int block_n,
+                      int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
+                      int32_t* perm, int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks,
+                      moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Weights                                                                  */
 /* ------------------------------------------------------------------------ */
