@@ -78,7 +78,7 @@ struct TcParams {
   const int32_t* num_blocks;
   void* out;
   int* err;
-  unsigned long long wait_ns;
+  unsigned long long wait_cycles;
   int T, H, F, E, k, bn, cap;
   int nb;       // activation ring depth
   int sb;       // bytes of one activation stage (boxr rows x 128 bytes)
@@ -86,18 +86,22 @@ struct TcParams {
   int lag;      // cp.async groups each gather thread keeps in flight
 };
 
+// Bounded waits.  The time limit is counted in SM clock cycles (clock64, cheap
+// to read) from the first unsuccessful try; `limit` is in cycles.
+//
 // Bounded wait on phase `parity` of `bar`.  Returns false on timeout or when
 // another role has already given up (s_abort).  Warp-uniform when called by
 // all lanes of a warp (the decision uses lane 0's clock).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
                                           unsigned long long limit) {
-  const unsigned long long t0 = ptx::globaltimer();
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
   for (uint32_t i = 0;; ++i) {
     const bool done = ptx::mbar_try_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
     if ((i & 15) == 15) {
       int give_up = *s_abort;
-      if (!give_up && ptx::globaltimer() - t0 > limit) give_up = 2;
+      if (!give_up && static_cast<unsigned long long>(clock64() - t0) > limit) give_up = 2;
       give_up = __shfl_sync(0xffffffffu, give_up, 0);
       if (give_up) {
         if (give_up == 2 && (threadIdx.x & 31) == 0) {
@@ -113,12 +117,13 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 // Single-thread variant.
 __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
                                          unsigned long long limit) {
-  const unsigned long long t0 = ptx::globaltimer();
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
   for (uint32_t i = 0;; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((i & 15) == 15) {
       if (*s_abort) return false;
-      if (ptx::globaltimer() - t0 > limit) {
+      if (static_cast<unsigned long long>(clock64() - t0) > limit) {
         set_device_error(err, MOE_DEV_TIMEOUT);
         *s_abort = 1;
         return false;
@@ -129,9 +134,10 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile
 
 // Wait that ignores s_abort (used to drain copies already in flight).
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
-  const unsigned long long t0 = ptx::globaltimer();
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  const long long t0 = clock64();
   while (!ptx::mbar_try_wait(bar, parity)) {
-    if (ptx::globaltimer() - t0 > limit) return;
+    if (static_cast<unsigned long long>(clock64() - t0) > limit) return;
   }
 }
 
@@ -215,7 +221,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const unsigned long long lim = p.wait_ns;
+  const unsigned long long lim = p.wait_cycles;
   int prod_w = 0, prod_b = 0;  // bulk/tensor copies issued (for the drain after a timeout)
 
   if (warp == 0) {
@@ -593,7 +599,8 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   prm.num_blocks = num_blocks;
   prm.out = out;
   prm.err = device_error_ptr();
-  prm.wait_ns = g_wait_ns;
+  // the limit is applied in SM cycles; 2.1 cycles per ns bounds the fastest SM clock
+  prm.wait_cycles = g_wait_ns > (~0ull) / 3 ? ~0ull : g_wait_ns * 21 / 10;
   prm.T = T;
   prm.H = H;
   prm.F = F;
