@@ -15,10 +15,15 @@
 //   M = 128 weight rows of one expert (one "M-tile"), N = the tile's token
 //   rows rounded up to 16 (<= 256), K stepped 64 at a time (one quant group).
 //
-// Roles (512 threads, one CTA per SM, persistent over (block-map tile, M-tile)):
+// Roles (512 threads, one CTA per SM, persistent over (block-map tile, M-tile)).
+// Warps 0-2 run their loops converged with warp-uniform operands and let
+// elect.sync pick the lane that issues each copy, MMA or commit:
 //   warp 0      bulk-copies the packed 4-bit block of each K step into smem
-//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (A from TMEM, B from smem)
-//   warps 2-3   gather the tile's token rows with cp.async into 128B-swizzled smem
+//   warp 1      allocates TMEM; issues tcgen05.mma (A from TMEM, B from smem)
+//   warp 2      loads the tile's activation rows into 128B-swizzled smem with
+//               TMA: gate/up gathers token rows of x four at a time
+//               (tile::gather4), down loads contiguous rows of h
+//   warp 3      idle
 //   warps 4-11  two dequant warpgroups (alternate K steps): nibbles -> bf16
 //               w = bf16(q*scale + bias) with one fma.rn.bf16x2 per pair,
 //               written to TMEM with tcgen05.st
@@ -49,7 +54,6 @@ constexpr int W_STAGE = W_PACKED + TC_M * 4;  // + (scale, bias) per row
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_A0 = 256;        // A ring columns 256..511; D uses 0..255
 constexpr int NTHREADS = 512;
-constexpr int GATHER_T = 64;        // threads of the gather warps (gate/up mode)
 
 // barrier indices
 constexpr int BAR_WFULL = 0;
@@ -65,7 +69,9 @@ constexpr int NBAR = BAR_FIN + 1;
 
 // smem layout (offsets from a 1024-byte aligned base): B ring | W ring | barriers | misc
 constexpr int W_RING_BYTES = NW * W_STAGE;
-constexpr int TAIL_BYTES = W_RING_BYTES + NBAR * 8 + 16;
+constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
+constexpr int MISC_BYTES = 16 + 256 * 4;  // abort flag, TMEM base, token rows of the current tile
+constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;
 
 static_assert(W_STAGE % 16 == 0, "bulk copies move multiples of 16 bytes");
 
@@ -83,7 +89,6 @@ struct TcParams {
   int nb;       // activation ring depth
   int sb;       // bytes of one activation stage (boxr rows x 128 bytes)
   int nd;       // accumulator buffers (2 when tiles have <= 128 rows)
-  int lag;      // cp.async groups each gather thread keeps in flight
 };
 
 // Bounded waits.  The time limit is counted in SM clock cycles (clock64, cheap
@@ -108,24 +113,6 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
           set_device_error(err, MOE_DEV_TIMEOUT);
           *s_abort = 1;
         }
-        return false;
-      }
-    }
-  }
-}
-
-// Single-thread variant.
-__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
-                                         unsigned long long limit) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (uint32_t i = 0;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 15) == 15) {
-      if (*s_abort) return false;
-      if (static_cast<unsigned long long>(clock64() - t0) > limit) {
-        set_device_error(err, MOE_DEV_TIMEOUT);
-        *s_abort = 1;
         return false;
       }
     }
@@ -176,8 +163,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t off_w = static_cast<uint32_t>(NB * SB);
   const uint32_t bar0 = sbase + off_w + W_RING_BYTES;
   auto bar = [bar0](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + off_w + W_RING_BYTES + NBAR * 8);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + off_w + W_RING_BYTES + NBAR * 8 + 4);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + off_w + W_RING_BYTES + BAR_BYTES);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + off_w + W_RING_BYTES + BAR_BYTES + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = MODE == 0 ? p.H : p.F;
@@ -203,7 +190,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ptx::mbar_init(bar(BAR_AEMPTY + s), 1);
     }
     for (int s = 0; s < NBMAX; ++s) {
-      ptx::mbar_init(bar(BAR_BFULL + s), MODE == 0 ? GATHER_T : 1);
+      ptx::mbar_init(bar(BAR_BFULL + s), 1);
       ptx::mbar_init(bar(BAR_BEMPTY + s), 1);
     }
     for (int d = 0; d < 2; ++d) {
@@ -225,134 +212,103 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   int prod_w = 0, prod_b = 0;  // bulk/tensor copies issued (for the drain after a timeout)
 
   if (warp == 0) {
-    // ------------------------------------------------ packed-weight producer
-    if (lane == 0) {
-      int& it = prod_w;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        Tile t;
-        int mt;
-        if (!unit_tile(p, u, MT, &t, &mt)) continue;
-        const uint8_t* src = p.w + (static_cast<size_t>(t.expert) * MT + mt) * KT * static_cast<size_t>(W_STAGE);
-        for (int kg = 0; kg < KT; ++kg, ++it) {
-          const int s = it % NW, r = it / NW;
-          if (r > 0 && !wait_one(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto producer_done;
-          ptx::mbar_arrive_expect_tx(bar(BAR_WFULL + s), W_STAGE);
-          ptx::bulk_g2s(sbase + off_w + s * W_STAGE, src + static_cast<size_t>(kg) * W_STAGE, W_STAGE,
-                        bar(BAR_WFULL + s));
-        }
+    // ------------------------------------------------ packed-weight producer (whole warp, one lane issues)
+    int& it = prod_w;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      Tile t;
+      int mt;
+      if (!unit_tile(p, u, MT, &t, &mt)) continue;
+      const uint8_t* src = p.w + (static_cast<size_t>(t.expert) * MT + mt) * KT * static_cast<size_t>(W_STAGE);
+      for (int kg = 0; kg < KT; ++kg, ++it) {
+        const int s = it % NW, r = it / NW;
+        if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto producer_done;
+        ptx::mbar_arrive_expect_tx_elect(bar(BAR_WFULL + s), W_STAGE);
+        ptx::bulk_g2s_elect(sbase + off_w + s * W_STAGE, src + static_cast<size_t>(kg) * W_STAGE, W_STAGE,
+                            bar(BAR_WFULL + s));
       }
-    producer_done:;
     }
+  producer_done:;
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int it = 0, ui = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        Tile t;
-        int mt;
-        if (!unit_tile(p, u, MT, &t, &mt)) continue;
-        const uint32_t idesc = ptx::idesc_bf16_f32(TC_M, round16(t.rows));
-        const int d = ui % ND, rd = ui / ND;
-        if (rd > 0 && !wait_one(bar(BAR_DEMPTY + d), (rd - 1) & 1, s_abort, p.err, lim)) goto mma_done;
+    // ------------------------------------------------ MMA issuer (whole warp, one lane issues)
+    int it = 0, ui = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      Tile t;
+      int mt;
+      if (!unit_tile(p, u, MT, &t, &mt)) continue;
+      const uint32_t idesc = ptx::idesc_bf16_f32(TC_M, round16(t.rows));
+      const int d = ui % ND, rd = ui / ND;
+      if (rd > 0 && !wait_warp(bar(BAR_DEMPTY + d), (rd - 1) & 1, s_abort, p.err, lim)) goto mma_done;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem + d * DCOLS;
+      for (int kg = 0; kg < KT; ++kg, ++it) {
+        const int sa = it % NA, sb = it % NB;
+        if (!wait_warp(bar(BAR_AFULL + sa), (it / NA) & 1, s_abort, p.err, lim)) goto mma_done;
+        if (!wait_warp(bar(BAR_BFULL + sb), (it / NB) & 1, s_abort, p.err, lim)) goto mma_done;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem + d * DCOLS;
-        for (int kg = 0; kg < KT; ++kg, ++it) {
-          const int sa = it % NA, sb = it % NB;
-          if (!wait_one(bar(BAR_AFULL + sa), (it / NA) & 1, s_abort, p.err, lim)) goto mma_done;
-          if (!wait_one(bar(BAR_BFULL + sb), (it / NB) & 1, s_abort, p.err, lim)) goto mma_done;
-          ptx::tc_fence_after();
-          const uint32_t a_tmem = tmem + TMEM_A0 + 32 * sa;
-          const uint64_t bdesc = ptx::smem_desc_sw128(sbase + sb * SB);
-#pragma unroll
-          for (int j = 0; j < KG / 16; ++j)
-            ptx::mma_ts(d_tmem, a_tmem + 8 * j, bdesc + 2 * j, idesc, (kg | j) != 0);
-          ptx::mma_commit(bar(BAR_AEMPTY + sa));
-          ptx::mma_commit(bar(BAR_BEMPTY + sb));
-        }
-        ptx::mma_commit(bar(BAR_DFULL + d));
-        ++ui;
+        const uint32_t a_tmem = tmem + TMEM_A0 + 32 * sa;
+        const uint64_t bdesc = ptx::smem_desc_sw128(sbase + sb * SB);
+        ptx::mma_ts_elect(d_tmem, a_tmem, bdesc, idesc, kg != 0);
+        ptx::mma_ts_elect(d_tmem, a_tmem + 8, bdesc + 2, idesc, 1);
+        ptx::mma_ts_elect(d_tmem, a_tmem + 16, bdesc + 4, idesc, 1);
+        ptx::mma_ts_elect(d_tmem, a_tmem + 24, bdesc + 6, idesc, 1);
+        ptx::mma_commit_elect(bar(BAR_AEMPTY + sa));
+        ptx::mma_commit_elect(bar(BAR_BEMPTY + sb));
       }
-    mma_done:
-      ptx::mma_commit(bar(BAR_FIN));
-      wait_drain(bar(BAR_FIN), 0, lim);
+      ptx::mma_commit_elect(bar(BAR_DFULL + d));
+      ++ui;
     }
-  } else if (warp < 4) {
-    if (MODE == 1) {
-      // ------------------------------------------------ activation producer (TMA, contiguous rows)
-      if (warp == 2 && lane == 0) {
-        int& it = prod_b;
-        const uint32_t bytes = static_cast<uint32_t>(SB);
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-          Tile t;
-          int mt;
-          if (!unit_tile(p, u, MT, &t, &mt)) continue;
-          for (int kg = 0; kg < KT; ++kg, ++it) {
-            const int s = it % NB, r = it / NB;
-            if (r > 0 && !wait_one(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto bprod_done;
-            ptx::mbar_arrive_expect_tx(bar(BAR_BFULL + s), bytes);
-            ptx::tma_load_2d(sbase + s * SB, &tmap_act, kg * KG, t.row0, bar(BAR_BFULL + s));
-          }
-        }
-      bprod_done:;
-      }
-    } else {
-      // ------------------------------------------------ activation gather (cp.async, token rows)
-      const int gt = threadIdx.x - 64;  // 0..63
-      const int chunk = gt & 7, row_a = gt >> 3;
-      const int lag = p.lag;
-      int it = 0;
-      bool aborted = false;
-      for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
-        Tile t;
-        int mt;
-        if (!unit_tile(p, u, MT, &t, &mt)) continue;
-        int src_row[256 / 8];
-#pragma unroll
-        for (int j = 0; j < 256 / 8; ++j) {
-          const int i = row_a + 8 * j;
-          int sr = -1;
+  mma_done:
+    ptx::mma_commit_elect(bar(BAR_FIN));
+    if (lane == 0) wait_drain(bar(BAR_FIN), 0, lim);
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------ activation producer (whole warp, one lane issues)
+    int& it = prod_b;
+    int* s_tok = reinterpret_cast<int*>(smem + off_w + W_RING_BYTES + BAR_BYTES + 16);  // [256], this warp only
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      Tile t;
+      int mt;
+      if (!unit_tile(p, u, MT, &t, &mt)) continue;
+      const int N = round16(t.rows);
+      if (MODE == 0) {
+        // token row of every tile row (padding rows read token 0; their columns are never used)
+        __syncwarp();
+        for (int i = lane; i < N; i += 32) {
+          int tok = 0;
           if (i < t.rows) {
             const int r = t.row0 + i;
             if (r < A) {
               const int a = __ldg(p.perm + r);
-              if (a >= 0 && a < A) sr = a / p.k;
+              if (a >= 0 && a < A) tok = a / p.k;
               else set_device_error(p.err, MOE_DEV_BAD_INDEX);
             } else {
-              sr = r - A;
+              tok = r - A;
             }
           }
-          src_row[j] = sr;
+          s_tok[i] = tok;
         }
-        for (int kg = 0; kg < KT; ++kg, ++it) {
-          const int s = it % NB, r = it / NB;
-          if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) {
-            aborted = true;
-            break;
-          }
-          const uint32_t dst0 = sbase + s * SB;
-#pragma unroll
-          for (int j = 0; j < 256 / 8; ++j) {
-            const int i = row_a + 8 * j;
-            if (src_row[j] >= 0) {
-              const uint16_t* src = p.act + static_cast<size_t>(src_row[j]) * K + kg * KG + chunk * 8;
-              const uint32_t dst = dst0 + (i >> 3) * 1024 + (i & 7) * 128 + ((chunk ^ (i & 7)) << 4);
-              ptx::cp_async_16(dst, src);
-            }
-          }
-          ptx::cp_async_commit();
-          if (it >= lag) {
-            ptx::cp_async_wait_n(lag);
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(bar(BAR_BFULL + (it - lag) % NB));
-          }
-        }
+        __syncwarp();
       }
-      ptx::cp_async_wait_all();
-      if (!aborted && !*s_abort) {
-        ptx::fence_proxy_async_smem();
-        for (int t = it - lag < 0 ? 0 : it - lag; t < it; ++t) ptx::mbar_arrive(bar(BAR_BFULL + t % NB));
+      for (int kg = 0; kg < KT; ++kg, ++it) {
+        const int s = it % NB, r = it / NB;
+        if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto bprod_done;
+        const uint32_t dst = sbase + s * SB;
+        if (MODE == 1) {
+          ptx::mbar_arrive_expect_tx_elect(bar(BAR_BFULL + s), static_cast<uint32_t>(SB));
+          ptx::tma_load_2d_elect(dst, &tmap_act, kg * KG, t.row0, bar(BAR_BFULL + s));
+        } else {
+          ptx::mbar_arrive_expect_tx_elect(bar(BAR_BFULL + s), static_cast<uint32_t>(N * 128));
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            if (4 * c < N) {
+              const int4 tk = *reinterpret_cast<const int4*>(s_tok + 4 * c);
+              ptx::tma_gather4_elect(dst + 512 * c, &tmap_act, kg * KG, tk.x, tk.y, tk.z, tk.w, bar(BAR_BFULL + s));
+            }
+          }
+        }
       }
     }
+  bprod_done:;
   } else if (warp < 12) {
     // ------------------------------------------------ dequant (two warpgroups, alternate K steps)
     const int wg = (warp - 4) >> 2;
@@ -476,7 +432,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0 && lane == 0)
       for (int t = prod_w - NW < 0 ? 0 : prod_w - NW; t < prod_w; ++t)
         wait_drain(bar(BAR_WFULL + t % NW), (t / NW) & 1, lim);
-    if (MODE == 1 && warp == 2 && lane == 0)
+    if (warp == 2 && lane == 0)
       for (int t = prod_b - NB < 0 ? 0 : prod_b - NB; t < prod_b; ++t)
         wait_drain(bar(BAR_BFULL + t % NB), (t / NB) & 1, lim);
   }
@@ -616,18 +572,21 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   if (nbs < 3) return cudaErrorInvalidValue;
   prm.nb = nbs;
   prm.nd = boxr <= 128 ? 2 : 1;
-  prm.lag = nbs - 1 < 6 ? nbs - 1 : 6;
   const int smem = nbs * prm.sb + TAIL_BYTES + 1024;
 
+  // activation tensor map: gate/up gathers single token rows of x [T, H] four at a
+  // time (one-row box); down loads whole tiles of h [A+T, F] (boxr-row box)
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
-  if (mode == MOE_DOWN_COMBINE) {
+  {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int A = T * k;
-    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(F), static_cast<cuuint64_t>(A + T)};
-    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(F) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(boxr)};
+    const bool down = mode == MOE_DOWN_COMBINE;
+    const cuuint64_t K = static_cast<cuuint64_t>(down ? F : H);
+    cuuint64_t gdim[2] = {K, static_cast<cuuint64_t>(down ? A + T : T)};
+    cuuint64_t gstride[1] = {K * 2};
+    cuuint32_t box[2] = {64, down ? static_cast<cuuint32_t>(boxr) : 1u};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(act), gdim, gstride, box,
                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
