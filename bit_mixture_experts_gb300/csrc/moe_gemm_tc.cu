@@ -18,7 +18,8 @@
 // Roles (512 threads, one CTA per SM, persistent over (block-map tile, M-tile)).
 // Warps 0-2 run their loops converged with warp-uniform operands and let
 // elect.sync pick the lane that issues each copy, MMA or commit:
-//   warp 0      bulk-copies the packed 4-bit block of each K step into smem
+//   warp 0      copies the packed 4-bit block of each K step into smem with
+//               per-lane cp.async (completion counted on an mbarrier)
 //   warp 1      allocates TMEM; issues tcgen05.mma (A from TMEM, B from smem)
 //   warp 2      loads the tile's activation rows into 128B-swizzled smem with
 //               TMA: gate/up gathers token rows of x four at a time
@@ -73,7 +74,7 @@ constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
 constexpr int MISC_BYTES = 16 + 256 * 4;  // abort flag, TMEM base, token rows of the current tile
 constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;
 
-static_assert(W_STAGE % 16 == 0, "bulk copies move multiples of 16 bytes");
+static_assert(W_STAGE % (16 * 32) == 0, "the weight block is copied as 16-byte chunks by 32 lanes");
 
 struct TcParams {
   const uint16_t* act;
@@ -101,20 +102,19 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
                                           unsigned long long limit) {
   if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
   const long long t0 = clock64();
-  for (uint32_t i = 0;; ++i) {
-    const bool done = ptx::mbar_try_wait(bar, parity);
+  for (;;) {
+    // sleep until the phase completes (or 20 us pass) rather than polling
+    const bool done = ptx::mbar_try_wait_sleep(bar, parity, 20000u);
     if (__all_sync(0xffffffffu, done)) return true;
-    if ((i & 15) == 15) {
-      int give_up = *s_abort;
-      if (!give_up && static_cast<unsigned long long>(clock64() - t0) > limit) give_up = 2;
-      give_up = __shfl_sync(0xffffffffu, give_up, 0);
-      if (give_up) {
-        if (give_up == 2 && (threadIdx.x & 31) == 0) {
-          set_device_error(err, MOE_DEV_TIMEOUT);
-          *s_abort = 1;
-        }
-        return false;
+    int give_up = *s_abort;
+    if (!give_up && static_cast<unsigned long long>(clock64() - t0) > limit) give_up = 2;
+    give_up = __shfl_sync(0xffffffffu, give_up, 0);
+    if (give_up) {
+      if (give_up == 2 && (threadIdx.x & 31) == 0) {
+        set_device_error(err, MOE_DEV_TIMEOUT);
+        *s_abort = 1;
       }
+      return false;
     }
   }
 }
@@ -123,7 +123,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
   if (ptx::mbar_try_wait(bar, parity)) return;
   const long long t0 = clock64();
-  while (!ptx::mbar_try_wait(bar, parity)) {
+  while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (static_cast<unsigned long long>(clock64() - t0) > limit) return;
   }
 }
@@ -148,7 +148,7 @@ __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
 // Rings (each with full/empty mbarriers, stage index = running K-step count
 // `it` modulo the ring depth):
-//   W  packed 4-bit blocks, smem, bulk copy -> dequant warps
+//   W  packed 4-bit blocks, smem, cp.async -> dequant warps
 //   A  dequantised bf16 weights, TMEM, dequant warps -> MMA
 //   B  activation rows (128B-swizzled, K-major), smem, gather/TMA -> MMA
 //   D  FP32 accumulators, TMEM, MMA -> epilogue (1 or 2 buffers)
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     *s_abort = 0;
     for (int s = 0; s < NW; ++s) {
-      ptx::mbar_init(bar(BAR_WFULL + s), 1);
+      ptx::mbar_init(bar(BAR_WFULL + s), 32);
       ptx::mbar_init(bar(BAR_WEMPTY + s), 4);
     }
     for (int s = 0; s < NA; ++s) {
@@ -222,12 +222,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int kg = 0; kg < KT; ++kg, ++it) {
         const int s = it % NW, r = it / NW;
         if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto producer_done;
-        ptx::mbar_arrive_expect_tx_elect(bar(BAR_WFULL + s), W_STAGE);
-        ptx::bulk_g2s_elect(sbase + off_w + s * W_STAGE, src + static_cast<size_t>(kg) * W_STAGE, W_STAGE,
-                            bar(BAR_WFULL + s));
+        // per-lane 16-byte async copies (load/store unit, not the TMA engine, which
+        // stays free for the activation tiles); the barrier counts the 32 lanes
+        const uint8_t* g = src + static_cast<size_t>(kg) * W_STAGE;
+        const uint32_t d = sbase + off_w + s * W_STAGE;
+#pragma unroll
+        for (int c = 0; c < W_STAGE / 16 / 32; ++c) ptx::cp_async_16(d + (c * 32 + lane) * 16, g + (c * 32 + lane) * 16);
+        ptx::cp_async_mbar_arrive(bar(BAR_WFULL + s));
       }
     }
-  producer_done:;
+  producer_done:
+    ptx::cp_async_wait_all();  // no copy of this warp may still be landing when the CTA exits
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (whole warp, one lane issues)
     int it = 0, ui = 0;
@@ -298,12 +303,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ptx::tma_load_2d_elect(dst, &tmap_act, kg * KG, t.row0, bar(BAR_BFULL + s));
         } else {
           ptx::mbar_arrive_expect_tx_elect(bar(BAR_BFULL + s), static_cast<uint32_t>(N * 128));
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            if (4 * c < N) {
-              const int4 tk = *reinterpret_cast<const int4*>(s_tok + 4 * c);
-              ptx::tma_gather4_elect(dst + 512 * c, &tmap_act, kg * KG, tk.x, tk.y, tk.z, tk.w, bar(BAR_BFULL + s));
-            }
+#pragma unroll 1
+          for (int c = 0; c < N / 4; ++c) {
+            const int4 tk = *reinterpret_cast<const int4*>(s_tok + 4 * c);
+            ptx::tma_gather4_elect(dst + 512 * c, &tmap_act, kg * KG, tk.x, tk.y, tk.z, tk.w, bar(BAR_BFULL + s));
           }
         }
       }
@@ -429,9 +432,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (*s_abort) {
     // after a timeout some copies may never have been consumed: let them land before the CTA exits
-    if (warp == 0 && lane == 0)
-      for (int t = prod_w - NW < 0 ? 0 : prod_w - NW; t < prod_w; ++t)
-        wait_drain(bar(BAR_WFULL + t % NW), (t / NW) & 1, lim);
     if (warp == 2 && lane == 0)
       for (int t = prod_b - NB < 0 ? 0 : prod_b - NB; t < prod_b; ++t)
         wait_drain(bar(BAR_BFULL + t % NB), (t / NB) & 1, lim);
