@@ -141,7 +141,7 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
   if (impl == MOE_IMPL_AUTO) impl = MOE_IMPL_TC;
   switch (impl) {
     case MOE_IMPL_TC:
-      if (block_n > 256 || H % 128 != 0) return MOE_ERR_SHAPE;
+      if (block_n > 128 || H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
       return cuda_status(launch_gemm_tc(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
                                         block_n, cap, out, num_sms(), s));
     case MOE_IMPL_SIMT:

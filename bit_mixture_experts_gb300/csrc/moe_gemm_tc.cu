@@ -45,16 +45,23 @@ namespace moe {
 
 namespace {
 
-constexpr int TC_M = 128;           // weight rows per M-tile
-constexpr int KG = 64;              // K per pipeline stage (= one quant group)
-constexpr int NW = 12;              // packed-weight ring (smem)
-constexpr int NA = 8;               // dequantised-weight ring (TMEM, 32 columns each)
-constexpr int NBMAX = 16;           // activation ring (smem), run-time depth <= NBMAX
-constexpr int W_PACKED = TC_M * 32; // packed nibbles of one M-tile x K group
-constexpr int W_STAGE = W_PACKED + TC_M * 4;  // + (scale, bias) per row
+constexpr int TC_M = 128;              // weight rows per M-tile (the MMA's M)
+constexpr int MG = 2;                  // M-tiles per work unit; they share each activation stage
+constexpr int KG = 64;                 // one quantisation group
+constexpr int GPS = 2;                 // quant groups per pipeline stage
+constexpr int KS = KG * GPS;           // K per stage
+constexpr int W_PACKED = TC_M * 32;    // packed nibbles of one M-tile x K group
+constexpr int W_BLOCK = W_PACKED + TC_M * 4;  // + (scale, bias) per row: one repacked block
+constexpr int W_STAGE = MG * GPS * W_BLOCK;   // packed weights of one stage
+constexpr int NW = 4;                  // packed-weight ring (smem)
+constexpr int A_COLS = MG * GPS * 32;  // TMEM columns of one dequantised stage
+constexpr int NA = 2;                  // dequantised-weight ring (TMEM)
+constexpr int NBMAX = 12;              // activation ring (smem), run-time depth <= NBMAX
 constexpr int TMEM_COLS = 512;
-constexpr int TMEM_A0 = 256;        // A ring columns 256..511; D uses 0..255
+constexpr int TMEM_A0 = 256;           // A ring in columns 256..511; accumulators in 0..255
 constexpr int NTHREADS = 512;
+constexpr int GATHER_T = 64;           // threads gathering activation rows (gate/up)
+constexpr int LAGMAX = 8;
 
 // barrier indices
 constexpr int BAR_WFULL = 0;
@@ -71,10 +78,10 @@ constexpr int NBAR = BAR_FIN + 1;
 // smem layout (offsets from a 1024-byte aligned base): B ring | W ring | barriers | misc
 constexpr int W_RING_BYTES = NW * W_STAGE;
 constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
-constexpr int MISC_BYTES = 16 + 256 * 4;  // abort flag, TMEM base, token rows of the current tile
+constexpr int MISC_BYTES = 16;  // abort flag, TMEM base
 constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;
 
-static_assert(W_STAGE % (16 * 32) == 0, "the weight block is copied as 16-byte chunks by 32 lanes");
+static_assert((GPS * W_BLOCK) % (16 * 32) == 0, "a weight stage is copied as 16-byte chunks by 32 lanes");
 
 struct TcParams {
   const uint16_t* act;
@@ -87,17 +94,19 @@ struct TcParams {
   int* err;
   unsigned long long wait_cycles;
   int T, H, F, E, k, bn, cap;
+  int boxr;     // activation rows per stage buffer (block_n rounded up to 16, <= 128)
   int nb;       // activation ring depth
-  int sb;       // bytes of one activation stage (boxr rows x 128 bytes)
-  int nd;       // accumulator buffers (2 when tiles have <= 128 rows)
+  int sb;       // bytes of one activation stage: GPS atoms of boxr rows x 128 bytes
+  int nd;       // accumulator buffers (2 when tiles have <= 64 rows)
+  int lag;      // cp.async groups each gather thread keeps in flight
 };
 
 // Bounded waits.  The time limit is counted in SM clock cycles (clock64, cheap
 // to read) from the first unsuccessful try; `limit` is in cycles.
 //
-// Bounded wait on phase `parity` of `bar`.  Returns false on timeout or when
-// another role has already given up (s_abort).  Warp-uniform when called by
-// all lanes of a warp (the decision uses lane 0's clock).
+// Bounded wait on phase `parity` of `bar` by a whole warp.  Returns false on
+// timeout or when another role has already given up (s_abort); the decision
+// is warp-uniform (lane 0's clock).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
                                           unsigned long long limit) {
   if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
@@ -128,11 +137,11 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsign
   }
 }
 
-// Block-map entry of unit u; false for a malformed entry (the same decision
-// in every role, so all roles skip it together).
-__device__ __forceinline__ bool unit_tile(const TcParams& p, int u, int MT, Tile* t, int* mt) {
-  const int b = u / MT;
-  *mt = u - b * MT;
+// Unit u = (block-map tile u / MGT, M-group u % MGT).  False for a malformed
+// entry (the same decision in every role, so all roles skip it together).
+__device__ __forceinline__ bool unit_tile(const TcParams& p, int u, int MGT, Tile* t, int* grp) {
+  const int b = u / MGT;
+  *grp = u - b * MGT;
   t->expert = __ldg(p.block_map + 3 * b);
   t->row0 = __ldg(p.block_map + 3 * b + 1);
   t->rows = __ldg(p.block_map + 3 * b + 2);
@@ -146,11 +155,18 @@ __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
 }  // namespace
 
-// Rings (each with full/empty mbarriers, stage index = running K-step count
-// `it` modulo the ring depth):
-//   W  packed 4-bit blocks, smem, cp.async -> dequant warps
-//   A  dequantised bf16 weights, TMEM, dequant warps -> MMA
-//   B  activation rows (128B-swizzled, K-major), smem, gather/TMA -> MMA
+// Work unit: one block-map tile (<= 128 token rows) x MG = 2 M-tiles (256
+// weight rows) of one expert.  Each pipeline stage covers K = 128 (two quant
+// groups): both M-tiles' packed blocks, their dequantised bf16 in TMEM and one
+// activation stage read by both M-tiles' MMAs.
+//
+// Rings (full/empty mbarriers; stage index = running stage count `it` modulo
+// the ring depth):
+//   W  packed 4-bit blocks, smem, cp.async (warp 0) -> dequant warps
+//   A  dequantised bf16 weights, TMEM, dequant warps -> MMA (warp 1)
+//   B  activation rows, 128B-swizzled K-major atoms of 64 K, smem,
+//      gate/up: cp.async gather of token rows (warps 2-3),
+//      down: TMA tiles of contiguous h rows (warp 2)  -> MMA
 //   D  FP32 accumulators, TMEM, MMA -> epilogue (1 or 2 buffers)
 template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -159,7 +175,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
-  const int NB = p.nb, SB = p.sb, ND = p.nd;
+  const int NB = p.nb, SB = p.sb, ND = p.nd, BOXR = p.boxr;
+  const uint32_t atom_bytes = static_cast<uint32_t>(BOXR) * 128u;
   const uint32_t off_w = static_cast<uint32_t>(NB * SB);
   const uint32_t bar0 = sbase + off_w + W_RING_BYTES;
   auto bar = [bar0](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -168,29 +185,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = MODE == 0 ? p.H : p.F;
-  const int KT = K / KG;
+  const int KT = K / KG;                     // quant groups along K
+  const int NS = K / KS;                     // stages per unit
   const int MT = MODE == 0 ? (2 * p.F) / TC_M : p.H / TC_M;
+  const int MGT = (MT + MG - 1) / MG;        // M-groups per tile
   const int A = p.T * p.k;
-  const int DCOLS = ND == 2 ? 128 : 256;
+  const int DBUF = ND == 2 ? 128 : 256;      // columns per accumulator buffer
+  const int DM = DBUF / MG;                  // columns per M-tile accumulator
   int nb = __ldg(p.num_blocks);
   if (nb < 0 || nb > p.cap) {
     if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(p.err, MOE_DEV_BAD_BLOCK);
     nb = nb < 0 ? 0 : p.cap;
   }
-  const int units = nb * MT;
+  const int units = nb * MGT;
 
   if (threadIdx.x == 0) {
     *s_abort = 0;
     for (int s = 0; s < NW; ++s) {
       ptx::mbar_init(bar(BAR_WFULL + s), 32);
-      ptx::mbar_init(bar(BAR_WEMPTY + s), 4);
+      ptx::mbar_init(bar(BAR_WEMPTY + s), 8);
     }
     for (int s = 0; s < NA; ++s) {
-      ptx::mbar_init(bar(BAR_AFULL + s), 4);
+      ptx::mbar_init(bar(BAR_AFULL + s), 8);
       ptx::mbar_init(bar(BAR_AEMPTY + s), 1);
     }
     for (int s = 0; s < NBMAX; ++s) {
-      ptx::mbar_init(bar(BAR_BFULL + s), 1);
+      ptx::mbar_init(bar(BAR_BFULL + s), MODE == 0 ? GATHER_T : 1);
       ptx::mbar_init(bar(BAR_BEMPTY + s), 1);
     }
     for (int d = 0; d < 2; ++d) {
@@ -209,25 +229,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const unsigned long long lim = p.wait_cycles;
-  int prod_w = 0, prod_b = 0;  // bulk/tensor copies issued (for the drain after a timeout)
+  int prod_b = 0;  // activation TMA stages issued (down), for the drain after a timeout
 
   if (warp == 0) {
-    // ------------------------------------------------ packed-weight producer (whole warp, one lane issues)
-    int& it = prod_w;
+    // ------------------------------------------------ packed-weight producer (cp.async, 32 lanes)
+    int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
-      int mt;
-      if (!unit_tile(p, u, MT, &t, &mt)) continue;
-      const uint8_t* src = p.w + (static_cast<size_t>(t.expert) * MT + mt) * KT * static_cast<size_t>(W_STAGE);
-      for (int kg = 0; kg < KT; ++kg, ++it) {
+      int grp;
+      if (!unit_tile(p, u, MGT, &t, &grp)) continue;
+      const int nm = min(MG, MT - grp * MG);
+      for (int ks = 0; ks < NS; ++ks, ++it) {
         const int s = it % NW, r = it / NW;
         if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto producer_done;
-        // per-lane 16-byte async copies (load/store unit, not the TMA engine, which
-        // stays free for the activation tiles); the barrier counts the 32 lanes
-        const uint8_t* g = src + static_cast<size_t>(kg) * W_STAGE;
-        const uint32_t d = sbase + off_w + s * W_STAGE;
-#pragma unroll
-        for (int c = 0; c < W_STAGE / 16 / 32; ++c) ptx::cp_async_16(d + (c * 32 + lane) * 16, g + (c * 32 + lane) * 16);
+        for (int m = 0; m < nm; ++m) {
+          const uint8_t* g = p.w + ((static_cast<size_t>(t.expert) * MT + grp * MG + m) * KT + ks * GPS) *
+                                       static_cast<size_t>(W_BLOCK);
+          const uint32_t d = sbase + off_w + s * W_STAGE + m * GPS * W_BLOCK;
+#pragma unroll 6
+          for (int c = 0; c < GPS * W_BLOCK / 16 / 32; ++c)
+            ptx::cp_async_16(d + (c * 32 + lane) * 16, g + (c * 32 + lane) * 16);
+        }
         ptx::cp_async_mbar_arrive(bar(BAR_WFULL + s));
       }
     }
@@ -238,24 +260,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int it = 0, ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
-      int mt;
-      if (!unit_tile(p, u, MT, &t, &mt)) continue;
+      int grp;
+      if (!unit_tile(p, u, MGT, &t, &grp)) continue;
+      const bool two = grp * MG + 1 < MT;
       const uint32_t idesc = ptx::idesc_bf16_f32(TC_M, round16(t.rows));
       const int d = ui % ND, rd = ui / ND;
       if (rd > 0 && !wait_warp(bar(BAR_DEMPTY + d), (rd - 1) & 1, s_abort, p.err, lim)) goto mma_done;
       ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem + d * DCOLS;
-      for (int kg = 0; kg < KT; ++kg, ++it) {
+      const uint32_t d0 = tmem + d * DBUF, d1 = d0 + DM;
+      for (int ks = 0; ks < NS; ++ks, ++it) {
         const int sa = it % NA, sb = it % NB;
         if (!wait_warp(bar(BAR_AFULL + sa), (it / NA) & 1, s_abort, p.err, lim)) goto mma_done;
         if (!wait_warp(bar(BAR_BFULL + sb), (it / NB) & 1, s_abort, p.err, lim)) goto mma_done;
         ptx::tc_fence_after();
-        const uint32_t a_tmem = tmem + TMEM_A0 + 32 * sa;
-        const uint64_t bdesc = ptx::smem_desc_sw128(sbase + sb * SB);
-        ptx::mma_ts_elect(d_tmem, a_tmem, bdesc, idesc, kg != 0);
-        ptx::mma_ts_elect(d_tmem, a_tmem + 8, bdesc + 2, idesc, 1);
-        ptx::mma_ts_elect(d_tmem, a_tmem + 16, bdesc + 4, idesc, 1);
-        ptx::mma_ts_elect(d_tmem, a_tmem + 24, bdesc + 6, idesc, 1);
+        const uint32_t a0 = tmem + TMEM_A0 + sa * A_COLS;
+        const uint32_t b0 = sbase + sb * SB;
+#pragma unroll
+        for (int j = 0; j < KS / 16; ++j) {
+          const uint64_t bdesc = ptx::smem_desc_sw128(b0 + (j >> 2) * atom_bytes) + 2 * (j & 3);
+          const uint32_t acc = (ks | j) != 0;
+          ptx::mma_ts_elect(d0, a0 + 8 * j, bdesc, idesc, acc);
+          if (two) ptx::mma_ts_elect(d1, a0 + GPS * 32 + 8 * j, bdesc, idesc, acc);
+        }
         ptx::mma_commit_elect(bar(BAR_AEMPTY + sa));
         ptx::mma_commit_elect(bar(BAR_BEMPTY + sb));
       }
@@ -266,78 +292,118 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ptx::mma_commit_elect(bar(BAR_FIN));
     if (lane == 0) wait_drain(bar(BAR_FIN), 0, lim);
     __syncwarp();
-  } else if (warp == 2) {
-    // ------------------------------------------------ activation producer (whole warp, one lane issues)
-    int& it = prod_b;
-    int* s_tok = reinterpret_cast<int*>(smem + off_w + W_RING_BYTES + BAR_BYTES + 16);  // [256], this warp only
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      Tile t;
-      int mt;
-      if (!unit_tile(p, u, MT, &t, &mt)) continue;
-      const int N = round16(t.rows);
-      if (MODE == 0) {
-        // token row of every tile row (padding rows read token 0; their columns are never used)
-        __syncwarp();
-        for (int i = lane; i < N; i += 32) {
-          int tok = 0;
+  } else if (warp < 4) {
+    if (MODE == 1) {
+      // ------------------------------------------------ activation producer: TMA tiles of h rows
+      if (warp == 2) {
+        int& it = prod_b;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+          Tile t;
+          int grp;
+          if (!unit_tile(p, u, MGT, &t, &grp)) continue;
+          for (int ks = 0; ks < NS; ++ks, ++it) {
+            const int s = it % NB, r = it / NB;
+            if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto bprod_done;
+            const uint32_t dst = sbase + s * SB;
+            ptx::mbar_arrive_expect_tx_elect(bar(BAR_BFULL + s), static_cast<uint32_t>(SB));
+            for (int a = 0; a < GPS; ++a)
+              ptx::tma_load_2d_elect(dst + a * atom_bytes, &tmap_act, ks * KS + a * KG, t.row0, bar(BAR_BFULL + s));
+          }
+        }
+      bprod_done:;
+      }
+    } else {
+      // ------------------------------------------------ activation gather: token rows of x by cp.async
+      const int gt = threadIdx.x - 64;  // 0..63
+      const int chunk = gt & 7, row_a = gt >> 3;
+      const int lag = p.lag;
+      int it = 0;
+      bool aborted = false;
+      for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
+        Tile t;
+        int grp;
+        if (!unit_tile(p, u, MGT, &t, &grp)) continue;
+        int tok[128 / 8];  // token row of tile rows row_a + 8j
+#pragma unroll
+        for (int j = 0; j < 128 / 8; ++j) {
+          const int i = row_a + 8 * j;
+          int tk = -1;
           if (i < t.rows) {
             const int r = t.row0 + i;
             if (r < A) {
               const int a = __ldg(p.perm + r);
-              if (a >= 0 && a < A) tok = a / p.k;
+              if (a >= 0 && a < A) tk = a / p.k;
               else set_device_error(p.err, MOE_DEV_BAD_INDEX);
             } else {
-              tok = r - A;
+              tk = r - A;
             }
           }
-          s_tok[i] = tok;
+          tok[j] = tk;
         }
-        __syncwarp();
-      }
-      for (int kg = 0; kg < KT; ++kg, ++it) {
-        const int s = it % NB, r = it / NB;
-        if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto bprod_done;
-        const uint32_t dst = sbase + s * SB;
-        if (MODE == 1) {
-          ptx::mbar_arrive_expect_tx_elect(bar(BAR_BFULL + s), static_cast<uint32_t>(SB));
-          ptx::tma_load_2d_elect(dst, &tmap_act, kg * KG, t.row0, bar(BAR_BFULL + s));
-        } else {
-          ptx::mbar_arrive_expect_tx_elect(bar(BAR_BFULL + s), static_cast<uint32_t>(N * 128));
-#pragma unroll 1
-          for (int c = 0; c < N / 4; ++c) {
-            const int4 tk = *reinterpret_cast<const int4*>(s_tok + 4 * c);
-            ptx::tma_gather4_elect(dst + 512 * c, &tmap_act, kg * KG, tk.x, tk.y, tk.z, tk.w, bar(BAR_BFULL + s));
+        for (int ks = 0; ks < NS; ++ks, ++it) {
+          const int s = it % NB, r = it / NB;
+          if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t dst0 = sbase + s * SB;
+#pragma unroll
+          for (int j = 0; j < 128 / 8; ++j) {
+            const int i = row_a + 8 * j;
+            if (tok[j] >= 0) {
+              const uint16_t* src = p.act + static_cast<size_t>(tok[j]) * K + ks * KS + chunk * 8;
+              const uint32_t dst = dst0 + (i >> 3) * 1024 + (i & 7) * 128 + ((chunk ^ (i & 7)) << 4);
+              ptx::cp_async_16(dst, src);
+              ptx::cp_async_16(dst + atom_bytes, src + KG);
+            }
+          }
+          ptx::cp_async_commit();
+          if (it >= lag) {
+            ptx::cp_async_wait_n(lag);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(bar(BAR_BFULL + (it - lag) % NB));
           }
         }
       }
+      ptx::cp_async_wait_all();
+      if (!aborted && !*s_abort) {
+        ptx::fence_proxy_async_smem();
+        for (int t = it - lag < 0 ? 0 : it - lag; t < it; ++t) ptx::mbar_arrive(bar(BAR_BFULL + t % NB));
+      }
     }
-  bprod_done:;
   } else if (warp < 12) {
-    // ------------------------------------------------ dequant (two warpgroups, alternate K steps)
-    const int wg = (warp - 4) >> 2;
+    // ------------------------------------------------ dequant: warpgroup m expands M-tile m of the unit
+    const int m = (warp - 4) >> 2;
     const int q = warp & 3;
     const int L = 32 * q + lane;  // weight row within the M-tile = TMEM lane
     int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
-      int mt;
-      if (!unit_tile(p, u, MT, &t, &mt)) continue;
-      for (int kg = 0; kg < KT; ++kg, ++it) {
-        if ((it & 1) != wg) continue;
+      int grp;
+      if (!unit_tile(p, u, MGT, &t, &grp)) continue;
+      for (int ks = 0; ks < NS; ++ks, ++it) {
         const int sw = it % NW, sa = it % NA;
         if (!wait_warp(bar(BAR_WFULL + sw), (it / NW) & 1, s_abort, p.err, lim)) goto dequant_done;
-        const uint8_t* ws = smem + off_w + sw * W_STAGE;
-        const uint4 p0 = *reinterpret_cast<const uint4*>(ws + L * 16);
-        const uint4 p1 = *reinterpret_cast<const uint4*>(ws + 2048 + L * 16);
-        const uint32_t sbw = *reinterpret_cast<const uint32_t*>(ws + W_PACKED + L * 4);
+        // (when the unit has one M-tile, warpgroup 1 expands stale bytes that no MMA reads)
+        const uint8_t* ws = smem + off_w + sw * W_STAGE + m * GPS * W_BLOCK;
+        uint4 pk[GPS][2];
+        uint32_t sbw[GPS];
+#pragma unroll
+        for (int g = 0; g < GPS; ++g) {
+          pk[g][0] = *reinterpret_cast<const uint4*>(ws + g * W_BLOCK + L * 16);
+          pk[g][1] = *reinterpret_cast<const uint4*>(ws + g * W_BLOCK + 2048 + L * 16);
+          sbw[g] = *reinterpret_cast<const uint32_t*>(ws + g * W_BLOCK + W_PACKED + L * 4);
+        }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(BAR_WEMPTY + sw));
         if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
           goto dequant_done;
-        {
-          const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-          const uint32_t s2 = (sbw & 0xffffu) * 0x10001u;
-          const uint32_t b2 = (sbw >> 16) * 0x10001u;
+#pragma unroll
+        for (int g = 0; g < GPS; ++g) {
+          const uint32_t words[8] = {pk[g][0].x, pk[g][0].y, pk[g][0].z, pk[g][0].w,
+                                     pk[g][1].x, pk[g][1].y, pk[g][1].z, pk[g][1].w};
+          const uint32_t s2 = (sbw[g] & 0xffffu) * 0x10001u;
+          const uint32_t b2 = (sbw[g] >> 16) * 0x10001u;
           constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
           uint32_t v[32];
 #pragma unroll
@@ -349,10 +415,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
             }
           }
-          ptx::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + TMEM_A0 + 32 * sa, v);
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
+          ptx::tmem_st_32x32b_x32(
+              tmem + (static_cast<uint32_t>(32 * q) << 16) + TMEM_A0 + sa * A_COLS + m * GPS * 32 + g * 32, v);
         }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(BAR_AFULL + sa));
       }
@@ -364,60 +431,65 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
-      int mt;
-      if (!unit_tile(p, u, MT, &t, &mt)) {
+      int grp;
+      if (!unit_tile(p, u, MGT, &t, &grp)) {
         if (threadIdx.x == 12 * 32) set_device_error(p.err, MOE_DEV_BAD_BLOCK);
         continue;
       }
+      const int nm = min(MG, MT - grp * MG);
       const int d = ui % ND;
       if (!wait_warp(bar(BAR_DFULL + d), (ui / ND) & 1, s_abort, p.err, lim)) break;
       ptx::tc_fence_after();
       const int N = round16(t.rows);
-      for (int c0 = 0; c0 < N; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + d * DCOLS + c0, v);
-        if (MODE == 0) {
-          ptx::tmem_wait_ld();
-          const int f = 64 * mt + 16 * q + (lane & 15);
-          uint16_t* h = static_cast<uint16_t*>(p.out);
-          const bool lo = lane < 16;
+      for (int m = 0; m < nm; ++m) {
+        const int mt = grp * MG + m;
+        const uint32_t dcol = d * DBUF + m * DM;
+        for (int c0 = 0; c0 < N; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + dcol + c0, v);
+          if (MODE == 0) {
+            ptx::tmem_wait_ld();
+            const int f = 64 * mt + 16 * q + (lane & 15);
+            uint16_t* h = static_cast<uint16_t*>(p.out);
+            const bool lo = lane < 16;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const uint32_t send = lo ? v[16 + j] : v[j];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const float g = __uint_as_float(lo ? v[j] : recv);
-            const float uu = __uint_as_float(lo ? recv : v[16 + j]);
-            const int n = c0 + j + (lo ? 0 : 16);
-            if (n < t.rows) h[static_cast<size_t>(t.row0 + n) * p.F + f] = float_to_bf16_bits(silu(g) * uu);
-          }
-        } else {
-          // token and combine weight of column c0 + lane, loaded once and broadcast
-          int tok = -1;
-          float wt = 0.f;
-          const int n_l = c0 + lane;
-          if (n_l < t.rows) {
-            const int r = t.row0 + n_l;
-            if (r < A) {
-              const int a = __ldg(p.perm + r);
-              if (a >= 0 && a < A) {
-                tok = a / p.k;
-                wt = __ldg(p.topk_w + a);
-              } else {
-                set_device_error(p.err, MOE_DEV_BAD_INDEX);
-              }
-            } else {
-              tok = r - A;
-              wt = 1.0f;
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t send = lo ? v[16 + j] : v[j];
+              const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+              const float g = __uint_as_float(lo ? v[j] : recv);
+              const float uu = __uint_as_float(lo ? recv : v[16 + j]);
+              const int n = c0 + j + (lo ? 0 : 16);
+              if (n < t.rows) h[static_cast<size_t>(t.row0 + n) * p.F + f] = float_to_bf16_bits(silu(g) * uu);
             }
-          }
-          ptx::tmem_wait_ld();
-          const int ch = TC_M * mt + 32 * q + lane;
-          float* acc = static_cast<float*>(p.out);
+          } else {
+            // token and combine weight of column c0 + lane, loaded once and broadcast
+            int tok = -1;
+            float wt = 0.f;
+            const int n_l = c0 + lane;
+            if (n_l < t.rows) {
+              const int r = t.row0 + n_l;
+              if (r < A) {
+                const int a = __ldg(p.perm + r);
+                if (a >= 0 && a < A) {
+                  tok = a / p.k;
+                  wt = __ldg(p.topk_w + a);
+                } else {
+                  set_device_error(p.err, MOE_DEV_BAD_INDEX);
+                }
+              } else {
+                tok = r - A;
+                wt = 1.0f;
+              }
+            }
+            ptx::tmem_wait_ld();
+            const int ch = TC_M * mt + 32 * q + lane;
+            float* acc = static_cast<float*>(p.out);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int tj = __shfl_sync(0xffffffffu, tok, j);
-            const float wj = __shfl_sync(0xffffffffu, wt, j);
-            if (tj >= 0) atomicAdd(acc + static_cast<size_t>(tj) * p.H + ch, wj * __uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) {
+              const int tj = __shfl_sync(0xffffffffu, tok, j);
+              const float wj = __shfl_sync(0xffffffffu, wt, j);
+              if (tj >= 0) atomicAdd(acc + static_cast<size_t>(tj) * p.H + ch, wj * __uint_as_float(v[j]));
+            }
           }
         }
       }
@@ -430,11 +502,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (*s_abort) {
-    // after a timeout some copies may never have been consumed: let them land before the CTA exits
-    if (warp == 2 && lane == 0)
-      for (int t = prod_b - NB < 0 ? 0 : prod_b - NB; t < prod_b; ++t)
-        wait_drain(bar(BAR_BFULL + t % NB), (t / NB) & 1, lim);
+  if (*s_abort && MODE == 1 && warp == 2 && lane == 0) {
+    // after a timeout some tile loads may never have been consumed: let them land before the CTA exits
+    for (int t = prod_b - NB < 0 ? 0 : prod_b - NB; t < prod_b; ++t)
+      wait_drain(bar(BAR_BFULL + t % NB), (t / NB) & 1, lim);
   }
   if (warp == 1) {
     ptx::tc_fence_after();
@@ -472,7 +543,7 @@ __global__ void repack_kernel(const uint32_t* __restrict__ packed, const uint16_
       row = TC_M * mt + L;
     }
     const size_t crow = static_cast<size_t>(mat) * rows + row;
-    uint8_t* blk = out + ((static_cast<size_t>(mat) * MT + mt) * KT + kg) * W_STAGE;
+    uint8_t* blk = out + ((static_cast<size_t>(mat) * MT + mt) * KT + kg) * W_BLOCK;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
       const uint32_t in = packed[crow * (K / 8) + kg * 8 + w];
@@ -491,7 +562,7 @@ __global__ void repack_kernel(const uint32_t* __restrict__ packed, const uint16_
 }
 
 size_t repacked_bytes(int n_mat, int rows, int K) {
-  return static_cast<size_t>(n_mat) * (rows / TC_M) * (K / KG) * W_STAGE;
+  return static_cast<size_t>(n_mat) * (rows / TC_M) * (K / KG) * W_BLOCK;
 }
 
 cudaError_t launch_repack(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias, int n_mat, int rows,
@@ -565,28 +636,28 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   prm.bn = bn;
   prm.cap = cap;
   const int boxr = (bn + 15) & ~15;
-  prm.sb = boxr * 128;
+  if (boxr > 128) return cudaErrorInvalidValue;
+  prm.boxr = boxr;
+  prm.sb = GPS * boxr * 128;
   const int budget = max_dyn_smem() - TAIL_BYTES - 1024;
   int nbs = budget / prm.sb;
   if (nbs > NBMAX) nbs = NBMAX;
-  if (nbs < 3) return cudaErrorInvalidValue;
+  if (nbs < 2) return cudaErrorInvalidValue;
   prm.nb = nbs;
-  prm.nd = boxr <= 128 ? 2 : 1;
+  prm.nd = boxr <= 64 ? 2 : 1;
+  prm.lag = nbs - 1 < LAGMAX ? nbs - 1 : LAGMAX;
   const int smem = nbs * prm.sb + TAIL_BYTES + 1024;
 
-  // activation tensor map: gate/up gathers single token rows of x [T, H] four at a
-  // time (one-row box); down loads whole tiles of h [A+T, F] (boxr-row box)
+  // activation tensor map (down only): tiles of boxr contiguous rows of h [A+T, F]
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
-  {
+  if (mode == MOE_DOWN_COMBINE) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int A = T * k;
-    const bool down = mode == MOE_DOWN_COMBINE;
-    const cuuint64_t K = static_cast<cuuint64_t>(down ? F : H);
-    cuuint64_t gdim[2] = {K, static_cast<cuuint64_t>(down ? A + T : T)};
-    cuuint64_t gstride[1] = {K * 2};
-    cuuint32_t box[2] = {64, down ? static_cast<cuuint32_t>(boxr) : 1u};
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(F), static_cast<cuuint64_t>(A + T)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(F) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(boxr)};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(act), gdim, gstride, box,
                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -9,7 +9,7 @@ import numpy as np
 
 from . import _lib
 
-DEFAULT_BLOCK_N = {_lib.IMPL_SIMT: 128, _lib.IMPL_TC: 256, _lib.IMPL_GEMV: 256, _lib.IMPL_AUTO: 256}
+DEFAULT_BLOCK_N = {_lib.IMPL_SIMT: 128, _lib.IMPL_TC: 128, _lib.IMPL_GEMV: 128, _lib.IMPL_AUTO: 128}
 
 
 def _dev(a: np.ndarray, device):
@@ -36,6 +36,9 @@ class MoELayerW4:
         self.H, self.E, self.k, self.F = H, E, k, F
         self.device = torch.device(device)
         self.impl = _lib.IMPLS[impl] if isinstance(impl, str) else int(impl)
+        if self.impl == _lib.IMPL_AUTO:
+            # the tensor-core kernel takes K in steps of 128; other shapes use the CUDA-core kernel
+            self.impl = _lib.IMPL_TC if H % 128 == 0 and F % 128 == 0 else _lib.IMPL_SIMT
         self.block_n = block_n or DEFAULT_BLOCK_N[self.impl]
         _lib.load()
         w = {n: (v if isinstance(v, torch.Tensor) else _dev(v, self.device)) for n, v in weights.items()

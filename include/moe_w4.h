@@ -69,7 +69,7 @@ enum {
 
 /* GEMM implementations. */
 enum {
-  MOE_IMPL_AUTO = 0,      /* tensor-core kernel for prefill, GEMV kernel for T <= 8 */
+  MOE_IMPL_AUTO = 0,      /* the tensor-core kernel */
   MOE_IMPL_SIMT = 1,      /* CUDA-core tiled kernel (canonical weight layout) */
   MOE_IMPL_TC = 2,        /* tcgen05 kernel (repacked weight layout) */
   MOE_IMPL_GEMV = 3       /* CUDA-core decode kernel (repacked weight layout) */
@@ -195,8 +195,8 @@ int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t*
  *        FP32 additions is not fixed.
  * weights: canonical layout for MOE_IMPL_SIMT, repacked layout otherwise.
  * block_map / num_blocks: moe_route's outputs for the same block_n.
- * impl: MOE_IMPL_* (AUTO picks by T).  The TC kernel needs block_n <= 256
- * and H % 128 == 0; SIMT needs block_n <= 128.
+ * impl: MOE_IMPL_* (AUTO = TC).  The TC kernel needs block_n <= 128,
+ * H % 128 == 0 and F % 128 == 0; SIMT needs block_n <= 128.
  */
 int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,
                        const void* w_packed, const uint16_t* w_scale, const uint16_t* w_bias,

@@ -40,8 +40,8 @@ SMALL = [
     (300, 512, 32, 4, 256, False),    # ragged tiles, several shared-expert tiles
     (512, 256, 8, 2, 128, False),     # experts above one tile
     (1, 256, 16, 2, 128, False),      # a single token
-    (77, 128, 64, 8, 64, False),      # many empty experts
-    (1000, 256, 16, 4, 192, True),    # skewed logits (Zipf offset), F not a power of two
+    (77, 128, 64, 8, 128, False),     # many empty experts
+    (1000, 256, 16, 4, 384, True),    # skewed logits (Zipf offset), F not a power of two
 ]
 
 
@@ -53,13 +53,21 @@ def test_layer_small(spec, impl):
     G.check_layer(d, layer, got, what=f"layer {spec} {impl}")
 
 
-@pytest.mark.parametrize("block_n", [16, 64, 128, 200, 256])
+@pytest.mark.parametrize("block_n", [16, 48, 64, 96, 128])
 def test_layer_tc_block_sizes(block_n):
     """The tensor-core kernel with every tile height it supports (N = rows rounded up to 16)."""
     spec = (700, 256, 16, 4, 128, False)
     d = G.workload(spec)
     (got,), layer = run_layer(d, "tc", block_n=block_n)
     G.check_layer(d, layer, got, what=f"tc block_n={block_n}")
+
+
+def test_layer_simt_odd_widths():
+    """The CUDA-core kernel covers widths the tensor-core one does not take (F % 128 != 0)."""
+    for spec in [(77, 128, 64, 8, 64, False), (300, 256, 16, 4, 192, True)]:
+        d = G.workload(spec)
+        (got,), layer = run_layer(d, "simt")
+        G.check_layer(d, layer, got, what=f"simt {spec}")
 
 
 @pytest.mark.parametrize("impl", IMPLS)
