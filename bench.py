@@ -61,6 +61,21 @@ def algorithmic(shape, T, n_touched):
             "flops_down": flops_down, "step_bytes": step_bytes, "step_flops": flops_gate_up + flops_down}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value across ranks (the timed region ends when the slowest rank ends)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_tokens(shape, T, rank, skew=False):
+    """Each rank's own batch of T tokens (weak scaling: a distinct seed per rank)."""
+    return workloads.make_tokens(shape, T, seed=rank, skew=skew)
+
+
 # --------------------------------------------------------------------------- #
 # clocks
 # --------------------------------------------------------------------------- #
@@ -139,7 +154,7 @@ def run_ours(args, rank, world, local_rank):
     T = wl.T
     d = workloads.make_workload(wl, seed=0, with_weights=True)
     if rank:  # each rank its own tokens (weights are the same replica)
-        d.update(workloads.make_tokens(s, T, seed=rank, skew=wl.skew))
+        d.update(rank_tokens(s, T, rank, wl.skew))
     layer = MoELayerW4(s.H, s.E, s.k, s.F, d, device=dev, impl=args.kernels, block_n=args.block_n)
     x = torch.from_numpy(d["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
     logits = torch.from_numpy(d["logits"]).to(dev)
@@ -200,10 +215,7 @@ def run_ours(args, rank, world, local_rank):
     seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)])
     step_ms = seg.sum(1)
     ms = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     assert _lib.moe_get_device_error() == 0, "device error word set"
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
@@ -225,10 +237,7 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize()
         t1 = time.perf_counter()
         e2e_ms = (t1 - t0) * 1e3 / ne
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(xh.numel() * 2 + lh.numel() * 4),
                "d2h_bytes_per_step": int(oh.numel() * 2), "ms_per_step": e2e_ms,
