@@ -18,8 +18,7 @@
 // Roles (512 threads, one CTA per SM, persistent over (block-map tile, M-tile)).
 // Warps 0-2 run their loops converged with warp-uniform operands and let
 // elect.sync pick the lane that issues each copy, MMA or commit:
-//   warp 0      copies the packed 4-bit block of each K step into smem with
-//               per-lane cp.async (completion counted on an mbarrier)
+//   warp 0      idle (each dequant thread fetches its own weight row)
 //   warp 1      allocates TMEM; issues tcgen05.mma (A from TMEM, B from smem)
 //   warp 2      loads the tile's activation rows into 128B-swizzled smem with
 //               TMA: gate/up gathers token rows of x four at a time
@@ -53,22 +52,19 @@ constexpr int KS = KG * GPS;           // K per stage
 constexpr int W_PACKED = TC_M * 32;    // packed nibbles of one M-tile x K group
 constexpr int W_BLOCK = W_PACKED + TC_M * 4;  // + (scale, bias) per row: one repacked block
 constexpr int W_STAGE = MG * GPS * W_BLOCK;   // packed weights of one stage
-constexpr int NW = 4;                  // packed-weight ring (smem)
+constexpr int NW = 4;                  // packed-weight ring (smem; each dequant thread fills its own rows)
+constexpr int PD = NW - 1;             // stages each dequant thread prefetches ahead
 constexpr int A_COLS = MG * GPS * 32;  // TMEM columns of one dequantised stage
-constexpr int NA = 2;                  // dequantised-weight ring (TMEM)
+constexpr int NAMAX = 3;               // dequantised-weight ring (TMEM), run-time depth 2 or 3
 constexpr int NBMAX = 12;              // activation ring (smem), run-time depth <= NBMAX
-constexpr int TMEM_COLS = 512;
-constexpr int TMEM_A0 = 256;           // A ring in columns 256..511; accumulators in 0..255
+constexpr int TMEM_COLS = 512;        // accumulators first, then the A ring
 constexpr int NTHREADS = 512;
 constexpr int GATHER_T = 64;           // threads gathering activation rows (gate/up)
-constexpr int LAGMAX = 8;
 
 // barrier indices
-constexpr int BAR_WFULL = 0;
-constexpr int BAR_WEMPTY = BAR_WFULL + NW;
-constexpr int BAR_AFULL = BAR_WEMPTY + NW;
-constexpr int BAR_AEMPTY = BAR_AFULL + NA;
-constexpr int BAR_BFULL = BAR_AEMPTY + NA;
+constexpr int BAR_AFULL = 0;
+constexpr int BAR_AEMPTY = BAR_AFULL + NAMAX;
+constexpr int BAR_BFULL = BAR_AEMPTY + NAMAX;
 constexpr int BAR_BEMPTY = BAR_BFULL + NBMAX;
 constexpr int BAR_DFULL = BAR_BEMPTY + NBMAX;
 constexpr int BAR_DEMPTY = BAR_DFULL + 2;
@@ -97,8 +93,10 @@ struct TcParams {
   int boxr;     // activation rows per stage buffer (block_n rounded up to 16, <= 128)
   int nb;       // activation ring depth
   int sb;       // bytes of one activation stage: GPS atoms of boxr rows x 128 bytes
-  int nd;       // accumulator buffers (2 when tiles have <= 64 rows)
-  int lag;      // cp.async groups each gather thread keeps in flight
+  int nd;       // accumulator buffers
+  int dm;       // TMEM columns of one M-tile's accumulator (= boxr)
+  int na;       // A ring depth
+  int a0;       // first TMEM column of the A ring
 };
 
 // Bounded waits.  The time limit is counted in SM clock cycles (clock64, cheap
@@ -162,7 +160,8 @@ __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 //
 // Rings (full/empty mbarriers; stage index = running stage count `it` modulo
 // the ring depth):
-//   W  packed 4-bit blocks, smem, cp.async (warp 0) -> dequant warps
+//   W  packed 4-bit blocks, smem; each dequant thread prefetches its own
+//      row's bytes with cp.async and waits for its own copies
 //   A  dequantised bf16 weights, TMEM, dequant warps -> MMA (warp 1)
 //   B  activation rows, 128B-swizzled K-major atoms of 64 K, smem,
 //      gate/up: cp.async gather of token rows (warps 2-3),
@@ -175,7 +174,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
-  const int NB = p.nb, SB = p.sb, ND = p.nd, BOXR = p.boxr;
+  const int NB = p.nb, SB = p.sb, ND = p.nd, BOXR = p.boxr, NA = p.na;
   const uint32_t atom_bytes = static_cast<uint32_t>(BOXR) * 128u;
   const uint32_t off_w = static_cast<uint32_t>(NB * SB);
   const uint32_t bar0 = sbase + off_w + W_RING_BYTES;
@@ -190,8 +189,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int MT = MODE == 0 ? (2 * p.F) / TC_M : p.H / TC_M;
   const int MGT = (MT + MG - 1) / MG;        // M-groups per tile
   const int A = p.T * p.k;
-  const int DBUF = ND == 2 ? 128 : 256;      // columns per accumulator buffer
-  const int DM = DBUF / MG;                  // columns per M-tile accumulator
+  const int DM = p.dm;                       // columns per M-tile accumulator
+  const int DBUF = MG * DM;                  // columns per accumulator buffer
+  const uint32_t A0 = static_cast<uint32_t>(p.a0);
   int nb = __ldg(p.num_blocks);
   if (nb < 0 || nb > p.cap) {
     if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(p.err, MOE_DEV_BAD_BLOCK);
@@ -201,11 +201,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     *s_abort = 0;
-    for (int s = 0; s < NW; ++s) {
-      ptx::mbar_init(bar(BAR_WFULL + s), 32);
-      ptx::mbar_init(bar(BAR_WEMPTY + s), 8);
-    }
-    for (int s = 0; s < NA; ++s) {
+    for (int s = 0; s < NAMAX; ++s) {
       ptx::mbar_init(bar(BAR_AFULL + s), 8);
       ptx::mbar_init(bar(BAR_AEMPTY + s), 1);
     }
@@ -232,29 +228,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   int prod_b = 0;  // activation TMA stages issued (down), for the drain after a timeout
 
   if (warp == 0) {
-    // ------------------------------------------------ packed-weight producer (cp.async, 32 lanes)
-    int it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      Tile t;
-      int grp;
-      if (!unit_tile(p, u, MGT, &t, &grp)) continue;
-      const int nm = min(MG, MT - grp * MG);
-      for (int ks = 0; ks < NS; ++ks, ++it) {
-        const int s = it % NW, r = it / NW;
-        if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto producer_done;
-        for (int m = 0; m < nm; ++m) {
-          const uint8_t* g = p.w + ((static_cast<size_t>(t.expert) * MT + grp * MG + m) * KT + ks * GPS) *
-                                       static_cast<size_t>(W_BLOCK);
-          const uint32_t d = sbase + off_w + s * W_STAGE + m * GPS * W_BLOCK;
-#pragma unroll 6
-          for (int c = 0; c < GPS * W_BLOCK / 16 / 32; ++c)
-            ptx::cp_async_16(d + (c * 32 + lane) * 16, g + (c * 32 + lane) * 16);
-        }
-        ptx::cp_async_mbar_arrive(bar(BAR_WFULL + s));
-      }
-    }
-  producer_done:
-    ptx::cp_async_wait_all();  // no copy of this warp may still be landing when the CTA exits
+    // (idle: the dequant warps fetch their own weight rows)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (whole warp, one lane issues)
     int it = 0, ui = 0;
@@ -272,8 +246,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int sa = it % NA, sb = it % NB;
         if (!wait_warp(bar(BAR_AFULL + sa), (it / NA) & 1, s_abort, p.err, lim)) goto mma_done;
         if (!wait_warp(bar(BAR_BFULL + sb), (it / NB) & 1, s_abort, p.err, lim)) goto mma_done;
+        if (MODE == 0) ptx::fence_proxy_async_smem();  // cp.async-written rows, read by the tensor core
         ptx::tc_fence_after();
-        const uint32_t a0 = tmem + TMEM_A0 + sa * A_COLS;
+        const uint32_t a0 = tmem + A0 + sa * A_COLS;
         const uint32_t b0 = sbase + sb * SB;
 #pragma unroll
         for (int j = 0; j < KS / 16; ++j) {
@@ -316,7 +291,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ------------------------------------------------ activation gather: token rows of x by cp.async
       const int gt = threadIdx.x - 64;  // 0..63
       const int chunk = gt & 7, row_a = gt >> 3;
-      const int lag = p.lag;
       int it = 0;
       bool aborted = false;
       for (int u = blockIdx.x; u < units && !aborted; u += gridDim.x) {
@@ -357,35 +331,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               ptx::cp_async_16(dst + atom_bytes, src + KG);
             }
           }
-          ptx::cp_async_commit();
-          if (it >= lag) {
-            ptx::cp_async_wait_n(lag);
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(bar(BAR_BFULL + (it - lag) % NB));
-          }
+          // the barrier counts one arrival per gather thread, made by the hardware
+          // once this thread's copies of the stage have landed
+          ptx::cp_async_mbar_arrive(bar(BAR_BFULL + s));
         }
       }
       ptx::cp_async_wait_all();
-      if (!aborted && !*s_abort) {
-        ptx::fence_proxy_async_smem();
-        for (int t = it - lag < 0 ? 0 : it - lag; t < it; ++t) ptx::mbar_arrive(bar(BAR_BFULL + t % NB));
-      }
     }
   } else if (warp < 12) {
     // ------------------------------------------------ dequant: warpgroup m expands M-tile m of the unit
+    // Each thread owns one weight row: it prefetches that row's packed bytes PD
+    // stages ahead into its own slots of the W ring with cp.async and waits for
+    // its own copies, so no other warp is involved in the weight stream.
     const int m = (warp - 4) >> 2;
     const int q = warp & 3;
     const int L = 32 * q + lane;  // weight row within the M-tile = TMEM lane
+    const uint32_t wring = sbase + off_w + m * GPS * W_BLOCK;
+    // prefetch cursor over this CTA's (unit, stage) sequence
+    int pu = blockIdx.x, pks = 0, pgrp = 0;
+    Tile pt;
+    while (pu < units && !unit_tile(p, pu, MGT, &pt, &pgrp)) pu += gridDim.x;
+    auto prefetch = [&](int slot) {
+      if (pu < units) {
+        if (pgrp * MG + m < MT) {
+          const uint8_t* g = p.w + ((static_cast<size_t>(pt.expert) * MT + pgrp * MG + m) * KT + pks * GPS) *
+                                       static_cast<size_t>(W_BLOCK);
+          const uint32_t d = wring + slot * W_STAGE;
+#pragma unroll
+          for (int gg = 0; gg < GPS; ++gg) {
+            ptx::cp_async_16(d + gg * W_BLOCK + L * 16, g + gg * W_BLOCK + L * 16);
+            ptx::cp_async_16(d + gg * W_BLOCK + 2048 + L * 16, g + gg * W_BLOCK + 2048 + L * 16);
+            ptx::cp_async_4(d + gg * W_BLOCK + W_PACKED + L * 4, g + gg * W_BLOCK + W_PACKED + L * 4);
+          }
+        }
+        if (++pks == NS) {
+          pks = 0;
+          do {
+            pu += gridDim.x;
+          } while (pu < units && !unit_tile(p, pu, MGT, &pt, &pgrp));
+        }
+      }
+      ptx::cp_async_commit();  // one group per stage, possibly empty
+    };
+#pragma unroll 1
+    for (int i = 0; i < PD; ++i) prefetch(i);
     int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
       int grp;
       if (!unit_tile(p, u, MGT, &t, &grp)) continue;
       for (int ks = 0; ks < NS; ++ks, ++it) {
-        const int sw = it % NW, sa = it % NA;
-        if (!wait_warp(bar(BAR_WFULL + sw), (it / NW) & 1, s_abort, p.err, lim)) goto dequant_done;
+        const int sa = it % NA;
+        prefetch((it + PD) % NW);
+        ptx::cp_async_wait<PD>();  // this thread's bytes of stage `it` have landed
         // (when the unit has one M-tile, warpgroup 1 expands stale bytes that no MMA reads)
-        const uint8_t* ws = smem + off_w + sw * W_STAGE + m * GPS * W_BLOCK;
+        const uint8_t* ws = smem + (wring - sbase) + (it % NW) * W_STAGE;
         uint4 pk[GPS][2];
         uint32_t sbw[GPS];
 #pragma unroll
@@ -394,8 +394,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           pk[g][1] = *reinterpret_cast<const uint4*>(ws + g * W_BLOCK + 2048 + L * 16);
           sbw[g] = *reinterpret_cast<const uint32_t*>(ws + g * W_BLOCK + W_PACKED + L * 4);
         }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(BAR_WEMPTY + sw));
         if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
           goto dequant_done;
 #pragma unroll
@@ -415,8 +413,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
             }
           }
-          ptx::tmem_st_32x32b_x32(
-              tmem + (static_cast<uint32_t>(32 * q) << 16) + TMEM_A0 + sa * A_COLS + m * GPS * 32 + g * 32, v);
+          ptx::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + A0 + sa * A_COLS + m * GPS * 32 +
+                                      g * 32,
+                                  v);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -424,7 +423,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) ptx::mbar_arrive(bar(BAR_AFULL + sa));
       }
     }
-  dequant_done:;
+  dequant_done:
+    ptx::cp_async_wait_all();  // no prefetch may still be landing when the CTA exits
   } else {
     // ------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -644,8 +644,12 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   if (nbs > NBMAX) nbs = NBMAX;
   if (nbs < 2) return cudaErrorInvalidValue;
   prm.nb = nbs;
-  prm.nd = boxr <= 64 ? 2 : 1;
-  prm.lag = nbs - 1 < LAGMAX ? nbs - 1 : LAGMAX;
+  prm.dm = boxr;
+  // TMEM: accumulators (nd buffers x 2 M-tiles x boxr columns), then the A ring
+  prm.nd = 2 * (2 * boxr) + 2 * A_COLS <= TMEM_COLS ? 2 : 1;
+  prm.a0 = prm.nd * 2 * boxr;
+  prm.na = (TMEM_COLS - prm.a0) / A_COLS;
+  if (prm.na > NAMAX) prm.na = NAMAX;
   const int smem = nbs * prm.sb + TAIL_BYTES + 1024;
 
   // activation tensor map (down only): tiles of boxr contiguous rows of h [A+T, F]
