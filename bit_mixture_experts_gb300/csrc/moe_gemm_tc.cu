@@ -24,7 +24,7 @@
 //               TMA: gate/up gathers token rows of x four at a time
 //               (tile::gather4), down loads contiguous rows of h
 //   warp 3      idle
-//   warps 4-11  two dequant warpgroups (alternate K steps): nibbles -> bf16
+//   warps 4-11  two dequant warpgroups (alternate stages): nibbles -> bf16
 //               w = bf16(q*scale + bias) with one fma.rn.bf16x2 per pair,
 //               written to TMEM with tcgen05.st
 //   warps 12-15 epilogue: tcgen05.ld of the FP32 accumulators, then
@@ -52,8 +52,8 @@ constexpr int KS = KG * GPS;           // K per stage
 constexpr int W_PACKED = TC_M * 32;    // packed nibbles of one M-tile x K group
 constexpr int W_BLOCK = W_PACKED + TC_M * 4;  // + (scale, bias) per row: one repacked block
 constexpr int W_STAGE = MG * GPS * W_BLOCK;   // packed weights of one stage
-constexpr int NW = 4;                  // packed-weight ring (smem; each dequant thread fills its own rows)
-constexpr int PD = NW - 1;             // stages each dequant thread prefetches ahead
+constexpr int NWW = 3;                 // packed-weight slots per dequant warpgroup (each thread fills its own rows)
+constexpr int PD = NWW - 1;            // own stages each dequant thread prefetches ahead
 constexpr int A_COLS = MG * GPS * 32;  // TMEM columns of one dequantised stage
 constexpr int NAMAX = 3;               // dequantised-weight ring (TMEM), run-time depth 2 or 3
 constexpr int NBMAX = 12;              // activation ring (smem), run-time depth <= NBMAX
@@ -72,7 +72,7 @@ constexpr int BAR_FIN = BAR_DEMPTY + 2;
 constexpr int NBAR = BAR_FIN + 1;
 
 // smem layout (offsets from a 1024-byte aligned base): B ring | W ring | barriers | misc
-constexpr int W_RING_BYTES = NW * W_STAGE;
+constexpr int W_RING_BYTES = 2 * NWW * W_STAGE;  // two warpgroups
 constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
 constexpr int MISC_BYTES = 16;  // abort flag, TMEM base
 constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     *s_abort = 0;
     for (int s = 0; s < NAMAX; ++s) {
-      ptx::mbar_init(bar(BAR_AFULL + s), 8);
+      ptx::mbar_init(bar(BAR_AFULL + s), 4);
       ptx::mbar_init(bar(BAR_AEMPTY + s), 1);
     }
     for (int s = 0; s < NBMAX; ++s) {
@@ -339,24 +339,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ptx::cp_async_wait_all();
     }
   } else if (warp < 12) {
-    // ------------------------------------------------ dequant: warpgroup m expands M-tile m of the unit
-    // Each thread owns one weight row: it prefetches that row's packed bytes PD
-    // stages ahead into its own slots of the W ring with cp.async and waits for
-    // its own copies, so no other warp is involved in the weight stream.
-    const int m = (warp - 4) >> 2;
+    // ------------------------------------------------ dequant: warpgroup wg expands the stages it with it % 2 == wg
+    // (both M-tiles of the unit), so one warpgroup computes while the other waits.
+    // Each thread owns one weight row of each M-tile: it prefetches that row's
+    // packed bytes PD of its own stages ahead into its own slots with cp.async
+    // and waits for its own copies, so no other warp is involved in the weight stream.
+    const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
-    const int L = 32 * q + lane;  // weight row within the M-tile = TMEM lane
-    const uint32_t wring = sbase + off_w + m * GPS * W_BLOCK;
-    // prefetch cursor over this CTA's (unit, stage) sequence
-    int pu = blockIdx.x, pks = 0, pgrp = 0;
+    const int L = 32 * q + lane;  // weight row within each M-tile = TMEM lane
+    const uint32_t wring = sbase + off_w + wg * NWW * W_STAGE;
+    // prefetch cursor over this CTA's (unit, stage) sequence, restricted to stages it % 2 == wg
+    int pu = blockIdx.x, pks = 0, pgrp = 0, pit = 0;
     Tile pt;
     while (pu < units && !unit_tile(p, pu, MGT, &pt, &pgrp)) pu += gridDim.x;
+    auto advance = [&]() {
+      ++pit;
+      if (++pks == NS) {
+        pks = 0;
+        do {
+          pu += gridDim.x;
+        } while (pu < units && !unit_tile(p, pu, MGT, &pt, &pgrp));
+      }
+    };
+    if ((pit & 1) != wg && pu < units) advance();
     auto prefetch = [&](int slot) {
       if (pu < units) {
-        if (pgrp * MG + m < MT) {
+        const int nm = min(MG, MT - pgrp * MG);
+        for (int m = 0; m < nm; ++m) {
           const uint8_t* g = p.w + ((static_cast<size_t>(pt.expert) * MT + pgrp * MG + m) * KT + pks * GPS) *
                                        static_cast<size_t>(W_BLOCK);
-          const uint32_t d = wring + slot * W_STAGE;
+          const uint32_t d = wring + slot * W_STAGE + m * GPS * W_BLOCK;
 #pragma unroll
           for (int gg = 0; gg < GPS; ++gg) {
             ptx::cp_async_16(d + gg * W_BLOCK + L * 16, g + gg * W_BLOCK + L * 16);
@@ -364,58 +376,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::cp_async_4(d + gg * W_BLOCK + W_PACKED + L * 4, g + gg * W_BLOCK + W_PACKED + L * 4);
           }
         }
-        if (++pks == NS) {
-          pks = 0;
-          do {
-            pu += gridDim.x;
-          } while (pu < units && !unit_tile(p, pu, MGT, &pt, &pgrp));
-        }
+        advance();
+        if (pu < units) advance();  // skip the other warpgroup's stage
       }
-      ptx::cp_async_commit();  // one group per stage, possibly empty
+      ptx::cp_async_commit();  // one group per own stage, possibly empty
     };
 #pragma unroll 1
     for (int i = 0; i < PD; ++i) prefetch(i);
-    int it = 0;
+    int it = 0, own = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
       int grp;
       if (!unit_tile(p, u, MGT, &t, &grp)) continue;
+      const int nm = min(MG, MT - grp * MG);
       for (int ks = 0; ks < NS; ++ks, ++it) {
+        if ((it & 1) != wg) continue;
         const int sa = it % NA;
-        prefetch((it + PD) % NW);
-        ptx::cp_async_wait<PD>();  // this thread's bytes of stage `it` have landed
-        // (when the unit has one M-tile, warpgroup 1 expands stale bytes that no MMA reads)
-        const uint8_t* ws = smem + (wring - sbase) + (it % NW) * W_STAGE;
-        uint4 pk[GPS][2];
-        uint32_t sbw[GPS];
-#pragma unroll
-        for (int g = 0; g < GPS; ++g) {
-          pk[g][0] = *reinterpret_cast<const uint4*>(ws + g * W_BLOCK + L * 16);
-          pk[g][1] = *reinterpret_cast<const uint4*>(ws + g * W_BLOCK + 2048 + L * 16);
-          sbw[g] = *reinterpret_cast<const uint32_t*>(ws + g * W_BLOCK + W_PACKED + L * 4);
-        }
+        prefetch((own + PD) % NWW);
+        ptx::cp_async_wait<PD>();  // this thread's bytes of this stage have landed
+        const uint8_t* ws = smem + (wring - sbase) + (own % NWW) * W_STAGE;
+        ++own;
         if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
           goto dequant_done;
+        for (int m = 0; m < nm; ++m) {
 #pragma unroll
-        for (int g = 0; g < GPS; ++g) {
-          const uint32_t words[8] = {pk[g][0].x, pk[g][0].y, pk[g][0].z, pk[g][0].w,
-                                     pk[g][1].x, pk[g][1].y, pk[g][1].z, pk[g][1].w};
-          const uint32_t s2 = (sbw[g] & 0xffffu) * 0x10001u;
-          const uint32_t b2 = (sbw[g] >> 16) * 0x10001u;
-          constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
-          uint32_t v[32];
+          for (int g = 0; g < GPS; ++g) {
+            const uint8_t* blk = ws + (m * GPS + g) * W_BLOCK;
+            const uint4 p0 = *reinterpret_cast<const uint4*>(blk + L * 16);
+            const uint4 p1 = *reinterpret_cast<const uint4*>(blk + 2048 + L * 16);
+            const uint32_t sbw = *reinterpret_cast<const uint32_t*>(blk + W_PACKED + L * 4);
+            const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            const uint32_t s2 = (sbw & 0xffffu) * 0x10001u;
+            const uint32_t b2 = (sbw >> 16) * 0x10001u;
+            constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
+            uint32_t v[32];
 #pragma unroll
-          for (int w = 0; w < 8; ++w) {
+            for (int w = 0; w < 8; ++w) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              // nibbles of K elements 8w+2j (low half) and 8w+2j+1 (high half): 128+q exactly
-              const uint32_t x = ((words[w] >> (4 * j)) & 0x000f000fu) | MAGIC;
-              v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
+              for (int j = 0; j < 4; ++j) {
+                // nibbles of K elements 8w+2j (low half) and 8w+2j+1 (high half): 128+q exactly
+                const uint32_t x = ((words[w] >> (4 * j)) & 0x000f000fu) | MAGIC;
+                v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
+              }
             }
+            ptx::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + A0 + sa * A_COLS +
+                                        m * GPS * 32 + g * 32,
+                                    v);
           }
-          ptx::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + A0 + sa * A_COLS + m * GPS * 32 +
-                                      g * 32,
-                                  v);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
