@@ -231,7 +231,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // (idle: the dequant warps fetch their own weight rows)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (whole warp, one lane issues)
-    int it = 0, ui = 0;
+    // The issue sequence is kept branch-free and fully unrolled with warp-uniform
+    // operands: a data-dependent branch or a run-time trip count around the
+    // elect.sync'ed MMAs multiplies their issue cost.
+    int ui = 0;
+    int sa = 0, pa = 0, sb = 0, pb = 0;  // ring slots and phases
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
       int grp;
@@ -242,23 +246,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (rd > 0 && !wait_warp(bar(BAR_DEMPTY + d), (rd - 1) & 1, s_abort, p.err, lim)) goto mma_done;
       ptx::tc_fence_after();
       const uint32_t d0 = tmem + d * DBUF, d1 = d0 + DM;
-      for (int ks = 0; ks < NS; ++ks, ++it) {
-        const int sa = it % NA, sb = it % NB;
-        if (!wait_warp(bar(BAR_AFULL + sa), (it / NA) & 1, s_abort, p.err, lim)) goto mma_done;
-        if (!wait_warp(bar(BAR_BFULL + sb), (it / NB) & 1, s_abort, p.err, lim)) goto mma_done;
+      for (int ks = 0; ks < NS; ++ks) {
+        if (!wait_warp(bar(BAR_AFULL + sa), pa, s_abort, p.err, lim)) goto mma_done;
+        if (!wait_warp(bar(BAR_BFULL + sb), pb, s_abort, p.err, lim)) goto mma_done;
         if (MODE == 0) ptx::fence_proxy_async_smem();  // cp.async-written rows, read by the tensor core
         ptx::tc_fence_after();
         const uint32_t a0 = tmem + A0 + sa * A_COLS;
         const uint32_t b0 = sbase + sb * SB;
+        const uint64_t bd0 = ptx::smem_desc_sw128(b0), bd1 = ptx::smem_desc_sw128(b0 + atom_bytes);
+        const uint32_t acc0 = ks != 0;
+        if (two) {
+          ptx::mma_ts_elect(d0, a0, bd0, idesc, acc0);
+          ptx::mma_ts_elect(d1, a0 + 64, bd0, idesc, acc0);
 #pragma unroll
-        for (int j = 0; j < KS / 16; ++j) {
-          const uint64_t bdesc = ptx::smem_desc_sw128(b0 + (j >> 2) * atom_bytes) + 2 * (j & 3);
-          const uint32_t acc = (ks | j) != 0;
-          ptx::mma_ts_elect(d0, a0 + 8 * j, bdesc, idesc, acc);
-          if (two) ptx::mma_ts_elect(d1, a0 + GPS * 32 + 8 * j, bdesc, idesc, acc);
+          for (int j = 1; j < 4; ++j) {
+            ptx::mma_ts_elect(d0, a0 + 8 * j, bd0 + 2 * j, idesc, 1);
+            ptx::mma_ts_elect(d1, a0 + 64 + 8 * j, bd0 + 2 * j, idesc, 1);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            ptx::mma_ts_elect(d0, a0 + 32 + 8 * j, bd1 + 2 * j, idesc, 1);
+            ptx::mma_ts_elect(d1, a0 + 96 + 8 * j, bd1 + 2 * j, idesc, 1);
+          }
+        } else {
+          ptx::mma_ts_elect(d0, a0, bd0, idesc, acc0);
+#pragma unroll
+          for (int j = 1; j < 4; ++j) ptx::mma_ts_elect(d0, a0 + 8 * j, bd0 + 2 * j, idesc, 1);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ptx::mma_ts_elect(d0, a0 + 32 + 8 * j, bd1 + 2 * j, idesc, 1);
         }
         ptx::mma_commit_elect(bar(BAR_AEMPTY + sa));
         ptx::mma_commit_elect(bar(BAR_BEMPTY + sb));
+        if (++sa == NA) {
+          sa = 0;
+          pa ^= 1;
+        }
+        if (++sb == NB) {
+          sb = 0;
+          pb ^= 1;
+        }
       }
       ptx::mma_commit_elect(bar(BAR_DFULL + d));
       ++ui;
