@@ -679,6 +679,8 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   prm.nb = nbs;
   prm.dm = boxr;
   // TMEM: accumulators (nd buffers x 2 M-tiles x boxr columns), then the A ring
+  // a second accumulator buffer (the epilogue of one unit overlaps the next
+  // unit's mainloop) when at least two A slots remain
   prm.nd = 2 * (2 * boxr) + 2 * A_COLS <= TMEM_COLS ? 2 : 1;
   prm.a0 = prm.nd * 2 * boxr;
   prm.na = (TMEM_COLS - prm.a0) / A_COLS;
