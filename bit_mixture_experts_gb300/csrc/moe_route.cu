@@ -35,19 +35,16 @@ __device__ __forceinline__ float key_float(uint32_t key) {
   return __uint_as_float(u);
 }
 
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
-  uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
-  lo = __shfl_xor_sync(FULL, lo, m);
-  hi = __shfl_xor_sync(FULL, hi, m);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-
 // Top-k of one token by one warp.  Lane L holds experts L, L+32, ...; each of
-// the k rounds takes every lane's best unchosen expert and reduces
-// (key, ~index) across the warp, so the largest logit wins and, among equal
-// logits, the lowest index.  Lane j < k ends with the j-th choice in
-// (*id, *w); the weights exp(l_j - l_0) / sum_i exp(l_i - l_0) are computed in
-// double and rounded once to float.
+// the k rounds takes every lane's best unchosen expert, reduces the keys with
+// redux.sync (max) and then, among the lanes holding that key, the expert
+// indices (min): the largest logit wins and, among equal logits, the lowest
+// index.  Lane j < k ends with the j-th choice in (*id, *w).
+//
+// Weights: w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0) in float.  The
+// difference l_j - l_0 is carried exactly as hi + lo (two-sum), so the only
+// errors are expf's (<= 2 ulp), the float sum of k terms and the division:
+// well under 1e-6 relative.
 template <int EPL>
 __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, int k, int lane,
                                           int* id_out, float* w_out) {
@@ -61,40 +58,39 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, 
   int my_id = 0;
   uint32_t my_key = 0;
   for (int j = 0; j < k; ++j) {
-    uint64_t best = 0;
+    uint32_t bk = 0;
+    int bi = -1;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      int e = i * 32 + lane;
-      if (e < E && !((chosen >> i) & 1u)) {
-        uint64_t c = (static_cast<uint64_t>(key[i]) << 32) | (0xffffffffu - static_cast<uint32_t>(e));
-        best = c > best ? c : best;
+      const int e = i * 32 + lane;
+      if (e < E && !((chosen >> i) & 1u) && (bi < 0 || key[i] > bk)) {
+        bk = key[i];
+        bi = i;
       }
     }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-      uint64_t o = shfl_xor_u64(best, m);
-      best = o > best ? o : best;
-    }
-    int e_win = static_cast<int>(0xffffffffu - static_cast<uint32_t>(best));
-    if ((e_win & 31) == lane) chosen |= 1u << (e_win >> 5);
+    const uint32_t kmax = __reduce_max_sync(FULL, bk);
+    const uint32_t cand = (bi >= 0 && bk == kmax) ? static_cast<uint32_t>(bi * 32 + lane) : 0xffffffffu;
+    const uint32_t e_win = __reduce_min_sync(FULL, cand);
+    if ((e_win & 31u) == static_cast<uint32_t>(lane)) chosen |= 1u << (e_win >> 5);
     if (lane == j) {
-      my_id = e_win;
-      my_key = static_cast<uint32_t>(best >> 32);
+      my_id = static_cast<int>(e_win);
+      my_key = kmax;
     }
   }
-  float l0 = key_float(__shfl_sync(FULL, my_key, 0));
-  double z = 0.0;
-  if (lane < k) z = exp(static_cast<double>(key_float(my_key)) - static_cast<double>(l0));
-  double s = z;
+  const float lj = key_float(my_key);
+  const float l0 = key_float(__shfl_sync(FULL, my_key, 0));
+  // two-sum: lj - l0 == dh + dl exactly
+  const float nl0 = -l0;
+  const float dh = lj + nl0;
+  const float bb = dh - lj;
+  const float dl = (lj - (dh - bb)) + (nl0 - bb);
+  float z = 0.f;
+  if (lane < k) z = expf(dh) * (1.0f + dl);
+  float s = z;
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) s += __shfl_xor_sync(FULL, s, m);
   *id_out = my_id;
-  *w_out = static_cast<float>(z / s);
-}
-
-template <int EPL>
-__device__ void topk_dispatch_row(const float* row, int E, int k, int lane, int* id, float* w) {
-  warp_topk<EPL>(row, E, k, lane, id, w);
+  *w_out = z / s;
 }
 
 __device__ __forceinline__ void warp_topk_any(const float* row, int E, int k, int lane, int* id, float* w) {
@@ -273,10 +269,12 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int T, int E, int k, i
   int sum = 0;
   if (e < E) {
     int c = c0;
-    for (; c + 4 <= c1; c += 4) {
-      int v0 = cc[static_cast<size_t>(c) * E + e], v1 = cc[static_cast<size_t>(c + 1) * E + e];
-      int v2 = cc[static_cast<size_t>(c + 2) * E + e], v3 = cc[static_cast<size_t>(c + 3) * E + e];
-      sum += v0 + v1 + v2 + v3;
+    for (; c + 16 <= c1; c += 16) {  // 16 independent loads in flight
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = cc[static_cast<size_t>(c + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sum += v[i];
     }
     for (; c < c1; ++c) sum += cc[static_cast<size_t>(c) * E + e];
   }
@@ -317,7 +315,18 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int T, int E, int k, i
   __syncthreads();
   if (e < E) {
     int run = s_off[e] + s_part[part * er + e];
-    for (int c = c0; c < c1; ++c) {
+    int c = c0;
+    for (; c + 16 <= c1; c += 16) {
+      int v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = cc[static_cast<size_t>(c + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        cc[static_cast<size_t>(c + i) * E + e] = run;
+        run += v[i];
+      }
+    }
+    for (; c < c1; ++c) {
       int32_t* p = cc + static_cast<size_t>(c) * E + e;
       int v = *p;
       *p = run;
