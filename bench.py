@@ -161,7 +161,7 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty((T, s.H), dtype=torch.bfloat16, device=dev)
     b = layer.buffers(T)
     stream = torch.cuda.current_stream()
-    impl, bn = layer.impl, layer.block_n
+    impl, bn = layer.impl_for(T), layer.block_n_for(T)
 
     def step(ev=None):
         if ev is not None:
@@ -254,9 +254,12 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved = work["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
-    roof = {"kernel": "gate/up grouped GEMM (moe_expert_gemm_w4, MOE_GATE_UP_SWIGLU)", "bound": bound,
+    kname = {_lib.IMPL_TC: "gemm_tc_kernel<0>", _lib.IMPL_GEMV: "gemv_kernel<0>",
+             _lib.IMPL_SIMT: "gemm_simt_kernel<0>"}.get(impl, str(impl))
+    traffic = profiled_traffic(wl.name, 0) if impl == _lib.IMPL_TC else None
+    roof = {"kernel": f"gate/up grouped GEMM {kname} (moe_expert_gemm_w4, MOE_GATE_UP_SWIGLU)", "bound": bound,
             "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-            "peak_source": peaks["source"], "traffic": None,
+            "peak_source": peaks["source"], "traffic": traffic,
             "algorithmic_per_launch": work["flops_gate_up"] if tensor_bound else work["gate_up_bytes"],
             "launch_ms": gu_ms}
 
@@ -282,6 +285,33 @@ def run_ours(args, rank, world, local_rank):
     if clocks:
         res["clocks"] = clocks.summary()
     return res, d, layer
+
+
+def kernel_source_sha():
+    """sha256[:16] of the tensor-core GEMM's sources (the profile summaries record the one they measured)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_mixture_experts_gb300", "csrc")
+    for f in ("moe_gemm_tc.cu", "moe_ptx.cuh", "moe_common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, mode):
+    """DRAM bytes per launch of gemm_tc_kernel<mode> from the committed ncu summary of this workload,
+    or None when there is none or the kernel's sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", f"gemm_tc_kernel.{workload}.md")
+    if not os.path.exists(p):
+        return None
+    sha, traffic = None, None
+    with open(p) as f:
+        for line in f:
+            if line.startswith("kernel source sha256"):
+                sha = line.rsplit("`", 2)[-2]
+            if line.startswith(f"traffic_bytes_per_launch mode{mode}:"):
+                traffic = int(line.split(":")[1])
+    return traffic if sha == kernel_source_sha() else None
 
 
 def load_peaks():

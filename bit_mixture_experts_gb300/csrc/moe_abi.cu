@@ -56,6 +56,10 @@ cudaError_t launch_combine(float* acc, uint16_t* out, int T, int H, int num_sms,
 size_t repacked_bytes(int n_mat, int rows, int K);
 cudaError_t launch_repack(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias, int n_mat, int rows,
                           int K, int gate_up, void* out, cudaStream_t s);
+cudaError_t launch_gemm_gemv(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
+                             const int32_t* perm, const float* topk_w, const int32_t* block_map,
+                             const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s);
+int gemv_max_rows();
 cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                            const int32_t* perm, const float* topk_w, const int32_t* block_map,
                            const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s);
@@ -138,8 +142,12 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
   if (!device_error_ptr()) return MOE_ERR_CUDA;
   const int cap = moe_block_map_capacity(T, E, k, block_n);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (impl == MOE_IMPL_AUTO) impl = MOE_IMPL_TC;
+  if (impl == MOE_IMPL_AUTO) impl = block_n <= gemv_max_rows() ? MOE_IMPL_GEMV : MOE_IMPL_TC;
   switch (impl) {
+    case MOE_IMPL_GEMV:
+      if (block_n > gemv_max_rows() || H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
+      return cuda_status(launch_gemm_gemv(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
+                                          block_n, cap, out, num_sms(), s));
     case MOE_IMPL_TC:
       if (block_n > 128 || H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
       return cuda_status(launch_gemm_tc(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
@@ -215,6 +223,7 @@ size_t moe_repacked_bytes(int n_mat, int rows, int K) {
 int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias, int n_mat, int rows, int K,
                   int gate_up, void* out, moe_stream_t stream) {
   if (n_mat < 1 || rows < 128 || rows % 128 != 0 || K < 64 || K % 64 != 0) return MOE_ERR_SHAPE;
+  if (gate_up && (rows / 2) % 128 != 0) return MOE_ERR_SHAPE;
   int rc = check_ptrs(packed, scale, bias, out);
   if (rc) return rc;
   return cuda_status(launch_repack(packed, scale, bias, n_mat, rows, K, gate_up ? 1 : 0, out,

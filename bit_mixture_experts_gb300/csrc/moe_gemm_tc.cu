@@ -28,8 +28,12 @@
 //               w = bf16(q*scale + bias) with one fma.rn.bf16x2 per pair,
 //               written to TMEM with tcgen05.st
 //   warps 12-15 epilogue: tcgen05.ld of the FP32 accumulators, then
-//               gate/up: h = bf16(silu(g) * u) stored to h[row, f]
-//               down:    acc[token] += w * y with FP32 reductions
+//               gate/up: the unit's two M-tiles are the gate and the up rows
+//                        of the same 128 features, so each thread holds g and
+//                        u of its feature: h = bf16(silu(g) * u) -> h[row, f]
+//               down:    y goes through shared memory (transpose to 4
+//                        channels per thread) and acc[token] += w * y is
+//                        added with 16-byte FP32 vector reductions
 //
 // Every mbarrier wait is bounded by a time limit; on expiry the kernel records
 // MOE_DEV_TIMEOUT in the device error word, every role leaves its loop, copies
@@ -75,7 +79,9 @@ constexpr int NBAR = BAR_FIN + 1;
 constexpr int W_RING_BYTES = 2 * NWW * W_STAGE;  // two warpgroups
 constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
 constexpr int MISC_BYTES = 16;  // abort flag, TMEM base
-constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;
+constexpr int EPI_PITCH = 36;   // floats per token row of the down epilogue's transpose buffer (16-byte rows)
+constexpr int EPI_BYTES = 4 * 32 * EPI_PITCH * 4;  // one 32 tokens x 32 channels buffer per epilogue warp
+constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;  // + EPI_BYTES for the down GEMM
 
 static_assert((GPS * W_BLOCK) % (16 * 32) == 0, "a weight stage is copied as 16-byte chunks by 32 lanes");
 
@@ -150,6 +156,11 @@ __device__ __forceinline__ bool unit_tile(const TcParams& p, int u, int MGT, Til
 }
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+// silu(g) = g / (1 + e^-g) with the fast exponential and division; the
+// product with u is rounded to bf16 afterwards, which hides their few-ulp
+// error except within a few FP32 ulps of a bf16 rounding boundary.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 }  // namespace
 
@@ -474,28 +485,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!wait_warp(bar(BAR_DFULL + d), (ui / ND) & 1, s_abort, p.err, lim)) break;
       ptx::tc_fence_after();
       const int N = round16(t.rows);
-      for (int m = 0; m < nm; ++m) {
-        const int mt = grp * MG + m;
-        const uint32_t dcol = d * DBUF + m * DM;
+      const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + d * DBUF;  // this warp's lanes
+      if (MODE == 0) {
+        // M-tile 0 = gate rows, M-tile 1 = up rows of features 128 grp + (0..127)
+        const int f = TC_M * grp + 32 * q + lane;
+        uint16_t* h = static_cast<uint16_t*>(p.out) + static_cast<size_t>(t.row0) * p.F + f;
         for (int c0 = 0; c0 < N; c0 += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + dcol + c0, v);
-          if (MODE == 0) {
-            ptx::tmem_wait_ld();
-            const int f = 64 * mt + 16 * q + (lane & 15);
-            uint16_t* h = static_cast<uint16_t*>(p.out);
-            const bool lo = lane < 16;
+          uint32_t g[32], uu[32];
+          ptx::tmem_ld_32x32b_x32(tq + c0, g);
+          ptx::tmem_ld_32x32b_x32(tq + DM + c0, uu);
+          ptx::tmem_wait_ld();
+          const int nv = t.rows - c0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint32_t send = lo ? v[16 + j] : v[j];
-              const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
-              const float g = __uint_as_float(lo ? v[j] : recv);
-              const float uu = __uint_as_float(lo ? recv : v[16 + j]);
-              const int n = c0 + j + (lo ? 0 : 16);
-              if (n < t.rows) h[static_cast<size_t>(t.row0 + n) * p.F + f] = float_to_bf16_bits(silu(g) * uu);
-            }
-          } else {
-            // token and combine weight of column c0 + lane, loaded once and broadcast
+          for (int j = 0; j < 32; ++j)
+            if (j < nv)
+              h[static_cast<size_t>(c0 + j) * p.F] =
+                  float_to_bf16_bits(silu_fast(__uint_as_float(g[j])) * __uint_as_float(uu[j]));
+        }
+      } else {
+        // y[channel 32q + lane, token c0 + j] -> sx[j][lane]; then lane 8r + c adds
+        // channels 4c..4c+3 of tokens 4i + r (i = 0..7) with one 16-byte reduction each
+        float* sx = reinterpret_cast<float*>(smem + off_w + W_RING_BYTES + BAR_BYTES + MISC_BYTES) +
+                    q * (32 * EPI_PITCH);
+        const int r4 = lane >> 3, c4 = lane & 7;
+        float* acc = static_cast<float*>(p.out);
+        for (int m = 0; m < nm; ++m) {
+          const int ch0 = TC_M * (grp * MG + m) + 32 * q + 4 * c4;
+          for (int c0 = 0; c0 < N; c0 += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tq + m * DM + c0, v);
+            // token and combine weight of column c0 + lane
             int tok = -1;
             float wt = 0.f;
             const int n_l = c0 + lane;
@@ -515,14 +534,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
             }
             ptx::tmem_wait_ld();
-            const int ch = TC_M * mt + 32 * q + lane;
-            float* acc = static_cast<float*>(p.out);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 32; ++j) sx[j * EPI_PITCH + lane] = __uint_as_float(v[j]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int j = 4 * i + r4;
               const int tj = __shfl_sync(0xffffffffu, tok, j);
               const float wj = __shfl_sync(0xffffffffu, wt, j);
-              if (tj >= 0) atomicAdd(acc + static_cast<size_t>(tj) * p.H + ch, wj * __uint_as_float(v[j]));
+              const float4 y = *reinterpret_cast<const float4*>(sx + j * EPI_PITCH + 4 * c4);
+              if (tj >= 0)
+                atomicAdd(reinterpret_cast<float4*>(acc + static_cast<size_t>(tj) * p.H + ch0),
+                          make_float4(wj * y.x, wj * y.y, wj * y.z, wj * y.w));
             }
+            __syncwarp();
           }
         }
       }
@@ -551,8 +576,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // [2 halves][128 rows][4 words] packed nibbles + [128 rows] (scale, bias).
 // Within a word the nibbles are reordered so that (word >> 4j) & 0x000f000f
 // yields K elements 2j (low half) and 2j+1 (high half) of that word's eight.
-// Gate/up tiles hold 64 features: per 32-row quadrant, 16 gate rows followed
-// by the 16 up rows of the same features.
+// Gate/up M-tiles come in pairs: M-tile 2j holds the gate rows and M-tile
+// 2j+1 the up rows of features 128j .. 128j+127 (needs F % 128 == 0).
 // --------------------------------------------------------------------------
 __global__ void repack_kernel(const uint32_t* __restrict__ packed, const uint16_t* __restrict__ scale,
                               const uint16_t* __restrict__ bias, int n_mat, int rows, int K, int gate_up,
@@ -569,9 +594,7 @@ __global__ void repack_kernel(const uint32_t* __restrict__ packed, const uint16_
     const int mat = static_cast<int>(rest / MT);
     int row;
     if (gate_up) {
-      const int q = L >> 5, i = L & 31;
-      const int f = 64 * mt + 16 * q + (i & 15);
-      row = i < 16 ? f : rows / 2 + f;
+      row = (mt & 1) * (rows / 2) + TC_M * (mt >> 1) + L;
     } else {
       row = TC_M * mt + L;
     }
@@ -672,7 +695,8 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   if (boxr > 128) return cudaErrorInvalidValue;
   prm.boxr = boxr;
   prm.sb = GPS * boxr * 128;
-  const int budget = max_dyn_smem() - TAIL_BYTES - 1024;
+  const int tail = TAIL_BYTES + (mode == MOE_DOWN_COMBINE ? EPI_BYTES : 0);
+  const int budget = max_dyn_smem() - tail - 1024;
   int nbs = budget / prm.sb;
   if (nbs > NBMAX) nbs = NBMAX;
   if (nbs < 2) return cudaErrorInvalidValue;
@@ -685,7 +709,7 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   prm.a0 = prm.nd * 2 * boxr;
   prm.na = (TMEM_COLS - prm.a0) / A_COLS;
   if (prm.na > NAMAX) prm.na = NAMAX;
-  const int smem = nbs * prm.sb + TAIL_BYTES + 1024;
+  const int smem = nbs * prm.sb + tail + 1024;
 
   // activation tensor map (down only): tiles of boxr contiguous rows of h [A+T, F]
   CUtensorMap tmap;

@@ -9,7 +9,23 @@ import numpy as np
 
 from . import _lib
 
-DEFAULT_BLOCK_N = {_lib.IMPL_SIMT: 128, _lib.IMPL_TC: 128, _lib.IMPL_GEMV: 128, _lib.IMPL_AUTO: 128}
+DEFAULT_BLOCK_N = {_lib.IMPL_SIMT: 128, _lib.IMPL_TC: 128, _lib.IMPL_GEMV: 8}
+DECODE_MAX_T = 16  # token counts up to this take the GEMV kernel under impl="auto"
+
+
+def default_block_n(impl: int, T: int, E: int, k: int) -> int:
+    """Tile height of the block map for T tokens.
+
+    The tensor-core kernel expands a 256-row slice of an expert's weights once
+    per tile, so tiles should be as tall as the expert's rows allow: with fewer
+    than 64 assignments per expert on average (512-token prompts through 256
+    experts top-8 average 16) 64-row tiles waste less of the MMA on padding and
+    give the grid more tiles; from there on 128-row tiles halve the
+    dequantisation per token.  The GEMV kernel takes tiles of up to 8 rows.
+    """
+    if impl == _lib.IMPL_TC and T * k < 64 * E:
+        return 64
+    return DEFAULT_BLOCK_N[impl]
 
 
 def _dev(a: np.ndarray, device):
@@ -36,10 +52,10 @@ class MoELayerW4:
         self.H, self.E, self.k, self.F = H, E, k, F
         self.device = torch.device(device)
         self.impl = _lib.IMPLS[impl] if isinstance(impl, str) else int(impl)
-        if self.impl == _lib.IMPL_AUTO:
-            # the tensor-core kernel takes K in steps of 128; other shapes use the CUDA-core kernel
-            self.impl = _lib.IMPL_TC if H % 128 == 0 and F % 128 == 0 else _lib.IMPL_SIMT
-        self.block_n = block_n or DEFAULT_BLOCK_N[self.impl]
+        if self.impl == _lib.IMPL_AUTO and not (H % 128 == 0 and F % 128 == 0):
+            # the tensor-core and GEMV kernels take K in steps of 128; other shapes use the tiled CUDA-core kernel
+            self.impl = _lib.IMPL_SIMT
+        self.block_n = block_n  # None: chosen per token count by default_block_n
         _lib.load()
         w = {n: (v if isinstance(v, torch.Tensor) else _dev(v, self.device)) for n, v in weights.items()
              if n.startswith(("w13_", "w2_"))}
@@ -63,12 +79,22 @@ class MoELayerW4:
         _lib.moe_repack_w4(packed, scale, bias, gate_up, out)
         return out
 
+    def impl_for(self, T):
+        """GEMM kernel used for T tokens: under "auto", GEMV for decode-sized T, else tensor cores."""
+        if self.impl != _lib.IMPL_AUTO:
+            return self.impl
+        return _lib.IMPL_GEMV if T <= DECODE_MAX_T and (self.block_n or 8) <= 8 else _lib.IMPL_TC
+
+    def block_n_for(self, T):
+        """Block-map tile height used for T tokens."""
+        return self.block_n or default_block_n(self.impl_for(T), T, self.E, self.k)
+
     def buffers(self, T):
         """Routing / intermediate buffers for T tokens (allocated once per T)."""
         import torch
         if T in self._bufs:
             return self._bufs[T]
-        E, k, H, F, bn = self.E, self.k, self.H, self.F, self.block_n
+        E, k, H, F, bn = self.E, self.k, self.H, self.F, self.block_n_for(T)
         A = T * k
         dev = self.device
         cap = _lib.moe_block_map_capacity(T, E, k, bn)
@@ -101,7 +127,7 @@ class MoELayerW4:
         b = self.buffers(T)
         if out is None:
             out = torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device)
-        _lib.moe_layer_forward(x, logits, out, T, self.H, self.F, self.E, self.k, self.block_n, self.impl,
+        _lib.moe_layer_forward(x, logits, out, T, self.H, self.F, self.E, self.k, self.block_n_for(T), self.impl_for(T),
                                self.weights, b["struct"], stream)
         return out
 
@@ -110,5 +136,5 @@ class MoELayerW4:
         T = x_host.shape[0]
         b = self.buffers(T)
         _lib.moe_layer_forward_host(x_host, logits_host, out_host, stage["x"], stage["logits"], stage["out"], T,
-                                    self.H, self.F, self.E, self.k, self.block_n, self.impl, self.weights,
+                                    self.H, self.F, self.E, self.k, self.block_n_for(T), self.impl_for(T), self.weights,
                                     b["struct"], stream)

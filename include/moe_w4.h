@@ -69,7 +69,7 @@ enum {
 
 /* GEMM implementations. */
 enum {
-  MOE_IMPL_AUTO = 0,      /* the tensor-core kernel */
+  MOE_IMPL_AUTO = 0,      /* GEMV when block_n <= 8, else the tensor-core kernel */
   MOE_IMPL_SIMT = 1,      /* CUDA-core tiled kernel (canonical weight layout) */
   MOE_IMPL_TC = 2,        /* tcgen05 kernel (repacked weight layout) */
   MOE_IMPL_GEMV = 3       /* CUDA-core decode kernel (repacked weight layout) */
@@ -164,9 +164,10 @@ size_t moe_repacked_bytes(int n_mat, int rows, int K);
  * block: [2 halves][128 rows][16 bytes] of packed nibbles (half h holds K
  * elements 32h..32h+31 of the group; within each word the nibbles are ordered
  * so that (word >> 4j) & 0x000f000f holds elements 2j and 2j+1 of its eight)
- * followed by [128 rows] x (scale bf16, bias bf16).  With gate_up = 1 a tile
- * holds 64 features: in each 32-row quarter, 16 gate rows then the 16 up rows
- * of the same features (rows = 2F).  Needs rows % 128 == 0 and K % 64 == 0.
+ * followed by [128 rows] x (scale bf16, bias bf16).  With gate_up = 1 the
+ * tiles come in pairs: tile 2j holds the gate rows and tile 2j+1 the up rows
+ * of features 128j .. 128j+127 (rows = 2F, F % 128 == 0).  Needs rows % 128
+ * == 0 and K % 64 == 0; returns MOE_ERR_SHAPE otherwise.
  */
 int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias,
                   int n_mat, int rows, int K, int gate_up, void* out, moe_stream_t stream);
@@ -195,8 +196,11 @@ int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t*
  *        FP32 additions is not fixed.
  * weights: canonical layout for MOE_IMPL_SIMT, repacked layout otherwise.
  * block_map / num_blocks: moe_route's outputs for the same block_n.
- * impl: MOE_IMPL_* (AUTO = TC).  The TC kernel needs block_n <= 128,
- * H % 128 == 0 and F % 128 == 0; SIMT needs block_n <= 128.
+ * impl: MOE_IMPL_*.  AUTO takes GEMV for block_n <= 8 and TC otherwise
+ * (both read the repacked layout).  TC needs block_n <= 128, H % 128 == 0
+ * and F % 128 == 0; GEMV (decode: tiles of at most 8 token rows) needs
+ * block_n <= 8, H % 128 == 0 and F % 128 == 0; SIMT needs block_n <= 128.
+ * Returns MOE_ERR_SHAPE when the chosen kernel cannot take the shape.
  */
 int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,
                        const void* w_packed, const uint16_t* w_scale, const uint16_t* w_bias,

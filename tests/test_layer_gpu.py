@@ -10,7 +10,7 @@ import gpu_util as G
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["tc", "simt"]
+IMPLS = ["tc", "simt", "gemv"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -109,11 +109,11 @@ def test_gate_up_intermediate(impl):
     x, logits = G.to_dev_inputs(d)
     b = layer.buffers(T)
     w = layer.weights
-    bn = layer.block_n
+    bn = layer.block_n_for(T)
     _lib.moe_route(logits, k, bn, b["topk_ids"], b["topk_w"], b["counts"], b["offsets"], b["perm"],
                    b["inv_perm"], b["block_map"], b["num_blocks"], b["workspace"])
     b["h"].zero_()
-    _lib.moe_expert_gemm_w4(_lib.GATE_UP, layer.impl, x, T, H, F, E, k, w.w13, w.s13, w.b13, b["perm"],
+    _lib.moe_expert_gemm_w4(_lib.GATE_UP, layer.impl_for(T), x, T, H, F, E, k, w.w13, w.s13, w.b13, b["perm"],
                             b["topk_w"], b["block_map"], b["num_blocks"], bn, b["h"])
     torch.cuda.synchronize()
     assert _lib.moe_get_device_error() == 0
