@@ -44,7 +44,7 @@ class Weights(ctypes.Structure):
 
 class Buffers(ctypes.Structure):
     _fields_ = [("topk_ids", _vp), ("topk_w", _vp), ("counts", _vp), ("offsets", _vp), ("perm", _vp),
-                ("inv_perm", _vp), ("block_map", _vp), ("num_blocks", _vp), ("h", _vp), ("acc", _vp),
+                ("inv_perm", _vp), ("block_map", _vp), ("num_blocks", _vp), ("h", _vp), ("y", _vp),
                 ("workspace", _vp), ("workspace_bytes", _sz)]
 
 
@@ -58,7 +58,7 @@ _SIGS = {
     "moe_repacked_bytes": ([_i, _i, _i], _sz),
     "moe_repack_w4": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
     "moe_expert_gemm_w4": ([_i, _i, _vp, _i, _i, _i, _i, _i] + [_vp] * 7 + [_i, _vp, _vp], _i),
-    "moe_combine": ([_vp, _vp, _i, _i, _vp], _i),
+    "moe_combine": ([_vp, _vp, _vp, _vp, _i, _i, _i, _vp], _i),
     "moe_layer_forward": ([_vp, _vp, _vp] + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
     "moe_layer_forward_host": ([_vp] * 6 + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
     "moe_get_device_error": ([ctypes.POINTER(ctypes.c_int32)], _i),
@@ -156,9 +156,11 @@ def moe_expert_gemm_w4(mode, impl, act, T, H, F, E, k, w_packed, w_scale, w_bias
           _ptr(perm), _ptr(topk_w), _ptr(block_map), _ptr(num_blocks), block_n, _ptr(out), _stream(stream))
 
 
-def moe_combine(acc, out, stream=None):
-    T, H = acc.shape
-    _call("moe_combine", _ptr(acc), _ptr(out), T, H, _stream(stream))
+def moe_combine(y, inv_perm, topk_w, out, stream=None):
+    """out[t] = bf16(sum_j topk_w[t, j] * y[inv_perm[t*k + j]] + y[A + t]); y bf16 [A+T, H]."""
+    T, k = topk_w.shape
+    H = out.shape[1]
+    _call("moe_combine", _ptr(y), _ptr(inv_perm), _ptr(topk_w), _ptr(out), T, H, k, _stream(stream))
 
 
 def moe_layer_forward(x, logits, out, T, H, F, E, k, block_n, impl, weights: Weights, buffers: Buffers,

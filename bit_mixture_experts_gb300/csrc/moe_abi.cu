@@ -52,7 +52,8 @@ cudaError_t launch_gemm_simt(int mode, const uint16_t* act, int T, int H, int F,
                              const uint16_t* ws, const uint16_t* wb, const int32_t* perm, const float* topk_w,
                              const int32_t* block_map, const int32_t* num_blocks, int bn, int nb_cap, void* out,
                              cudaStream_t s);
-cudaError_t launch_combine(float* acc, uint16_t* out, int T, int H, int num_sms, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T,
+                           int H, int k, int num_sms, cudaStream_t s);
 size_t repacked_bytes(int n_mat, int rows, int K);
 cudaError_t launch_repack(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias, int n_mat, int rows,
                           int K, int gate_up, void* out, cudaStream_t s);
@@ -136,7 +137,7 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
                        void* out, moe_stream_t stream) {
   int rc = check_shape(T, H, F, E, k, block_n);
   if (rc) return rc;
-  if (mode != MOE_GATE_UP_SWIGLU && mode != MOE_DOWN_COMBINE) return MOE_ERR_MODE;
+  if (mode != MOE_GATE_UP_SWIGLU && mode != MOE_DOWN) return MOE_ERR_MODE;
   rc = check_ptrs(act, w_packed, perm, topk_w, block_map, num_blocks, out);
   if (rc) return rc;
   if (!device_error_ptr()) return MOE_ERR_CUDA;
@@ -163,11 +164,14 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
   }
 }
 
-int moe_combine(float* acc, uint16_t* out, int T, int H, moe_stream_t stream) {
-  if (T < 1 || H < 64 || H % 64 != 0) return MOE_ERR_SHAPE;
-  int rc = check_ptrs(acc, out);
+int moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T, int H,
+                int k, moe_stream_t stream) {
+  if (T < 1 || T > (1 << 20) || H < 8 || H % 8 != 0 || k < 1 || k > 32) return MOE_ERR_SHAPE;
+  int rc = check_ptrs(y, inv_perm, topk_w, out);
   if (rc) return rc;
-  return cuda_status(launch_combine(acc, out, T, H, num_sms(), reinterpret_cast<cudaStream_t>(stream)));
+  if (!device_error_ptr()) return MOE_ERR_CUDA;
+  return cuda_status(
+      launch_combine(y, inv_perm, topk_w, out, T, H, k, num_sms(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out, int T, int H, int F, int E, int k,
@@ -179,10 +183,10 @@ int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out, int
   rc = moe_expert_gemm_w4(MOE_GATE_UP_SWIGLU, impl, x, T, H, F, E, k, w->w13, w->s13, w->b13, b->perm, b->topk_w,
                           b->block_map, b->num_blocks, block_n, b->h, stream);
   if (rc) return rc;
-  rc = moe_expert_gemm_w4(MOE_DOWN_COMBINE, impl, b->h, T, H, F, E, k, w->w2, w->s2, w->b2, b->perm, b->topk_w,
-                          b->block_map, b->num_blocks, block_n, b->acc, stream);
+  rc = moe_expert_gemm_w4(MOE_DOWN, impl, b->h, T, H, F, E, k, w->w2, w->s2, w->b2, b->perm, b->topk_w,
+                          b->block_map, b->num_blocks, block_n, b->y, stream);
   if (rc) return rc;
-  return moe_combine(b->acc, out, T, H, stream);
+  return moe_combine(b->y, b->inv_perm, b->topk_w, out, T, H, k, stream);
 }
 
 int moe_layer_forward_host(const uint16_t* x_host, const float* logits_host, uint16_t* out_host, uint16_t* x_dev,

@@ -5,26 +5,36 @@
 // 1 every routed expert's weights are read once per token, so the layer is a
 // stream of the 8 + 1 selected experts' packed weights and the work per weight
 // is a handful of ALU operations.  There is nothing for the tensor cores to do
-// here; what matters is keeping enough of that stream in flight on every SM.
+// here; what matters is keeping that stream in flight on every SM and keeping
+// the chain of dependent steps per work item short.
 //
 // Weights use the repacked layout of the tensor-core kernel (per matrix, per
 // 128-row M-tile, per 64-wide K group: [2 halves][128 rows][16 B] nibbles +
 // [128 rows](scale, bias)), so one copy of the weights serves both kernels and
 // a warp's 32 rows of one half are 512 contiguous bytes.
 //
-// Work item (persistent grid, GV_CTAS_PER_SM CTAs of 256 threads per SM):
-//   gate/up: (tile, 32 features): the 32 gate and 32 up rows of those
-//            features (M-tiles 2j, 2j+1 of the repacked pair layout) against
-//            all H; warp w takes K groups w, w+8, ...; lane = feature.
-//   down:    (tile, 128 output channels = one M-tile) against all F; warp w
-//            takes lane quarter w % 4 and K groups w / 4, w / 4 + 2, ...
-// Each thread first issues the loads of all its weight words (up to GV_GB
-// groups) into registers, then stages the tile's activation rows in shared
-// memory, then expands each word to bf16 pairs exactly as the tensor-core
-// kernel does (w = bf16(q * scale + bias), one fma.rn.bf16x2 per pair) and
-// accumulates w * x in FP32 with mixed-precision FMAs.  Partial sums of the
-// warps are added in shared memory in a fixed order.
+// Work item (persistent grid, GV_CTAS_PER_SM CTAs of 256 threads per SM; 32
+// weight rows per item so that a batch-1 layer still gives every CTA work):
+//   gate/up: (tile, 16 features): lanes 0-15 take the gate rows and lanes
+//            16-31 the up rows of those features (M-tiles 2j, 2j+1 of the
+//            repacked pair layout); warp w takes K groups w, w+8, ...
+//   down:    (tile, 32 output channels); warp w takes K groups w, w+8, ...
+// Each thread owns one weight row of the item.  It copies its row's groups (36
+// bytes each) into its own shared-memory slots with cp.async one item ahead
+// (two slot buffers), so the next item's weights stream while this one is
+// computed, and it waits only for its own copies: no barrier guards the weight
+// stream.  The activations (a few rows, shared by every warp) are read straight
+// from global memory through L1 in the inner loop.  Each word is expanded to
+// bf16 pairs exactly as the tensor-core kernel does (w = bf16(q * scale +
+// bias), one fma.rn.bf16x2 per pair) and multiplied into FP32 accumulators with
+// mixed-precision FMAs (bf16 x bf16 -> FP32, full rate on the FMA pipe).  The
+// group loop is not unrolled and the token count is a template parameter
+// picked per tile (1, 2 or 4 rows per pass), which keeps the code small: a fully
+// unrolled version spent most of its time on instruction-cache misses.  The
+// warps' partial sums are added in shared memory in a fixed order (one barrier
+// per item; the partial-sum buffer alternates between items).
 #include "moe_common.cuh"
+#include "moe_ptx.cuh"
 
 namespace moe {
 
@@ -33,7 +43,7 @@ namespace {
 constexpr int GV_THREADS = 256;
 constexpr int GV_WARPS = GV_THREADS / 32;
 constexpr int GV_MAXN = 8;  // token rows per tile
-constexpr int GV_GB = 4;    // K groups a thread holds in registers at once
+constexpr int GV_GB = 8;    // K groups per thread at most (K <= 64 * 8 * 8 = 4096)
 constexpr int GV_CTAS_PER_SM = 2;
 constexpr int KG = 64;
 constexpr int TC_M = 128;
@@ -50,6 +60,7 @@ struct GvParams {
   void* out;
   int* err;
   int T, H, F, E, k, bn, cap;
+  int G;  // K groups per thread: ceil(K / 64 / 8)
 };
 
 // bf16 pair of weights (element 2j in the low half, 2j+1 in the high half) of
@@ -70,62 +81,45 @@ __device__ __forceinline__ void dot_pair(float& acc, uint32_t w2, uint32_t x2) {
       : "r"(w2), "r"(x2));
 }
 
-// One repacked row of one K group: 8 words (K elements 8w .. 8w+7) + (scale, bias).
-struct RowGroup {
-  uint4 lo, hi;
-  uint32_t sb;
-};
-
-__device__ __forceinline__ RowGroup load_row_group(const uint8_t* blk, int L) {
-  RowGroup g;
-  g.lo = __ldg(reinterpret_cast<const uint4*>(blk + L * 16));
-  g.hi = __ldg(reinterpret_cast<const uint4*>(blk + 2048 + L * 16));
-  g.sb = __ldg(reinterpret_cast<const uint32_t*>(blk + W_PACKED + L * 4));
-  return g;
-}
-
-__device__ __forceinline__ uint32_t word_of(const RowGroup& g, int w) {
-  const uint4& v = w < 4 ? g.lo : g.hi;
-  switch (w & 3) {
-    case 0: return v.x;
-    case 1: return v.y;
-    case 2: return v.z;
-    default: return v.w;
-  }
-}
-
-// acc[n] += sum over the group's 64 K of w * x[n], n < rows (x: bf16 rows in smem, pitch K)
-template <int NM>
-__device__ __forceinline__ void group_dot(const RowGroup (&g)[NM], const uint16_t* sx, int K, int k0, int rows,
-                                          float (&acc)[NM][GV_MAXN]) {
-  uint32_t s2[NM], b2[NM];
-#pragma unroll
-  for (int m = 0; m < NM; ++m) {
-    s2[m] = (g[m].sb & 0xffffu) * 0x10001u;
-    b2[m] = (g[m].sb >> 16) * 0x10001u;
-  }
+// acc[n] += sum over one K group of w * x[n] for token rows n = N0 .. N0+NT-1:
+// the row's packed words (lo: K 0..31, hi: K 32..63 of the group), its
+// (scale, bias) and the group's activations of each row at xg + xoff[n]
+// (bf16, global, read via L1).
+template <int N0, int NT>
+__device__ __forceinline__ void group_dot(uint4 lo, uint4 hi, uint32_t sb, const uint16_t* xg,
+                                          const uint32_t (&xoff)[GV_MAXN], float (&acc)[GV_MAXN]) {
+  const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
+  const uint32_t b2 = (sb >> 16) * 0x10001u;
+  const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
-    uint32_t wp[NM][4];
+    uint32_t wp[4];
 #pragma unroll
-    for (int m = 0; m < NM; ++m) {
-      const uint32_t word = word_of(g[m], w);
+    for (int j = 0; j < 4; ++j) wp[j] = dequant_pair(words[w], j, s2, b2);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) wp[m][j] = dequant_pair(word, j, s2[m], b2[m]);
+    for (int n = N0; n < N0 + NT; ++n) {
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(xg + xoff[n]) + w);
+      dot_pair(acc[n], wp[0], x.x);
+      dot_pair(acc[n], wp[1], x.y);
+      dot_pair(acc[n], wp[2], x.z);
+      dot_pair(acc[n], wp[3], x.w);
     }
-#pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n) {
-      if (n < rows) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(sx + n * K + k0 + 8 * w);
-#pragma unroll
-        for (int m = 0; m < NM; ++m) {
-          dot_pair(acc[m][n], wp[m][0], xv.x);
-          dot_pair(acc[m][n], wp[m][1], xv.y);
-          dot_pair(acc[m][n], wp[m][2], xv.z);
-          dot_pair(acc[m][n], wp[m][3], xv.w);
-        }
-      }
-    }
+  }
+}
+
+// All of this thread's groups of one item from its slots (slot i of the
+// buffer: words at swq[2i], swq[2i+1], (scale, bias) at swsb[i]; one thread's
+// slots are GV_THREADS apart).
+template <int N0, int NT>
+__device__ __forceinline__ void item_dot(const uint4* swq, const uint32_t* swsb, const uint16_t* act,
+                                         const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
+                                         float (&acc)[GV_MAXN]) {
+#pragma unroll 1
+  for (int i = 0; i < G; ++i) {
+    const int kg = warp + GV_WARPS * i;
+    if (kg >= KT) break;
+    group_dot<N0, NT>(swq[(2 * i) * GV_THREADS], swq[(2 * i + 1) * GV_THREADS], swsb[i * GV_THREADS], act + kg * KG,
+                  xoff, acc);
   }
 }
 
@@ -140,24 +134,39 @@ __device__ __forceinline__ bool gv_tile(const GvParams& p, int b, Tile* t) {
   return ok;
 }
 
+// Weight row of item j of a tile for this lane: (M-tile, row within it).
+template <int MODE>
+__device__ __forceinline__ void item_row(int j, int lane, int* mt, int* L) {
+  if (MODE == 0) {
+    const int f = 16 * j + (lane & 15);
+    *mt = 2 * (f / TC_M) + (lane >> 4);  // gate M-tile, or the up M-tile after it
+    *L = f % TC_M;
+  } else {
+    const int c = 32 * j + lane;
+    *mt = c / TC_M;
+    *L = c % TC_M;
+  }
+}
+
 }  // namespace
 
-// MODE 0: h[r, f] = bf16(silu(g) * u) for the tile's rows r.  MODE 1: acc[token] += w * y.
+// MODE 0: h[r, f] = bf16(silu(g) * u) for the tile's rows r.  MODE 1: y[r, c] = bf16(h[r] . Wd[c]).
 template <int MODE>
 __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) gemv_kernel(const GvParams p) {
   extern __shared__ uint4 gv_smem[];
-  __shared__ int s_tok[GV_MAXN];
-  __shared__ float s_wt[GV_MAXN];
-  constexpr int NM = MODE == 0 ? 2 : 1;  // matrices per thread: gate and up, or down
   const int K = MODE == 0 ? p.H : p.F;
   const int KT = K / KG;
+  const int G = p.G;
   const int MT = MODE == 0 ? (2 * p.F) / TC_M : p.H / TC_M;
-  const int IPT = MODE == 0 ? p.F / 32 : MT;  // work items per tile
+  const int IPT = MODE == 0 ? p.F / 16 : p.H / 32;  // work items per tile
   const int A = p.T * p.k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint16_t* sx = reinterpret_cast<uint16_t*>(gv_smem);  // [GV_MAXN][K] bf16
-  float* spart = reinterpret_cast<float*>(sx + GV_MAXN * K);
-  // MODE 0: spart[warp][m][n][lane]; MODE 1: spart[khalf][n][128 rows]
+  // shared memory: per buffer b: weight slots [2 G][threads] x 16 B and (scale, bias)
+  // slots [G][threads] x 4 B; then partial sums [2][warps][GV_MAXN][32] floats
+  const int slot_q = 2 * G * GV_THREADS, slot_sb = G * GV_THREADS;
+  uint4* swq0 = gv_smem;
+  uint32_t* swsb0 = reinterpret_cast<uint32_t*>(gv_smem + 2 * slot_q);
+  float* spart0 = reinterpret_cast<float*>(swsb0 + 2 * slot_sb);
 
   int nb = __ldg(p.num_blocks);
   if (nb < 0 || nb > p.cap) {
@@ -165,142 +174,128 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) gemv_kernel(const 
     nb = nb < 0 ? 0 : p.cap;
   }
   const int items = nb * IPT;
-  // K groups of this thread: MODE 0: warp, warp + 8, ...; MODE 1: khalf, khalf + 2, ...
-  const int kstep = MODE == 0 ? GV_WARPS : 2;
-  const int kfirst = MODE == 0 ? warp : (warp >> 2);
-  const int L = MODE == 0 ? 0 : 32 * (warp & 3) + lane;  // MODE 1: row within the M-tile
 
-  for (int u = blockIdx.x; u < items; u += gridDim.x) {
-    const int b = u / IPT, j = u - b * IPT;
+  // copies of item u's row of this thread into buffer b (one commit group, possibly empty)
+  auto issue = [&](int u, int b) {
+    if (u < items) {
+      const int tb = u / IPT, j = u - tb * IPT;
+      Tile t;
+      if (gv_tile(p, tb, &t)) {
+        int mt, L;
+        item_row<MODE>(j, lane, &mt, &L);
+        const uint8_t* wrow = p.w + (static_cast<size_t>(t.expert) * MT + mt) * KT * static_cast<size_t>(W_BLOCK);
+        uint4* q = swq0 + b * slot_q + threadIdx.x;
+        uint32_t* sb = swsb0 + b * slot_sb + threadIdx.x;
+#pragma unroll 1
+        for (int i = 0; i < G; ++i) {
+          const int kg = warp + GV_WARPS * i;
+          if (kg >= KT) break;
+          const uint8_t* blk = wrow + static_cast<size_t>(kg) * W_BLOCK;
+          ptx::cp_async_16(ptx::smem_u32(q + (2 * i) * GV_THREADS), blk + L * 16);
+          ptx::cp_async_16(ptx::smem_u32(q + (2 * i + 1) * GV_THREADS), blk + 2048 + L * 16);
+          ptx::cp_async_4(ptx::smem_u32(sb + i * GV_THREADS), blk + W_PACKED + L * 4);
+        }
+      }
+    }
+    ptx::cp_async_commit();
+  };
+
+  issue(blockIdx.x, 0);
+  int it = 0;
+  for (int u = blockIdx.x; u < items; u += gridDim.x, ++it) {
+    const int buf = it & 1;
+    issue(u + gridDim.x, buf ^ 1);  // next item's weights stream during this one
+    const int tb = u / IPT, j = u - tb * IPT;
     Tile t;
-    if (!gv_tile(p, b, &t)) {
+    if (!gv_tile(p, tb, &t)) {
       if (threadIdx.x == 0) set_device_error(p.err, MOE_DEV_BAD_BLOCK);
       continue;
     }
-    // weight rows of this item
-    const uint8_t* wbase[NM];
-    int Lw;
-    if (MODE == 0) {
-      const int f = 32 * j + lane, pair = f / TC_M;
-      Lw = f % TC_M;
-      wbase[0] = p.w + (static_cast<size_t>(t.expert) * MT + 2 * pair) * KT * static_cast<size_t>(W_BLOCK);
-      if (NM > 1) wbase[NM - 1] = wbase[0] + static_cast<size_t>(KT) * W_BLOCK;
-    } else {
-      Lw = L;
-      wbase[0] = p.w + (static_cast<size_t>(t.expert) * MT + j) * KT * static_cast<size_t>(W_BLOCK);
+    // gate/up: token of tile row n in lane n (the down GEMM reads the h rows in place)
+    const int nrow = t.rows;
+    int tok_l = -1;
+    if (MODE == 0 && lane < nrow) {
+      const int r = t.row0 + lane;
+      if (r < A) {
+        const int a = __ldg(p.perm + r);
+        if (a >= 0 && a < A) tok_l = a / p.k;
+        else if (warp == 0) set_device_error(p.err, MOE_DEV_BAD_INDEX);
+      } else {
+        tok_l = r - A;
+      }
     }
-    float acc[NM][GV_MAXN];
+    // element offset of each row's activations in act (below 2^32: T x H and (A+T) x F are checked on the host)
+    uint32_t xoff[GV_MAXN];
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
+    for (int n = 0; n < GV_MAXN; ++n) {
+      const int tk = __shfl_sync(0xffffffffu, tok_l, n);
+      // MODE 0: token row of x (rows past the tile, or a bad index, read token 0); MODE 1: row of h
+      xoff[n] = MODE == 0 ? static_cast<uint32_t>(tk < 0 ? 0 : tk) * static_cast<uint32_t>(K)
+                          : static_cast<uint32_t>(t.row0 + (n < nrow ? n : 0)) * static_cast<uint32_t>(K);
+    }
+    float acc[GV_MAXN];
 #pragma unroll
-      for (int n = 0; n < GV_MAXN; ++n) acc[m][n] = 0.f;
-
-    __syncthreads();  // the previous item is done with sx / spart / s_tok
-    for (int kb = 0; kb < KT; kb += kstep * GV_GB) {
-      // 1. this thread's weight words for up to GV_GB groups, all loads in flight at once
-      RowGroup g[GV_GB][NM];
-#pragma unroll
-      for (int i = 0; i < GV_GB; ++i) {
-        const int kg = kb + kfirst + kstep * i;
-        if (kg < KT) {
-#pragma unroll
-          for (int m = 0; m < NM; ++m) g[i][m] = load_row_group(wbase[m] + static_cast<size_t>(kg) * W_BLOCK, Lw);
-        }
-      }
-      // 2. (first batch) the tile's activation rows -> smem, while those loads are in flight
-      if (kb == 0) {
-        if (threadIdx.x < t.rows) {
-          const int i = threadIdx.x, r = t.row0 + i;
-          int tok = -1;
-          float wt = 0.f;
-          if (r < A) {
-            const int a = __ldg(p.perm + r);
-            if (a >= 0 && a < A) {
-              tok = a / p.k;
-              wt = __ldg(p.topk_w + a);
-            } else {
-              set_device_error(p.err, MOE_DEV_BAD_INDEX);
-            }
-          } else {
-            tok = r - A;
-            wt = 1.0f;
-          }
-          s_tok[i] = tok;
-          s_wt[i] = wt;
-        }
-        __syncthreads();
-        const int cpr = K / 8;  // 16-byte chunks per row
-        for (int idx = threadIdx.x; idx < t.rows * cpr; idx += GV_THREADS) {
-          const int i = idx / cpr, c = idx - i * cpr;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (MODE == 0) {
-            const int tok = s_tok[i];
-            if (tok >= 0) v = __ldg(reinterpret_cast<const uint4*>(p.act + static_cast<size_t>(tok) * K) + c);
-          } else {
-            v = __ldg(reinterpret_cast<const uint4*>(p.act + static_cast<size_t>(t.row0 + i) * K) + c);
-          }
-          reinterpret_cast<uint4*>(sx + i * K)[c] = v;
-        }
-        __syncthreads();
-      }
-      // 3. expand and accumulate
-#pragma unroll
-      for (int i = 0; i < GV_GB; ++i) {
-        const int kg = kb + kfirst + kstep * i;
-        if (kg < KT) group_dot<NM>(g[i], sx, K, kg * KG, t.rows, acc);
-      }
+    for (int n = 0; n < GV_MAXN; ++n) acc[n] = 0.f;
+    ptx::cp_async_wait<1>();  // this thread's copies of item u have landed
+    const uint4* swq = swq0 + buf * slot_q + threadIdx.x;
+    const uint32_t* swsb = swsb0 + buf * slot_sb + threadIdx.x;
+    if (nrow == 1) {
+      item_dot<0, 1>(swq, swsb, p.act, xoff, warp, KT, G, acc);
+    } else if (nrow == 2) {
+      item_dot<0, 2>(swq, swsb, p.act, xoff, warp, KT, G, acc);
+    } else {
+      // up to 4 rows per pass (more would spill registers); 5-8 rows expand the weights twice
+      item_dot<0, 4>(swq, swsb, p.act, xoff, warp, KT, G, acc);
+      if (nrow > 4) item_dot<4, 4>(swq, swsb, p.act, xoff, warp, KT, G, acc);
     }
 
     // reduce the warps' partial sums (fixed order) and finish the item
+    float* spart = spart0 + buf * (GV_WARPS * GV_MAXN * 32);
+#pragma unroll
+    for (int n = 0; n < GV_MAXN; ++n)
+      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + lane] = acc[n];
+    __syncthreads();
     if (MODE == 0) {
-#pragma unroll
-      for (int m = 0; m < NM; ++m)
-#pragma unroll
-        for (int n = 0; n < GV_MAXN; ++n)
-          if (n < t.rows) spart[((warp * NM + m) * GV_MAXN + n) * 32 + lane] = acc[m][n];
-      __syncthreads();
-      if (threadIdx.x < t.rows * 32) {
-        const int n = threadIdx.x >> 5;
+      if (threadIdx.x < nrow * 16) {
+        const int n = threadIdx.x >> 4, fi = threadIdx.x & 15;
         float gs = 0.f, us = 0.f;
         for (int w = 0; w < GV_WARPS; ++w) {
-          gs += spart[((w * NM + 0) * GV_MAXN + n) * 32 + lane];
-          us += spart[((w * NM + NM - 1) * GV_MAXN + n) * 32 + lane];
+          gs += spart[(w * GV_MAXN + n) * 32 + fi];
+          us += spart[(w * GV_MAXN + n) * 32 + 16 + fi];
         }
         uint16_t* h = static_cast<uint16_t*>(p.out);
-        h[static_cast<size_t>(t.row0 + n) * p.F + 32 * j + lane] = float_to_bf16_bits(silu(gs) * us);
+        h[static_cast<size_t>(t.row0 + n) * p.F + 16 * j + fi] = float_to_bf16_bits(silu(gs) * us);
       }
     } else {
-      const int kh = warp >> 2;
-#pragma unroll
-      for (int n = 0; n < GV_MAXN; ++n)
-        if (n < t.rows) spart[(kh * GV_MAXN + n) * TC_M + L] = acc[0][n];
-      __syncthreads();
-      float* out = static_cast<float*>(p.out);
-      for (int idx = threadIdx.x; idx < t.rows * TC_M; idx += GV_THREADS) {
-        const int n = idx / TC_M, row = idx - n * TC_M;
-        const int tok = s_tok[n];
-        if (tok >= 0) {
-          const float y = spart[n * TC_M + row] + spart[(GV_MAXN + n) * TC_M + row];
-          atomicAdd(out + static_cast<size_t>(tok) * p.H + TC_M * j + row, s_wt[n] * y);
-        }
+      // warp n finishes tile row n: y[row0 + n, 32 j + lane]
+      if (warp < nrow) {
+        float y = 0.f;
+        for (int w = 0; w < GV_WARPS; ++w) y += spart[(w * GV_MAXN + warp) * 32 + lane];
+        static_cast<uint16_t*>(p.out)[static_cast<size_t>(t.row0 + warp) * p.H + 32 * j + lane] =
+            float_to_bf16_bits(y);
       }
     }
   }
+  ptx::cp_async_wait_all();  // no copy may still be landing when the CTA exits
 }
 
 int gemv_max_rows() { return GV_MAXN; }
 
+static int gemv_groups(int K) { return (K / KG + GV_WARPS - 1) / GV_WARPS; }
+
 size_t gemv_smem_bytes(int mode, int H, int F) {
-  const int K = mode == MOE_GATE_UP_SWIGLU ? H : F;
-  const size_t part = mode == MOE_GATE_UP_SWIGLU ? static_cast<size_t>(GV_WARPS) * 2 * GV_MAXN * 32 * 4
-                                                 : static_cast<size_t>(2) * GV_MAXN * TC_M * 4;
-  return static_cast<size_t>(GV_MAXN) * K * 2 + part;
+  const int G = gemv_groups(mode == MOE_GATE_UP_SWIGLU ? H : F);
+  return 2 * static_cast<size_t>(G) * GV_THREADS * (2 * 16 + 4) + 2 * static_cast<size_t>(GV_WARPS) * GV_MAXN * 32 * 4;
 }
 
 cudaError_t launch_gemm_gemv(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                              const int32_t* perm, const float* topk_w, const int32_t* block_map,
                              const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s) {
   if (bn > GV_MAXN) return cudaErrorInvalidValue;
+  // activation offsets are 32-bit
+  if (static_cast<unsigned long long>(T) * H >= (1ull << 32) ||
+      static_cast<unsigned long long>(T) * (k + 1) * F >= (1ull << 32))
+    return cudaErrorInvalidValue;
   GvParams prm;
   prm.act = act;
   prm.w = static_cast<const uint8_t*>(w);
@@ -317,6 +312,8 @@ cudaError_t launch_gemm_gemv(int mode, const uint16_t* act, int T, int H, int F,
   prm.k = k;
   prm.bn = bn;
   prm.cap = cap;
+  prm.G = gemv_groups(mode == MOE_GATE_UP_SWIGLU ? H : F);
+  if (prm.G > GV_GB) return cudaErrorInvalidValue;
   const size_t smem = gemv_smem_bytes(mode, H, F);
   int dev = 0, max_smem = 0;
   cudaGetDevice(&dev);

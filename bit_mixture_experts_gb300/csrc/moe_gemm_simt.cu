@@ -58,7 +58,7 @@ __device__ bool load_tile(const int32_t* __restrict__ block_map, int b, int E, i
   return true;
 }
 
-// MODE 0: gate/up + SwiGLU -> h bf16 [A+T, F].  MODE 1: down -> acc += w * y.
+// MODE 0: gate/up + SwiGLU -> h bf16 [A+T, F].  MODE 1: down -> y bf16 [A+T, H].
 template <int MODE>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const uint16_t* __restrict__ act, int T, int H, int F,
                                                         int E, int k, const uint32_t* __restrict__ wq,
@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const uint16_t* __restri
       uint16_t* h = static_cast<uint16_t*>(out);
       h[static_cast<size_t>(tile.row0 + i) * F + c0 + lane] = float_to_bf16_bits(silu(acc0[j]) * acc1[j]);
     } else {
-      float* accum = static_cast<float*>(out);
-      atomicAdd(accum + static_cast<size_t>(s_tok[i]) * H + c0 + lane, s_wt[i] * acc0[j]);
+      uint16_t* y = static_cast<uint16_t*>(out);
+      y[static_cast<size_t>(tile.row0 + i) * H + c0 + lane] = float_to_bf16_bits(acc0[j]);
     }
   }
 }
@@ -176,25 +176,80 @@ cudaError_t launch_gemm_simt(int mode, const uint16_t* act, int T, int H, int F,
 }
 
 // --------------------------------------------------------------------------
-// combine: out = bf16(acc), acc = 0
+// combine: out[t] = bf16(sum_j topk_w[t, j] y[inv_perm[t k + j]] + y[A + t])
+// One thread per 8 channels of a token (16-byte loads of each y row), the
+// FP32 sum in the fixed order j = 0 .. k-1, then the shared row.  Rows are
+// taken 8 at a time with all their index and row loads issued before the
+// sums, so the latency of the gather is paid once per 8 rows.
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) combine_kernel(float4* __restrict__ acc, uint2* __restrict__ out, size_t n4) {
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y,
+                                                      const int32_t* __restrict__ inv_perm,
+                                                      const float* __restrict__ topk_w, uint16_t* __restrict__ out,
+                                                      int T, int H, int k, int* err) {
+  constexpr int RB = 8;  // rows per batch
+  const int c8 = H / 8;  // 8-channel chunks per row
+  const int A = T * k;
+  const size_t n = static_cast<size_t>(T) * c8;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float4 v = acc[i];
-    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int t = static_cast<int>(i / c8), c = static_cast<int>(i - static_cast<size_t>(t) * c8);
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int j0 = 0; j0 <= k; j0 += RB) {
+      int r[RB];
+      float w[RB];
+#pragma unroll
+      for (int b = 0; b < RB; ++b) {
+        const int j = j0 + b;
+        r[b] = -1;
+        w[b] = 0.f;
+        if (j < k) {
+          r[b] = __ldg(inv_perm + static_cast<size_t>(t) * k + j);
+          w[b] = __ldg(topk_w + static_cast<size_t>(t) * k + j);
+        } else if (j == k) {
+          r[b] = A + t;
+          w[b] = 1.0f;
+        }
+      }
+      uint4 v[RB];
+#pragma unroll
+      for (int b = 0; b < RB; ++b) {
+        const int j = j0 + b;
+        const bool ok = j <= k && r[b] >= 0 && r[b] < A + T && (j == k || r[b] < A);
+        if (j <= k && !ok) set_device_error(err, MOE_DEV_BAD_INDEX);
+        v[b] = ok ? __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(r[b]) * H) + c)
+                  : make_uint4(0u, 0u, 0u, 0u);
+        if (!ok) w[b] = 0.f;
+      }
+#pragma unroll
+      for (int b = 0; b < RB; ++b) {
+        const uint32_t u[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = fmaf(w[b], __uint_as_float(u[q] << 16), acc[2 * q]);
+          acc[2 * q + 1] = fmaf(w[b], __uint_as_float(u[q] & 0xffff0000u), acc[2 * q + 1]);
+        }
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H)[c] = o;
   }
 }
 
-cudaError_t launch_combine(float* acc, uint16_t* out, int T, int H, int num_sms, cudaStream_t s) {
-  const size_t n4 = static_cast<size_t>(T) * H / 4;
-  size_t blocks = (n4 + 255) / 256;
+cudaError_t launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T,
+                           int H, int k, int num_sms, cudaStream_t s) {
+  const size_t n = static_cast<size_t>(T) * (H / 8);
+  size_t blocks = (n + 255) / 256;
   const size_t cap = static_cast<size_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks == 0) blocks = 1;
-  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<float4*>(acc),
-                                                               reinterpret_cast<uint2*>(out), n4);
+  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(y, inv_perm, topk_w, out, T, H, k,
+                                                               device_error_ptr());
   note_launches(1);
   return cudaGetLastError();
 }

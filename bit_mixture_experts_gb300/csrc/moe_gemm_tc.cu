@@ -31,9 +31,7 @@
 //               gate/up: the unit's two M-tiles are the gate and the up rows
 //                        of the same 128 features, so each thread holds g and
 //                        u of its feature: h = bf16(silu(g) * u) -> h[row, f]
-//               down:    y goes through shared memory (transpose to 4
-//                        channels per thread) and acc[token] += w * y is
-//                        added with 16-byte FP32 vector reductions
+//               down:    y = bf16(acc) -> y[row, channel]
 //
 // Every mbarrier wait is bounded by a time limit; on expiry the kernel records
 // MOE_DEV_TIMEOUT in the device error word, every role leaves its loop, copies
@@ -49,17 +47,14 @@ namespace moe {
 namespace {
 
 constexpr int TC_M = 128;              // weight rows per M-tile (the MMA's M)
-constexpr int MG = 2;                  // M-tiles per work unit; they share each activation stage
 constexpr int KG = 64;                 // one quantisation group
 constexpr int GPS = 2;                 // quant groups per pipeline stage
 constexpr int KS = KG * GPS;           // K per stage
 constexpr int W_PACKED = TC_M * 32;    // packed nibbles of one M-tile x K group
 constexpr int W_BLOCK = W_PACKED + TC_M * 4;  // + (scale, bias) per row: one repacked block
-constexpr int W_STAGE = MG * GPS * W_BLOCK;   // packed weights of one stage
 constexpr int NWW = 3;                 // packed-weight slots per dequant warpgroup (each thread fills its own rows)
 constexpr int PD = NWW - 1;            // own stages each dequant thread prefetches ahead
-constexpr int A_COLS = MG * GPS * 32;  // TMEM columns of one dequantised stage
-constexpr int NAMAX = 3;               // dequantised-weight ring (TMEM), run-time depth 2 or 3
+constexpr int NAMAX = 4;               // dequantised-weight ring (TMEM), run-time depth 2 to 4
 constexpr int NBMAX = 12;              // activation ring (smem), run-time depth <= NBMAX
 constexpr int TMEM_COLS = 512;        // accumulators first, then the A ring
 constexpr int NTHREADS = 512;
@@ -76,12 +71,17 @@ constexpr int BAR_FIN = BAR_DEMPTY + 2;
 constexpr int NBAR = BAR_FIN + 1;
 
 // smem layout (offsets from a 1024-byte aligned base): B ring | W ring | barriers | misc
-constexpr int W_RING_BYTES = 2 * NWW * W_STAGE;  // two warpgroups
 constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
 constexpr int MISC_BYTES = 16;  // abort flag, TMEM base
-constexpr int EPI_PITCH = 36;   // floats per token row of the down epilogue's transpose buffer (16-byte rows)
-constexpr int EPI_BYTES = 4 * 32 * EPI_PITCH * 4;  // one 32 tokens x 32 channels buffer per epilogue warp
-constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;  // + EPI_BYTES for the down GEMM
+
+// Sizes that depend on MG, the M-tiles per work unit (they share each activation stage).
+template <int MG>
+struct UnitCfg {
+  static constexpr int W_STAGE = MG * GPS * W_BLOCK;         // packed weights of one stage
+  static constexpr int A_COLS = MG * GPS * 32;               // TMEM columns of one dequantised stage
+  static constexpr int W_RING_BYTES = 2 * NWW * W_STAGE;     // two warpgroups
+  static constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;
+};
 
 static_assert((GPS * W_BLOCK) % (16 * 32) == 0, "a weight stage is copied as 16-byte chunks by 32 lanes");
 
@@ -164,10 +164,13 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f 
 
 }  // namespace
 
-// Work unit: one block-map tile (<= 128 token rows) x MG = 2 M-tiles (256
+// Work unit: one block-map tile (<= 128 token rows) x MG M-tiles (MG x 128
 // weight rows) of one expert.  Each pipeline stage covers K = 128 (two quant
-// groups): both M-tiles' packed blocks, their dequantised bf16 in TMEM and one
-// activation stage read by both M-tiles' MMAs.
+// groups): the M-tiles' packed blocks, their dequantised bf16 in TMEM and one
+// activation stage read by every M-tile's MMAs.  Gate/up always takes MG = 2
+// (the gate and the up M-tile of the same features); the down GEMM takes MG =
+// 1 for tiles of more than 64 rows, so that two accumulator buffers still fit
+// in TMEM and the epilogue of one unit overlaps the next unit's mainloop.
 //
 // Rings (full/empty mbarriers; stage index = running stage count `it` modulo
 // the ring depth):
@@ -178,9 +181,14 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f 
 //      gate/up: cp.async gather of token rows (warps 2-3),
 //      down: TMA tiles of contiguous h rows (warp 2)  -> MMA
 //   D  FP32 accumulators, TMEM, MMA -> epilogue (1 or 2 buffers)
-template <int MODE>
+template <int MODE, int MG>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmap_act) {
+  static_assert(MODE == 1 || MG == 2, "gate/up pairs the gate and the up M-tile in one unit");
+  static_assert(MG == 1 || MG == 2, "one or two M-tiles per unit");
+  constexpr int W_STAGE = UnitCfg<MG>::W_STAGE;
+  constexpr int A_COLS = UnitCfg<MG>::A_COLS;
+  constexpr int W_RING_BYTES = UnitCfg<MG>::W_RING_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       Tile t;
       int grp;
       if (!unit_tile(p, u, MGT, &t, &grp)) continue;
-      const bool two = grp * MG + 1 < MT;
+      const bool two = MG == 2 && grp * MG + 1 < MT;
       const uint32_t idesc = ptx::idesc_bf16_f32(TC_M, round16(t.rows));
       const int d = ui % ND, rd = ui / ND;
       if (rd > 0 && !wait_warp(bar(BAR_DEMPTY + d), (rd - 1) & 1, s_abort, p.err, lim)) goto mma_done;
@@ -503,51 +511,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                   float_to_bf16_bits(silu_fast(__uint_as_float(g[j])) * __uint_as_float(uu[j]));
         }
       } else {
-        // y[channel 32q + lane, token c0 + j] -> sx[j][lane]; then lane 8r + c adds
-        // channels 4c..4c+3 of tokens 4i + r (i = 0..7) with one 16-byte reduction each
-        float* sx = reinterpret_cast<float*>(smem + off_w + W_RING_BYTES + BAR_BYTES + MISC_BYTES) +
-                    q * (32 * EPI_PITCH);
-        const int r4 = lane >> 3, c4 = lane & 7;
-        float* acc = static_cast<float*>(p.out);
+        // lane = output channel of M-tile m: y[row0 + n, channel] = bf16(D[channel, n])
+        uint16_t* y = static_cast<uint16_t*>(p.out) + static_cast<size_t>(t.row0) * p.H;
         for (int m = 0; m < nm; ++m) {
-          const int ch0 = TC_M * (grp * MG + m) + 32 * q + 4 * c4;
+          const int ch = TC_M * (grp * MG + m) + 32 * q + lane;
           for (int c0 = 0; c0 < N; c0 += 32) {
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(tq + m * DM + c0, v);
-            // token and combine weight of column c0 + lane
-            int tok = -1;
-            float wt = 0.f;
-            const int n_l = c0 + lane;
-            if (n_l < t.rows) {
-              const int r = t.row0 + n_l;
-              if (r < A) {
-                const int a = __ldg(p.perm + r);
-                if (a >= 0 && a < A) {
-                  tok = a / p.k;
-                  wt = __ldg(p.topk_w + a);
-                } else {
-                  set_device_error(p.err, MOE_DEV_BAD_INDEX);
-                }
-              } else {
-                tok = r - A;
-                wt = 1.0f;
-              }
-            }
             ptx::tmem_wait_ld();
+            const int nv = t.rows - c0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sx[j * EPI_PITCH + lane] = __uint_as_float(v[j]);
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int j = 4 * i + r4;
-              const int tj = __shfl_sync(0xffffffffu, tok, j);
-              const float wj = __shfl_sync(0xffffffffu, wt, j);
-              const float4 y = *reinterpret_cast<const float4*>(sx + j * EPI_PITCH + 4 * c4);
-              if (tj >= 0)
-                atomicAdd(reinterpret_cast<float4*>(acc + static_cast<size_t>(tj) * p.H + ch0),
-                          make_float4(wj * y.x, wj * y.y, wj * y.z, wj * y.w));
-            }
-            __syncwarp();
+            for (int j = 0; j < 32; ++j)
+              if (j < nv) y[static_cast<size_t>(c0 + j) * p.H + ch] = float_to_bf16_bits(__uint_as_float(v[j]));
           }
         }
       }
@@ -695,7 +670,10 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   if (boxr > 128) return cudaErrorInvalidValue;
   prm.boxr = boxr;
   prm.sb = GPS * boxr * 128;
-  const int tail = TAIL_BYTES + (mode == MOE_DOWN_COMBINE ? EPI_BYTES : 0);
+  // M-tiles per unit: gate/up pairs gate and up; the down GEMM keeps two accumulator buffers
+  const int MG = (mode == MOE_GATE_UP_SWIGLU || boxr <= 64) ? 2 : 1;
+  const int tail = MG == 2 ? UnitCfg<2>::TAIL_BYTES : UnitCfg<1>::TAIL_BYTES;
+  const int a_cols = MG == 2 ? UnitCfg<2>::A_COLS : UnitCfg<1>::A_COLS;
   const int budget = max_dyn_smem() - tail - 1024;
   int nbs = budget / prm.sb;
   if (nbs > NBMAX) nbs = NBMAX;
@@ -705,16 +683,16 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   // TMEM: accumulators (nd buffers x 2 M-tiles x boxr columns), then the A ring
   // a second accumulator buffer (the epilogue of one unit overlaps the next
   // unit's mainloop) when at least two A slots remain
-  prm.nd = 2 * (2 * boxr) + 2 * A_COLS <= TMEM_COLS ? 2 : 1;
-  prm.a0 = prm.nd * 2 * boxr;
-  prm.na = (TMEM_COLS - prm.a0) / A_COLS;
+  prm.nd = 2 * (MG * boxr) + 2 * a_cols <= TMEM_COLS ? 2 : 1;
+  prm.a0 = prm.nd * MG * boxr;
+  prm.na = (TMEM_COLS - prm.a0) / a_cols;
   if (prm.na > NAMAX) prm.na = NAMAX;
   const int smem = nbs * prm.sb + tail + 1024;
 
   // activation tensor map (down only): tiles of boxr contiguous rows of h [A+T, F]
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
-  if (mode == MOE_DOWN_COMBINE) {
+  if (mode == MOE_DOWN) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int A = T * k;
@@ -728,11 +706,14 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   if (mode == MOE_GATE_UP_SWIGLU) {
-    cudaFuncSetAttribute(gemm_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    gemm_tc_kernel<0><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
+    cudaFuncSetAttribute(gemm_tc_kernel<0, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    gemm_tc_kernel<0, 2><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
+  } else if (MG == 2) {
+    cudaFuncSetAttribute(gemm_tc_kernel<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    gemm_tc_kernel<1, 2><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
   } else {
-    cudaFuncSetAttribute(gemm_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    gemm_tc_kernel<1><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
+    cudaFuncSetAttribute(gemm_tc_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    gemm_tc_kernel<1, 1><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
   }
   note_launches(1);
   return cudaGetLastError();

@@ -109,11 +109,11 @@ class MoELayerW4:
             "block_map": torch.empty((cap, 3), dtype=torch.int32, device=dev),
             "num_blocks": torch.empty(1, dtype=torch.int32, device=dev),
             "h": torch.empty((A + T, F), dtype=torch.bfloat16, device=dev),
-            "acc": torch.zeros((T, H), dtype=torch.float32, device=dev),
+            "y": torch.empty((A + T, H), dtype=torch.bfloat16, device=dev),
             "workspace": torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev),
         }
         t["struct"] = _lib.Buffers(*(t[n].data_ptr() for n in ("topk_ids", "topk_w", "counts", "offsets", "perm",
-                                                                 "inv_perm", "block_map", "num_blocks", "h", "acc",
+                                                                 "inv_perm", "block_map", "num_blocks", "h", "y",
                                                                  "workspace")), wsb)
         self._bufs[T] = t
         return t

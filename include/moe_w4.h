@@ -64,7 +64,7 @@ enum {
 /* GEMM modes. */
 enum {
   MOE_GATE_UP_SWIGLU = 0, /* h = bf16(silu(x Wg^T) * (x Wu^T)) per routed row */
-  MOE_DOWN_COMBINE = 1    /* acc[t] += w * (h Wd^T), FP32 */
+  MOE_DOWN = 1            /* y = bf16(h Wd^T) per routed row */
 };
 
 /* GEMM implementations. */
@@ -188,12 +188,10 @@ int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t*
  *        for r < A and token r-A for r >= A (shared expert);
  *   out  bf16 [A+T, F]: h[r] = bf16(silu(g) * u), g/u the gate/up projections
  *        accumulated in FP32 over the bf16-expanded weights.
- * mode MOE_DOWN_COMBINE:
+ * mode MOE_DOWN:
  *   act  bf16 [A+T, F] the h of the gate/up call;
- *   out  float32 [T, H] accumulator: acc[token(r)] += w(r) * (h[r] Wd^T), with
- *        w(r) = topk_w[perm[r]] for r < A and 1 for the shared expert.  acc
- *        must be zero on entry (moe_combine leaves it zero).  The order of the
- *        FP32 additions is not fixed.
+ *   out  bf16 [A+T, H]: y[r] = bf16(h[r] Wd^T) accumulated in FP32, in the
+ *        same permuted row order (perm and topk_w are not read).
  * weights: canonical layout for MOE_IMPL_SIMT, repacked layout otherwise.
  * block_map / num_blocks: moe_route's outputs for the same block_n.
  * impl: MOE_IMPL_*.  AUTO takes GEMV for block_n <= 8 and TC otherwise
@@ -209,11 +207,19 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
                        void* out, moe_stream_t stream);
 
 /*
- * moe_combine -- finish the weighted combine back to token order:
- * out[t, c] = bf16(acc[t, c]) (round to nearest even), then acc[t, c] = 0 so
- * the accumulator is ready for the next layer call.
+ * moe_combine -- weighted gather-combine back to token order ("Perplexity
+ * Open Sources Lily", Technical Details, Model bullet: 8 routed experts plus
+ * one shared expert per token):
+ *   out[t, c] = bf16( sum_{j<k} topk_w[t, j] * y[inv_perm[t*k + j], c]
+ *                     + y[A + t, c] )
+ * with the sum in FP32 in that fixed order (j = 0 .. k-1, then the shared
+ * row), rounded once to nearest even.  y bf16 [A+T, H] is the down GEMM's
+ * output, inv_perm int32 [A] and topk_w float32 [T, k] come from moe_route;
+ * out bf16 [T, H].  H % 8 == 0.  An inv_perm entry outside [0, A) sets
+ * MOE_DEV_BAD_INDEX and that term is skipped.
  */
-int moe_combine(float* acc, uint16_t* out, int T, int H, moe_stream_t stream);
+int moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T, int H,
+                int k, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Whole layer                                                              */
@@ -230,7 +236,7 @@ typedef struct {
   int32_t* block_map;  /* [moe_block_map_capacity, 3] */
   int32_t* num_blocks; /* [1] */
   uint16_t* h;         /* bf16 [A+T, F] */
-  float* acc;          /* [T, H], zero on the first call; left zero by every call */
+  uint16_t* y;         /* bf16 [A+T, H] */
   void* workspace;     /* moe_route_workspace_size bytes */
   size_t workspace_bytes;
 } moe_buffers_t;

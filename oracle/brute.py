@@ -90,11 +90,12 @@ def ffn_one(x, w13, w2):
         u = float(np.dot(w13[F + f], x))
         h.append(rne_bf16(g / (1.0 + math.exp(-g)) * u))
     h = np.array(h)
-    return np.array([float(np.dot(w2[c], h)) for c in range(w2.shape[0])]), h
+    # the down projection's rows are bf16 as well
+    return np.array([rne_bf16(float(np.dot(w2[c], h))) for c in range(w2.shape[0])]), h
 
 
 def forward(x_bits, logits, wts, k):
-    """Per token: out = bf16(sum_j w_j * FFN_{e_j}(x) + FFN_shared(x))."""
+    """Per token: out = bf16(sum_j w_j * FFN_{e_j}(x) + FFN_shared(x)), each FFN output row rounded to bf16."""
     T, E = np.asarray(logits).shape
     cache = ExpertCache(wts)
     outs, all_ids, all_w = [], [], []

@@ -11,16 +11,18 @@ Step by step, in the pages' order:
 3. groupwise affine 4-bit weights, 64 weights per group with a bf16 scale (and
    bias, "affine"), expanded to bf16 only inside the grouped GEMM (same bullet;
    itinai.com post, paragraph 2: no full bfloat16 copy is allocated);
-4. grouped SwiGLU expert GEMM with FP32 (here: exact float64) accumulation;
-5. weighted combine of the k routed experts plus the shared expert (weight 1)
-   back to token order (Technical Details, Model bullet: "8 of 256 experts plus
-   one shared expert").
+4. grouped SwiGLU expert GEMM with FP32 (here: exact float64) accumulation,
+   whose outputs (h of the gate/up projection, y of the down projection) are
+   bf16 rows in expert order;
+5. weighted gather-combine of each token's k routed rows plus its shared-expert
+   row (weight 1) back to token order (Technical Details, Model bullet: "8 of
+   256 experts plus one shared expert").
 
 Readings where the pages are silent (each is listed in the design notes):
 ties in top-k go to the lower expert index; the dequantised weight is
 round-to-nearest-even bf16 of the exact q*scale + bias; h = bf16(silu(g) * u);
-the down projection y stays unrounded; the output is bf16 of the exact
-weighted sum.  Nibble k of a 32-bit word holds K element 8*w + k in bits
+y = bf16(h Wd^T) (the grouped GEMM writes bf16); the output is bf16 of the
+exact weighted sum of the y rows.  Nibble k of a 32-bit word holds K element 8*w + k in bits
 [4k, 4k+4).
 """
 from __future__ import annotations
@@ -182,9 +184,14 @@ def bf16_floor_ceil(a):
     return np.ldexp(np.floor(m * 256.0), e - 8), np.ldexp(np.ceil(m * 256.0), e - 8)
 
 
-def expert_down(h, w2) -> np.ndarray:
-    """y = h Wd^T, exact (float64), not rounded."""
+def expert_down_exact(h, w2) -> np.ndarray:
+    """h Wd^T, exact (float64), before the grouped GEMM's bf16 output rounding."""
     return h @ w2.T
+
+
+def down_output(y_exact) -> np.ndarray:
+    """y = bf16(h Wd^T): the down projection's rows are written as bf16 like h."""
+    return round_bf16(y_exact)
 
 
 def expert_weights(wts: dict, e: int):
@@ -193,8 +200,9 @@ def expert_weights(wts: dict, e: int):
     return w13, w2
 
 
-def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = False, h_given=None) -> dict:
-    """The layer: out[t] = bf16( sum_j w[t,j] * y_{e_j}(x_t) + y_shared(x_t) ).
+def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = False, h_given=None,
+                want_y: bool = False, y_given=None) -> dict:
+    """The layer: out[t] = bf16( sum_j w[t,j] * y_{e_j}(x_t) + y_shared(x_t) ), y = bf16(h Wd^T).
 
     ``tokens`` restricts the computation to a subset of token indices (routing
     of a token depends on its own logits only), which is how full-size
@@ -204,7 +212,9 @@ def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = F
     (key "h_exact").  ``h_given(t, e)``, when set, supplies h instead of the
     gate/up projection: the down projection and combine are then evaluated
     exactly on that h (used to check a rounding of h that differs from
-    round-to-nearest on values next to a rounding midpoint).
+    round-to-nearest on values next to a rounding midpoint).  ``want_y`` and
+    ``y_given`` do the same for the bf16 rows y of the down projection (keys
+    "y" and "y_exact"; with ``y_given`` only the combine is evaluated).
     """
     logits = np.asarray(logits, dtype=np.float32)
     T, E = logits.shape
@@ -213,13 +223,17 @@ def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = F
     x = bf16_value(np.asarray(x_bits)[sel])
     n, H = x.shape
     acc = np.zeros((n, H), dtype=np.float64)
-    hs, hx = {}, {}
+    hs, hx, ys, yx = {}, {}, {}, {}
     for e in sorted(set(np.unique(ids).tolist()) | {E}):
         if e == E:
             rows, wt = np.arange(n), np.ones(n)
         else:
             rows, cols = np.nonzero(ids == e)
             wt = w[rows, cols]
+        if y_given is not None:
+            y = np.stack([np.asarray(y_given(int(sel[r]), int(e)), dtype=np.float64) for r in rows])
+            acc[rows] += wt[:, None] * y
+            continue
         w13, w2 = expert_weights(wts, e)
         if h_given is not None:
             h = np.stack([np.asarray(h_given(int(sel[r]), int(e)), dtype=np.float64) for r in rows])
@@ -230,10 +244,18 @@ def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = F
                 for i, r in enumerate(rows):
                     hs[(int(sel[r]), int(e))] = h[i]
                     hx[(int(sel[r]), int(e))] = v[i]
-        y = expert_down(h, w2)
+        yv = expert_down_exact(h, w2)
+        y = down_output(yv)
+        if want_y:
+            for i, r in enumerate(rows):
+                ys[(int(sel[r]), int(e))] = y[i]
+                yx[(int(sel[r]), int(e))] = yv[i]
         acc[rows] += wt[:, None] * y
     res = {"out": round_bf16(acc), "topk_ids": ids, "topk_w": w, "tokens": sel}
     if want_h:
         res["h"] = hs
         res["h_exact"] = hx
+    if want_y:
+        res["y"] = ys
+        res["y_exact"] = yx
     return res

@@ -81,6 +81,9 @@ def test_gemm_argument_errors(lib):
 
 
 def test_combine_argument_errors(lib):
-    assert lib.moe_combine(ctypes.c_void_p(16), ctypes.c_void_p(16), 4, 100, None) == -3
-    assert lib.moe_combine(None, ctypes.c_void_p(16), 4, 128, None) == -1
-    assert lib.moe_combine(ctypes.c_void_p(20), ctypes.c_void_p(16), 4, 128, None) == -2
+    p = ctypes.c_void_p(16)
+    assert lib.moe_combine(p, p, p, p, 4, 100, 2, None) == -3       # H % 8
+    assert lib.moe_combine(p, p, p, p, 4, 128, 0, None) == -3       # k < 1
+    assert lib.moe_combine(p, p, p, p, 4, 128, 33, None) == -3      # k > 32
+    assert lib.moe_combine(None, p, p, p, 4, 128, 2, None) == -1
+    assert lib.moe_combine(p, p, ctypes.c_void_p(20), p, 4, 128, 2, None) == -2

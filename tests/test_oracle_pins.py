@@ -50,6 +50,17 @@ def test_given_h_reproduces_layer():
         assert np.array_equal(h, moe_ref.round_bf16(ref["h_exact"][key]))
 
 
+def test_given_y_reproduces_layer():
+    """The combine evaluated on the oracle's own bf16 y rows reproduces the layer output, and y is
+    the bf16 rounding of the exact down projection of h."""
+    d = workloads.make_workload(workloads.custom(9, 128, 4, 2, 64), 2)
+    ref = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, want_y=True)
+    again = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, y_given=lambda t, e: ref["y"][(t, e)])
+    assert np.array_equal(ref["out"], again["out"])
+    for key, y in ref["y"].items():
+        assert np.array_equal(y, moe_ref.round_bf16(ref["y_exact"][key]))
+
+
 def test_skew_calibration():
     """The skewed long prefill leaves about 30 experts empty and one expert chosen by
     nearly every token (at most T of the T*k assignments can go to one expert)."""
@@ -80,7 +91,7 @@ def test_generator_statistics():
 # --------------------------------------------------------------------------- #
 def _mutations():
     orig = {n: getattr(moe_ref, n) for n in
-            ("unpack_u4", "dequant", "expert_swiglu_exact", "topk_route", "expert_down",
+            ("unpack_u4", "dequant", "expert_swiglu_exact", "topk_route", "expert_down_exact",
              "expert_weights", "stable_permutation", "round_bf16", "block_map", "exclusive_scan")}
 
     def msb_first(p):
@@ -146,7 +157,8 @@ def _mutations():
         "silu_on_up": ("expert_swiglu_exact", silu_on_up),
         "ties_to_high_index": ("topk_route", ties_high),
         "no_renormalisation": ("topk_route", no_renorm),
-        "down_transposed": ("expert_down", down_transposed),
+        "down_transposed": ("expert_down_exact", down_transposed),
+        "y_not_rounded": ("down_output", lambda y: np.asarray(y, dtype=np.float64)),
         "shared_expert_dropped": ("expert_weights", no_shared),
         "unstable_scatter": ("stable_permutation", unstable),
         "bf16_truncation": ("round_bf16", truncate),
