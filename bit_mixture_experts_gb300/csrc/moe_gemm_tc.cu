@@ -18,7 +18,10 @@
 // Roles (512 threads, one CTA per SM, persistent over (block-map tile, M-tile)).
 // Warps 0-2 run their loops converged with warp-uniform operands and let
 // elect.sync pick the lane that issues each copy, MMA or commit:
-//   warp 0      idle (each dequant thread fetches its own weight row)
+//   warp 0      streams the packed weights into a shared-memory ring with
+//               cp.async.bulk: one copy per M-tile and stage (the stage's
+//               quant groups of an M-tile are contiguous), completion counted
+//               in bytes on the slot's mbarrier
 //   warp 1      allocates TMEM; issues tcgen05.mma (A from TMEM, B from smem)
 //   warp 2      loads the tile's activation rows into 128B-swizzled smem with
 //               TMA: gate/up gathers token rows of x four at a time
@@ -52,8 +55,7 @@ constexpr int GPS = 2;                 // quant groups per pipeline stage
 constexpr int KS = KG * GPS;           // K per stage
 constexpr int W_PACKED = TC_M * 32;    // packed nibbles of one M-tile x K group
 constexpr int W_BLOCK = W_PACKED + TC_M * 4;  // + (scale, bias) per row: one repacked block
-constexpr int NWW = 3;                 // packed-weight slots per dequant warpgroup (each thread fills its own rows)
-constexpr int PD = NWW - 1;            // own stages each dequant thread prefetches ahead
+constexpr int NWB = 12;                // packed-weight ring bytes, in units of one M-tile's stage
 constexpr int NAMAX = 4;               // dequantised-weight ring (TMEM), run-time depth 2 to 4
 constexpr int NBMAX = 12;              // activation ring (smem), run-time depth <= NBMAX
 constexpr int TMEM_COLS = 512;        // accumulators first, then the A ring
@@ -61,7 +63,10 @@ constexpr int NTHREADS = 512;
 constexpr int GATHER_T = 64;           // threads gathering activation rows (gate/up)
 
 // barrier indices
-constexpr int BAR_AFULL = 0;
+constexpr int NWMAX = NWB;             // weight ring slots (NWB / MG)
+constexpr int BAR_WFULL = 0;
+constexpr int BAR_WEMPTY = BAR_WFULL + NWMAX;
+constexpr int BAR_AFULL = BAR_WEMPTY + NWMAX;
 constexpr int BAR_AEMPTY = BAR_AFULL + NAMAX;
 constexpr int BAR_BFULL = BAR_AEMPTY + NAMAX;
 constexpr int BAR_BEMPTY = BAR_BFULL + NBMAX;
@@ -79,11 +84,12 @@ template <int MG>
 struct UnitCfg {
   static constexpr int W_STAGE = MG * GPS * W_BLOCK;         // packed weights of one stage
   static constexpr int A_COLS = MG * GPS * 32;               // TMEM columns of one dequantised stage
-  static constexpr int W_RING_BYTES = 2 * NWW * W_STAGE;     // two warpgroups
+  static constexpr int NW = NWB / MG;                        // weight ring slots
+  static constexpr int W_RING_BYTES = NW * W_STAGE;
   static constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;
 };
 
-static_assert((GPS * W_BLOCK) % (16 * 32) == 0, "a weight stage is copied as 16-byte chunks by 32 lanes");
+static_assert((GPS * W_BLOCK) % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 struct TcParams {
   const uint16_t* act;
@@ -174,8 +180,8 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f 
 //
 // Rings (full/empty mbarriers; stage index = running stage count `it` modulo
 // the ring depth):
-//   W  packed 4-bit blocks, smem; each dequant thread prefetches its own
-//      row's bytes with cp.async and waits for its own copies
+//   W  packed 4-bit blocks, smem, bulk copies by warp 0 -> dequant warps
+//      (freed as soon as a warp has its rows in registers)
 //   A  dequantised bf16 weights, TMEM, dequant warps -> MMA (warp 1)
 //   B  activation rows, 128B-swizzled K-major atoms of 64 K, smem,
 //      gate/up: cp.async gather of token rows (warps 2-3),
@@ -189,6 +195,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   constexpr int W_STAGE = UnitCfg<MG>::W_STAGE;
   constexpr int A_COLS = UnitCfg<MG>::A_COLS;
   constexpr int W_RING_BYTES = UnitCfg<MG>::W_RING_BYTES;
+  constexpr int NW = UnitCfg<MG>::NW;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -220,6 +227,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     *s_abort = 0;
+    for (int s = 0; s < NWMAX; ++s) {
+      ptx::mbar_init(bar(BAR_WFULL + s), 1);
+      ptx::mbar_init(bar(BAR_WEMPTY + s), 4);
+    }
     for (int s = 0; s < NAMAX; ++s) {
       ptx::mbar_init(bar(BAR_AFULL + s), 4);
       ptx::mbar_init(bar(BAR_AEMPTY + s), 1);
@@ -245,9 +256,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *s_tmem;
   const unsigned long long lim = p.wait_cycles;
   int prod_b = 0;  // activation TMA stages issued (down), for the drain after a timeout
+  int prod_w = 0;  // weight stages issued, for the drain after a timeout
 
   if (warp == 0) {
-    // (idle: the dequant warps fetch their own weight rows)
+    // ------------------------------------------------ weight producer: bulk copies into the W ring
+    int& it = prod_w;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      Tile t;
+      int grp;
+      if (!unit_tile(p, u, MGT, &t, &grp)) continue;
+      const int nm = min(MG, MT - grp * MG);
+      const uint8_t* g0 = p.w + (static_cast<size_t>(t.expert) * MT + grp * MG) * KT * static_cast<size_t>(W_BLOCK);
+      for (int ks = 0; ks < NS; ++ks, ++it) {
+        const int s = it % NW, r = it / NW;
+        if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto wprod_done;
+        const uint32_t dst = sbase + off_w + s * W_STAGE;
+        ptx::mbar_arrive_expect_tx_elect(bar(BAR_WFULL + s), static_cast<uint32_t>(nm * GPS * W_BLOCK));
+        for (int m = 0; m < nm; ++m)
+          ptx::bulk_g2s_elect(dst + m * GPS * W_BLOCK, g0 + (static_cast<size_t>(m) * KT + ks * GPS) * W_BLOCK,
+                              GPS * W_BLOCK, bar(BAR_WFULL + s));
+      }
+    }
+  wprod_done:;
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (whole warp, one lane issues)
     // The issue sequence is kept branch-free and fully unrolled with warp-uniform
@@ -272,27 +302,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::tc_fence_after();
         const uint32_t a0 = tmem + A0 + sa * A_COLS;
         const uint32_t b0 = sbase + sb * SB;
-        const uint64_t bd0 = ptx::smem_desc_sw128(b0), bd1 = ptx::smem_desc_sw128(b0 + atom_bytes);
         const uint32_t acc0 = ks != 0;
+        // A columns of the stage: M-tile m, quant group g at m * GPS * 32 + g * 32;
+        // group g's activations are B atom g (K = 64, four K16 steps)
         if (two) {
-          ptx::mma_ts_elect(d0, a0, bd0, idesc, acc0);
-          ptx::mma_ts_elect(d1, a0 + 64, bd0, idesc, acc0);
 #pragma unroll
-          for (int j = 1; j < 4; ++j) {
-            ptx::mma_ts_elect(d0, a0 + 8 * j, bd0 + 2 * j, idesc, 1);
-            ptx::mma_ts_elect(d1, a0 + 64 + 8 * j, bd0 + 2 * j, idesc, 1);
-          }
+          for (int g = 0; g < GPS; ++g) {
+            const uint64_t bd = ptx::smem_desc_sw128(b0 + g * atom_bytes);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            ptx::mma_ts_elect(d0, a0 + 32 + 8 * j, bd1 + 2 * j, idesc, 1);
-            ptx::mma_ts_elect(d1, a0 + 96 + 8 * j, bd1 + 2 * j, idesc, 1);
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t acc = (g == 0 && j == 0) ? acc0 : 1u;
+              ptx::mma_ts_elect(d0, a0 + g * 32 + 8 * j, bd + 2 * j, idesc, acc);
+              ptx::mma_ts_elect(d1, a0 + GPS * 32 + g * 32 + 8 * j, bd + 2 * j, idesc, acc);
+            }
           }
         } else {
-          ptx::mma_ts_elect(d0, a0, bd0, idesc, acc0);
 #pragma unroll
-          for (int j = 1; j < 4; ++j) ptx::mma_ts_elect(d0, a0 + 8 * j, bd0 + 2 * j, idesc, 1);
+          for (int g = 0; g < GPS; ++g) {
+            const uint64_t bd = ptx::smem_desc_sw128(b0 + g * atom_bytes);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) ptx::mma_ts_elect(d0, a0 + 32 + 8 * j, bd1 + 2 * j, idesc, 1);
+            for (int j = 0; j < 4; ++j)
+              ptx::mma_ts_elect(d0, a0 + g * 32 + 8 * j, bd + 2 * j, idesc, (g == 0 && j == 0) ? acc0 : 1u);
+          }
         }
         ptx::mma_commit_elect(bar(BAR_AEMPTY + sa));
         ptx::mma_commit_elect(bar(BAR_BEMPTY + sb));
@@ -372,8 +403,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (tok[j] >= 0) {
               const uint16_t* src = p.act + static_cast<size_t>(tok[j]) * K + ks * KS + chunk * 8;
               const uint32_t dst = dst0 + (i >> 3) * 1024 + (i & 7) * 128 + ((chunk ^ (i & 7)) << 4);
-              ptx::cp_async_16(dst, src);
-              ptx::cp_async_16(dst + atom_bytes, src + KG);
+#pragma unroll
+              for (int g = 0; g < GPS; ++g) ptx::cp_async_16(dst + g * atom_bytes, src + g * KG);
             }
           }
           // the barrier counts one arrival per gather thread, made by the hardware
@@ -385,50 +416,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp < 12) {
     // ------------------------------------------------ dequant: warpgroup wg expands the stages it with it % 2 == wg
-    // (both M-tiles of the unit), so one warpgroup computes while the other waits.
-    // Each thread owns one weight row of each M-tile: it prefetches that row's
-    // packed bytes PD of its own stages ahead into its own slots with cp.async
-    // and waits for its own copies, so no other warp is involved in the weight stream.
+    // (every M-tile of the unit), so one warpgroup computes while the other waits.
+    // Each thread owns one weight row of each M-tile (= its TMEM lane).  It loads
+    // its rows of the stage from the W ring into registers and frees the slot
+    // before expanding them.
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int L = 32 * q + lane;  // weight row within each M-tile = TMEM lane
-    const uint32_t wring = sbase + off_w + wg * NWW * W_STAGE;
-    // prefetch cursor over this CTA's (unit, stage) sequence, restricted to stages it % 2 == wg
-    int pu = blockIdx.x, pks = 0, pgrp = 0, pit = 0;
-    Tile pt;
-    while (pu < units && !unit_tile(p, pu, MGT, &pt, &pgrp)) pu += gridDim.x;
-    auto advance = [&]() {
-      ++pit;
-      if (++pks == NS) {
-        pks = 0;
-        do {
-          pu += gridDim.x;
-        } while (pu < units && !unit_tile(p, pu, MGT, &pt, &pgrp));
-      }
-    };
-    if ((pit & 1) != wg && pu < units) advance();
-    auto prefetch = [&](int slot) {
-      if (pu < units) {
-        const int nm = min(MG, MT - pgrp * MG);
-        for (int m = 0; m < nm; ++m) {
-          const uint8_t* g = p.w + ((static_cast<size_t>(pt.expert) * MT + pgrp * MG + m) * KT + pks * GPS) *
-                                       static_cast<size_t>(W_BLOCK);
-          const uint32_t d = wring + slot * W_STAGE + m * GPS * W_BLOCK;
-#pragma unroll
-          for (int gg = 0; gg < GPS; ++gg) {
-            ptx::cp_async_16(d + gg * W_BLOCK + L * 16, g + gg * W_BLOCK + L * 16);
-            ptx::cp_async_16(d + gg * W_BLOCK + 2048 + L * 16, g + gg * W_BLOCK + 2048 + L * 16);
-            ptx::cp_async_4(d + gg * W_BLOCK + W_PACKED + L * 4, g + gg * W_BLOCK + W_PACKED + L * 4);
-          }
-        }
-        advance();
-        if (pu < units) advance();  // skip the other warpgroup's stage
-      }
-      ptx::cp_async_commit();  // one group per own stage, possibly empty
-    };
-#pragma unroll 1
-    for (int i = 0; i < PD; ++i) prefetch(i);
-    int it = 0, own = 0;
+    int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
       int grp;
@@ -436,23 +431,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int nm = min(MG, MT - grp * MG);
       for (int ks = 0; ks < NS; ++ks, ++it) {
         if ((it & 1) != wg) continue;
-        const int sa = it % NA;
-        prefetch((own + PD) % NWW);
-        ptx::cp_async_wait<PD>();  // this thread's bytes of this stage have landed
-        const uint8_t* ws = smem + (wring - sbase) + (own % NWW) * W_STAGE;
-        ++own;
-        if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
-          goto dequant_done;
-        for (int m = 0; m < nm; ++m) {
+        const int sa = it % NA, sw = it % NW;
+        if (!wait_warp(bar(BAR_WFULL + sw), (it / NW) & 1, s_abort, p.err, lim)) goto dequant_done;
+        const uint8_t* ws = smem + off_w + sw * W_STAGE;
+        uint4 pk[MG][GPS][2];
+        uint32_t sbw[MG][GPS];
+#pragma unroll
+        for (int m = 0; m < MG; ++m)
 #pragma unroll
           for (int g = 0; g < GPS; ++g) {
             const uint8_t* blk = ws + (m * GPS + g) * W_BLOCK;
-            const uint4 p0 = *reinterpret_cast<const uint4*>(blk + L * 16);
-            const uint4 p1 = *reinterpret_cast<const uint4*>(blk + 2048 + L * 16);
-            const uint32_t sbw = *reinterpret_cast<const uint32_t*>(blk + W_PACKED + L * 4);
+            if (m < nm) {
+              pk[m][g][0] = *reinterpret_cast<const uint4*>(blk + L * 16);
+              pk[m][g][1] = *reinterpret_cast<const uint4*>(blk + 2048 + L * 16);
+              sbw[m][g] = *reinterpret_cast<const uint32_t*>(blk + W_PACKED + L * 4);
+            }
+          }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(BAR_WEMPTY + sw));  // this warp's rows are in registers
+        if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
+          goto dequant_done;
+#pragma unroll
+        for (int m = 0; m < MG; ++m) {
+          if (m >= nm) break;
+#pragma unroll
+          for (int g = 0; g < GPS; ++g) {
+            const uint4 p0 = pk[m][g][0], p1 = pk[m][g][1];
             const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            const uint32_t s2 = (sbw & 0xffffu) * 0x10001u;
-            const uint32_t b2 = (sbw >> 16) * 0x10001u;
+            const uint32_t s2 = (sbw[m][g] & 0xffffu) * 0x10001u;
+            const uint32_t b2 = (sbw[m][g] >> 16) * 0x10001u;
             constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
             uint32_t v[32];
 #pragma unroll
@@ -475,8 +482,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) ptx::mbar_arrive(bar(BAR_AFULL + sa));
       }
     }
-  dequant_done:
-    ptx::cp_async_wait_all();  // no prefetch may still be landing when the CTA exits
+  dequant_done:;
   } else {
     // ------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -539,6 +545,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // after a timeout some tile loads may never have been consumed: let them land before the CTA exits
     for (int t = prod_b - NB < 0 ? 0 : prod_b - NB; t < prod_b; ++t)
       wait_drain(bar(BAR_BFULL + t % NB), (t / NB) & 1, lim);
+  }
+  if (*s_abort && warp == 0 && lane == 0) {
+    // the same for the weight copies
+    for (int t = prod_w - NW < 0 ? 0 : prod_w - NW; t < prod_w; ++t)
+      wait_drain(bar(BAR_WFULL + t % NW), (t / NW) & 1, lim);
   }
   if (warp == 1) {
     ptx::tc_fence_after();
