@@ -191,7 +191,45 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if work["step_bytes"] < 2 * L2_BYTES \
         else None
 
+    def hold_stream():
+        # Hold the stream busy for a moment so the host can queue the steps ahead of the GPU: at
+        # decode sizes one host-side launch takes longer than the kernel, and the events would
+        # otherwise time the host.  (The end-to-end number below keeps the host in its clock.)
+        torch.cuda._sleep(int(min(100e-3, 0.3e-3 * args.steps + 2e-3) * 2.0e9))
+
+    # per-stage breakdown: eager launches with events between the stages (not the timed region)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    hold_stream()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)])
+    eager_ms = float(seg.sum(1).mean())
+    assert _lib.moe_get_device_error() == 0, "device error word set"
+
+    # the step captured once as a CUDA graph (the library launches only on the given stream and
+    # never synchronises, so the whole layer is capturable); the timed region replays it
+    graph, per_step_launches = None, None
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            n_cap = _lib.moe_launch_count()
+            with torch.cuda.graph(g):
+                step(None)
+            per_step_launches = _lib.moe_launch_count() - n_cap
+            g.replay()
+            torch.cuda.synchronize()
+            graph = g
+        except Exception as ex:  # report the eager timing instead
+            print(f"CUDA graph capture unavailable ({type(ex).__name__}: {ex}); timing eager launches",
+                  file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     clocks = ClockSampler(local_rank) if rank == 0 else None
     time.sleep(0.3)
     if world > 1:
@@ -200,25 +238,27 @@ def run_ours(args, rank, world, local_rank):
     n0 = _lib.moe_launch_count()
     if clocks:
         clocks.mark_start()
-    # Hold the stream busy for a moment so the host can queue the timed steps ahead of the GPU: at
-    # decode sizes one host-side launch takes longer than the kernel, and the events would otherwise
-    # time the host.  (The end-to-end number below keeps the host in its clock.)
-    torch.cuda._sleep(int(min(100e-3, 0.3e-3 * args.steps + 2e-3) * 2.0e9))
+    hold_stream()
     for i in range(args.steps):
         if flush is not None:
             flush.zero_()
-        step(events[i])
+        if graph is not None:
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        else:
+            ev[i][0].record(stream)
+            step(None)
+            ev[i][1].record(stream)
     torch.cuda.synchronize()
     if clocks:
         clocks.mark_end()
-    launches = _lib.moe_launch_count() - n0
+    launches = (_lib.moe_launch_count() - n0) if graph is None else per_step_launches * args.steps
     if world > 1:
         torch.distributed.barrier()
     if clocks:
         clocks.stop()
-    seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)])
-    step_ms = seg.sum(1)
-    ms = float(step_ms.mean())
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     ms = max_over_ranks(ms, world, dev)
     assert _lib.moe_get_device_error() == 0, "device error word set"
 
@@ -284,6 +324,8 @@ def run_ours(args, rank, world, local_rank):
         "tflops_step": work["step_flops"] / (ms * 1e-3) / 1e12,
         "roofline": roof,
         "gpu_launches": int(launches),
+        "launch": "cuda_graph" if graph is not None else "eager",
+        "eager_ms_per_step": eager_ms,
         "e2e": e2e,
     }
     if clocks:
@@ -398,6 +440,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a captured CUDA graph")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
