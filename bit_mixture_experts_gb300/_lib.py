@@ -25,7 +25,7 @@ IMPLS = {"auto": IMPL_AUTO, "simt": IMPL_SIMT, "tc": IMPL_TC, "gemv": IMPL_GEMV}
 
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
 SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
-           "moe_repacked_bytes", "moe_repack_w4", "moe_expert_gemm_w4", "moe_combine",
+           "moe_repacked_bytes", "moe_repack_w4", "moe_expert_gemm_w4", "moe_combine", "moe_decode_workspace_size",
            "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns"]
 
 
@@ -45,7 +45,7 @@ class Weights(ctypes.Structure):
 class Buffers(ctypes.Structure):
     _fields_ = [("topk_ids", _vp), ("topk_w", _vp), ("counts", _vp), ("offsets", _vp), ("perm", _vp),
                 ("inv_perm", _vp), ("block_map", _vp), ("num_blocks", _vp), ("h", _vp), ("y", _vp),
-                ("workspace", _vp), ("workspace_bytes", _sz)]
+                ("workspace", _vp), ("workspace_bytes", _sz), ("decode_ws", _vp), ("decode_ws_bytes", _sz)]
 
 
 _SIGS = {
@@ -59,6 +59,7 @@ _SIGS = {
     "moe_repack_w4": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
     "moe_expert_gemm_w4": ([_i, _i, _vp, _i, _i, _i, _i, _i] + [_vp] * 7 + [_i, _vp, _vp], _i),
     "moe_combine": ([_vp, _vp, _vp, _vp, _i, _i, _i, _vp], _i),
+    "moe_decode_workspace_size": ([_i, _i], _sz),
     "moe_layer_forward": ([_vp, _vp, _vp] + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
     "moe_layer_forward_host": ([_vp] * 6 + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
     "moe_get_device_error": ([ctypes.POINTER(ctypes.c_int32)], _i),
@@ -161,6 +162,10 @@ def moe_combine(y, inv_perm, topk_w, out, stream=None):
     T, k = topk_w.shape
     H = out.shape[1]
     _call("moe_combine", _ptr(y), _ptr(inv_perm), _ptr(topk_w), _ptr(out), T, H, k, _stream(stream))
+
+
+def moe_decode_workspace_size(T, H) -> int:
+    return int(load().moe_decode_workspace_size(T, H))
 
 
 def moe_layer_forward(x, logits, out, T, H, F, E, k, block_n, impl, weights: Weights, buffers: Buffers,

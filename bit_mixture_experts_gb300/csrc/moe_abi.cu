@@ -61,6 +61,14 @@ cudaError_t launch_gemm_gemv(int mode, const uint16_t* act, int T, int H, int F,
                              const int32_t* perm, const float* topk_w, const int32_t* block_map,
                              const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s);
 int gemv_max_rows();
+int decode_max_tokens();
+size_t decode_workspace_bytes(int T, int H);
+cudaError_t launch_decode(const uint16_t* x, const float* logits, const void* w13, const void* w2, int T, int H, int F,
+                          int E, int k, int bn, int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks, uint16_t* h,
+                          uint16_t* y, uint16_t* out, void* ws, unsigned long long wait_ns, int num_sms,
+                          cudaStream_t s);
+unsigned long long wait_limit_ns();
 cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                            const int32_t* perm, const float* topk_w, const int32_t* block_map,
                            const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s);
@@ -174,9 +182,30 @@ int moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
       launch_combine(y, inv_perm, topk_w, out, T, H, k, num_sms(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_decode_workspace_size(int T, int H) {
+  if (T < 1 || T > decode_max_tokens() || H < 64 || H % 32 != 0) return 0;
+  return decode_workspace_bytes(T, H);
+}
+
 int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out, int T, int H, int F, int E, int k,
                       int block_n, int impl, const moe_weights_t* w, const moe_buffers_t* b, moe_stream_t stream) {
   if (!w || !b) return MOE_ERR_NULL;
+  const bool gemv = impl == MOE_IMPL_GEMV || (impl == MOE_IMPL_AUTO && block_n <= gemv_max_rows());
+  if (gemv && b->decode_ws && T <= decode_max_tokens() && k <= 32) {
+    // the fused decode kernel: routing, both GEMVs and the combine in one launch
+    int rc = check_shape(T, H, F, E, k, block_n);
+    if (rc) return rc;
+    if (block_n > gemv_max_rows() || H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
+    rc = check_ptrs(x, logits, out, w->w13, w->w2, b->topk_ids, b->topk_w, b->counts, b->offsets, b->perm,
+                    b->inv_perm, b->block_map, b->num_blocks, b->h, b->y, b->decode_ws);
+    if (rc) return rc;
+    if (b->decode_ws_bytes < decode_workspace_bytes(T, H)) return MOE_ERR_WORKSPACE;
+    if (!device_error_ptr()) return MOE_ERR_CUDA;
+    return cuda_status(launch_decode(x, logits, w->w13, w->w2, T, H, F, E, k, block_n, b->topk_ids, b->topk_w,
+                                     b->counts, b->offsets, b->perm, b->inv_perm, b->block_map, b->num_blocks, b->h,
+                                     b->y, out, b->decode_ws, wait_limit_ns(), num_sms(),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+  }
   int rc = moe_route(logits, T, E, k, block_n, b->topk_ids, b->topk_w, b->counts, b->offsets, b->perm, b->inv_perm,
                      b->block_map, b->num_blocks, b->workspace, b->workspace_bytes, stream);
   if (rc) return rc;

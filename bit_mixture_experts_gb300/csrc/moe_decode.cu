@@ -1,0 +1,440 @@
+// Fused decode forward: the whole layer for at most DEC_MAXT tokens in one
+// persistent launch -- routing, gate/up GEMV + SwiGLU, down GEMV and the
+// weighted gather-combine.
+//
+// "Perplexity Open Sources Lily" (aitrending.vip), Technical Details: the
+// decode step is a small batch through 8 routed experts plus the shared
+// expert, every weight byte is read once per step, and the routing stays on
+// the GPU with no host synchronisation.  At batch 1 the four kernels of the
+// general path (route, gate/up, down, combine) each last only a few
+// microseconds, so their launch and dependency latencies dominate; here they
+// become phases of one kernel whose CTAs are all resident (cooperative
+// launch) and hand work to each other through counters in global memory.
+//
+// Phases, in every CTA (256 threads, GV_CTAS_PER_SM per SM):
+//   R  routing, recomputed by every CTA in shared memory from the logits with
+//      the same device code as moe_route (top-k and weights, counts, offsets,
+//      stable permutation, block map); CTA 0 also writes moe_route's outputs.
+//   G  gate/up work items (tile, 16 features), exactly as the GEMV kernel;
+//      after writing its h values an item adds 1 to its tile's counter.
+//   D  down work items (tile, 32 channels): the item's weights are copied in
+//      before it waits (bounded) until every gate/up item of its tile has
+//      finished; h is then read through L2 only.  After writing its y values
+//      it adds 1 to a counter per (token, 32 channels) for each of its rows;
+//      the item that brings a counter to k + 1 (all routed rows and the
+//      shared row of that token) gathers the combine for those 32 channels:
+//      out = bf16(sum_j topk_w[t, j] * y[row(t, j)] + y[shared row]), FP32 in
+//      the same fixed order as moe_combine.
+//   The last CTA to finish resets every counter to zero for the next call.
+// Items are dealt round-robin; each CTA finishes all of its gate/up items
+// before any down item, and only down items wait, so with every CTA resident
+// the waits always end.  Each wait is bounded nonetheless; on expiry it
+// records MOE_DEV_TIMEOUT and skips the item.
+#include "moe_common.cuh"
+#include "moe_gemv_dev.cuh"
+#include "moe_ptx.cuh"
+#include "moe_route_dev.cuh"
+
+namespace moe {
+
+using namespace gemv_dev;
+
+namespace {
+
+constexpr int DEC_MAXT = 8;                         // tokens per call
+constexpr int DEC_MAXA = DEC_MAXT * 32;             // assignments (k <= 32)
+constexpr int DEC_MAXTILES = DEC_MAXA + DEC_MAXT;   // routed tiles (>= 1 row each) + shared tiles
+
+struct DecParams {
+  const uint16_t* x;
+  const float* logits;
+  const uint8_t* w13;
+  const uint8_t* w2;
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv_perm;
+  int32_t* block_map;
+  int32_t* num_blocks;
+  uint16_t* h;
+  uint16_t* y;
+  uint16_t* out;
+  int* ws;  // [DEC_MAXTILES] gate/up items done per tile | [T][H/32] combine contributions | [1] CTAs done
+  int* err;
+  unsigned long long wait_cycles;
+  int T, H, F, E, k, bn;
+  int G;  // K groups per thread (max over the two matrices)
+};
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Groups of this thread's row of one item from its slots (see the GEMV kernel).
+template <int N0, int NT, bool COHERENT>
+__device__ __forceinline__ void dec_item_dot(const uint4* swq, const uint32_t* swsb, const uint16_t* act,
+                                             const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
+                                             float (&acc)[GV_MAXN]) {
+#pragma unroll 1
+  for (int i = 0; i < G; ++i) {
+    const int kg = warp + GV_WARPS * i;
+    if (kg >= KT) break;
+    group_dot<N0, NT, COHERENT>(swq[(2 * i) * GV_THREADS], swq[(2 * i + 1) * GV_THREADS], swsb[i * GV_THREADS],
+                                act + kg * KG, xoff, acc);
+  }
+}
+
+template <bool COHERENT>
+__device__ __forceinline__ void dec_dot(int nrow, const uint4* swq, const uint32_t* swsb, const uint16_t* act,
+                                        const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
+                                        float (&acc)[GV_MAXN]) {
+  if (nrow == 1) {
+    dec_item_dot<0, 1, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
+  } else if (nrow == 2) {
+    dec_item_dot<0, 2, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
+  } else {
+    dec_item_dot<0, 4, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
+    if (nrow > 4) dec_item_dot<4, 4, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(const DecParams p) {
+  __shared__ int s_ids[DEC_MAXA];
+  __shared__ float s_w[DEC_MAXA];
+  __shared__ int s_inv[DEC_MAXA];                // assignment -> permuted row
+  __shared__ int s_tok[DEC_MAXA + DEC_MAXT];     // permuted row -> token
+  __shared__ int s_tile[DEC_MAXTILES][3];        // (expert, first row, rows)
+  __shared__ uint64_t s_scan[33];
+  __shared__ int s_gather[GV_MAXN];              // tokens whose 32 channels this item completes
+  __shared__ int s_ngather, s_ok, s_last;
+  extern __shared__ uint4 dec_smem[];
+  const int T = p.T, E = p.E, k = p.k, bn = p.bn, H = p.H, F = p.F;
+  const int A = T * k;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // dynamic shared memory: weight slots of two items, (scale, bias) slots, partial sums, per-expert tables
+  const int G = p.G;
+  const int slot_q = 2 * G * GV_THREADS, slot_sb = G * GV_THREADS;
+  uint4* swq0 = dec_smem;
+  uint32_t* swsb0 = reinterpret_cast<uint32_t*>(dec_smem + 2 * slot_q);
+  float* spart0 = reinterpret_cast<float*>(swsb0 + 2 * slot_sb);
+  int* s_cnt = reinterpret_cast<int*>(spart0 + 2 * GV_WARPS * GV_MAXN * 32);  // [E]
+  int* s_off = s_cnt + E;                                                     // [E]
+  int* s_tile0 = s_off + E;                                                   // [E]
+  int* ws_tile = p.ws;
+  int* ws_cnt = p.ws + DEC_MAXTILES;
+  int* ws_done = ws_cnt + T * (H / 32);
+
+  // ---------------------------------------------------------------- R: routing
+  if (warp < T) {
+    int id;
+    float w;
+    route_dev::warp_topk_any(p.logits + static_cast<size_t>(warp) * E, E, k, lane, &id, &w);
+    if (lane < k) {
+      s_ids[warp * k + lane] = id;
+      s_w[warp * k + lane] = w;
+    }
+  }
+  for (int e = tid; e < E; e += GV_THREADS) s_cnt[e] = 0;
+  __syncthreads();
+  for (int a = tid; a < A; a += GV_THREADS) atomicAdd(&s_cnt[s_ids[a]], 1);  // integer counts
+  __syncthreads();
+  {
+    // offsets and first tile of every expert: exclusive scan of (count, tiles) in expert order
+    const int per = ceil_div(E, GV_THREADS);
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    uint64_t loc = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int c = s_cnt[e];
+      loc += (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(ceil_div(c, bn));
+    }
+    uint64_t total;
+    uint64_t run = route_dev::block_exclusive_scan(loc, s_scan, &total);
+    for (int e = e0; e < e1; ++e) {
+      const int c = s_cnt[e];
+      s_off[e] = static_cast<int>(run >> 32);
+      s_tile0[e] = static_cast<int>(run & 0xffffffffu);
+      run += (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(ceil_div(c, bn));
+    }
+    if (tid == 0) s_ok = static_cast<int>(total & 0xffffffffu);  // routed tiles
+  }
+  __syncthreads();
+  const int ntr = s_ok;
+  const int nt = ntr + ceil_div(T, bn);
+  // stable permutation: by expert, then by assignment index
+  for (int a = tid; a < A; a += GV_THREADS) {
+    const int e = s_ids[a];
+    int r = 0;
+    for (int a2 = 0; a2 < a; ++a2) r += s_ids[a2] == e;
+    const int row = s_off[e] + r;
+    s_inv[a] = row;
+    s_tok[row] = a / k;
+  }
+  for (int t = tid; t < T; t += GV_THREADS) s_tok[A + t] = t;
+  for (int e = tid; e < E; e += GV_THREADS) {
+    const int c = s_cnt[e];
+    for (int i = 0, r = 0; r < c; ++i, r += bn) {
+      s_tile[s_tile0[e] + i][0] = e;
+      s_tile[s_tile0[e] + i][1] = s_off[e] + r;
+      s_tile[s_tile0[e] + i][2] = min(bn, c - r);
+    }
+  }
+  for (int i = tid, r = tid * bn; r < T; i += GV_THREADS, r += GV_THREADS * bn) {
+    s_tile[ntr + i][0] = E;
+    s_tile[ntr + i][1] = A + r;
+    s_tile[ntr + i][2] = min(bn, T - r);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    // the outputs of moe_route for the same logits
+    for (int a = tid; a < A; a += GV_THREADS) {
+      p.topk_ids[a] = s_ids[a];
+      p.topk_w[a] = s_w[a];
+      p.inv_perm[a] = s_inv[a];
+      p.perm[s_inv[a]] = a;
+    }
+    for (int e = tid; e < E; e += GV_THREADS) {
+      p.counts[e] = s_cnt[e];
+      p.offsets[e] = s_off[e];
+    }
+    for (int i = tid; i < nt; i += GV_THREADS) {
+      p.block_map[3 * i] = s_tile[i][0];
+      p.block_map[3 * i + 1] = s_tile[i][1];
+      p.block_map[3 * i + 2] = s_tile[i][2];
+    }
+    if (tid == 0) {
+      p.offsets[E] = A;
+      p.num_blocks[0] = nt;
+    }
+  }
+
+  // ---------------------------------------------------------------- G, D: work items
+  const int IPT0 = F / 16, IPT1 = H / 32;
+  const int MT0 = (2 * F) / TC_M, MT1 = H / TC_M;
+  const int KT0 = H / KG, KT1 = F / KG;
+  const int nG = nt * IPT0, nD = nt * IPT1;
+  // this CTA's items: its gate/up items, then its down items
+  const int myG = blockIdx.x < nG ? ceil_div(nG - blockIdx.x, gridDim.x) : 0;
+  const int myD = blockIdx.x < nD ? ceil_div(nD - blockIdx.x, gridDim.x) : 0;
+
+  // copies of item q of this CTA (this thread's weight row) into slot buffer b; one commit group
+  auto issue = [&](int q, int b) {
+    if (q < myG + myD) {
+      const bool down = q >= myG;
+      const int u = blockIdx.x + (down ? q - myG : q) * gridDim.x;
+      const int ipt = down ? IPT1 : IPT0;
+      const int tile = u / ipt, j = u - tile * ipt;
+      int mt, L;
+      if (down) item_row<1>(j, lane, &mt, &L);
+      else item_row<0>(j, lane, &mt, &L);
+      const int KT = down ? KT1 : KT0;
+      const uint8_t* wrow = (down ? p.w2 : p.w13) +
+                            (static_cast<size_t>(s_tile[tile][0]) * (down ? MT1 : MT0) + mt) * KT *
+                                static_cast<size_t>(W_BLOCK);
+      uint4* qd = swq0 + b * slot_q + tid;
+      uint32_t* sd = swsb0 + b * slot_sb + tid;
+#pragma unroll 1
+      for (int i = 0; i < G; ++i) {
+        const int kg = warp + GV_WARPS * i;
+        if (kg >= KT) break;
+        const uint8_t* blk = wrow + static_cast<size_t>(kg) * W_BLOCK;
+        ptx::cp_async_16(ptx::smem_u32(qd + (2 * i) * GV_THREADS), blk + L * 16);
+        ptx::cp_async_16(ptx::smem_u32(qd + (2 * i + 1) * GV_THREADS), blk + 2048 + L * 16);
+        ptx::cp_async_4(ptx::smem_u32(sd + i * GV_THREADS), blk + W_PACKED + L * 4);
+      }
+    }
+    ptx::cp_async_commit();
+  };
+
+  issue(0, 0);
+  for (int q = 0; q < myG + myD; ++q) {
+    const int buf = q & 1;
+    issue(q + 1, buf ^ 1);  // the next item's weights stream during this one
+    const bool down = q >= myG;
+    const int u = blockIdx.x + (down ? q - myG : q) * gridDim.x;
+    const int ipt = down ? IPT1 : IPT0;
+    const int tile = u / ipt, j = u - tile * ipt;
+    const int row0 = s_tile[tile][1], nrow = s_tile[tile][2];
+    if (down) {
+      // every gate/up item of this tile has written its h values
+      if (tid == 0) {
+        int ok = 1;
+        if (ld_acquire(ws_tile + tile) < IPT0) {
+          const long long t0 = clock64();
+          while (ld_acquire(ws_tile + tile) < IPT0) {
+            if (static_cast<unsigned long long>(clock64() - t0) > p.wait_cycles) {
+              set_device_error(p.err, MOE_DEV_TIMEOUT);
+              ok = 0;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        s_ok = ok;
+      }
+      __syncthreads();
+      if (!s_ok) continue;
+    }
+    // activation row of each tile row (gate/up: x of the row's token; down: the row of h)
+    uint32_t xoff[GV_MAXN];
+#pragma unroll
+    for (int n = 0; n < GV_MAXN; ++n) {
+      const int r = row0 + (n < nrow ? n : 0);
+      xoff[n] = down ? static_cast<uint32_t>(r) * static_cast<uint32_t>(F)
+                     : static_cast<uint32_t>(s_tok[r]) * static_cast<uint32_t>(H);
+    }
+    float acc[GV_MAXN];
+#pragma unroll
+    for (int n = 0; n < GV_MAXN; ++n) acc[n] = 0.f;
+    ptx::cp_async_wait<1>();  // this thread's copies of item q have landed
+    const uint4* swq = swq0 + buf * slot_q + tid;
+    const uint32_t* swsb = swsb0 + buf * slot_sb + tid;
+    if (down) dec_dot<true>(nrow, swq, swsb, p.h, xoff, warp, KT1, G, acc);
+    else dec_dot<false>(nrow, swq, swsb, p.x, xoff, warp, KT0, G, acc);
+
+    // reduce the warps' partial sums (fixed order) and write the item's outputs
+    float* spart = spart0 + buf * (GV_WARPS * GV_MAXN * 32);
+#pragma unroll
+    for (int n = 0; n < GV_MAXN; ++n)
+      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + lane] = acc[n];
+    if (tid == 0) s_ngather = 0;
+    __syncthreads();
+    if (!down) {
+      if (tid < nrow * 16) {
+        const int n = tid >> 4, fi = tid & 15;
+        float gs = 0.f, us = 0.f;
+        for (int w = 0; w < GV_WARPS; ++w) {
+          gs += spart[(w * GV_MAXN + n) * 32 + fi];
+          us += spart[(w * GV_MAXN + n) * 32 + 16 + fi];
+        }
+        p.h[static_cast<size_t>(row0 + n) * F + 16 * j + fi] = float_to_bf16_bits(silu(gs) * us);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();  // this item's h values before its count
+        atomicAdd(ws_tile + tile, 1);
+      }
+    } else {
+      if (warp < nrow) {
+        float yv = 0.f;
+        for (int w = 0; w < GV_WARPS; ++w) yv += spart[(w * GV_MAXN + warp) * 32 + lane];
+        p.y[static_cast<size_t>(row0 + warp) * H + 32 * j + lane] = float_to_bf16_bits(yv);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();  // this item's y values before its counts
+        for (int n = 0; n < nrow; ++n) {
+          const int t = s_tok[row0 + n];
+          if (atomicAdd(ws_cnt + t * IPT1 + j, 1) == k) s_gather[s_ngather++] = t;
+        }
+        __threadfence();  // the other rows' y values, seen through the counts, before the gather
+      }
+      __syncthreads();
+      // combine for the tokens completed here: lane = channel 32 j + lane
+      for (int g = warp; g < s_ngather; g += GV_WARPS) {
+        const int t = s_gather[g];
+        float o = 0.f;
+        for (int jj = 0; jj < k; ++jj) {
+          const uint16_t yb = __ldcg(p.y + static_cast<size_t>(s_inv[t * k + jj]) * H + 32 * j + lane);
+          o = fmaf(s_w[t * k + jj], bf16_bits_to_float(yb), o);
+        }
+        const uint16_t ys = __ldcg(p.y + static_cast<size_t>(A + t) * H + 32 * j + lane);
+        o = fmaf(1.0f, bf16_bits_to_float(ys), o);
+        p.out[static_cast<size_t>(t) * H + 32 * j + lane] = float_to_bf16_bits(o);
+      }
+      __syncthreads();  // s_gather / s_ngather are reused by the next item
+    }
+  }
+  ptx::cp_async_wait_all();
+
+  // ---------------------------------------------------------------- the last CTA resets the counters
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(ws_done, 1) == static_cast<int>(gridDim.x) - 1;
+    if (s_last) __threadfence();
+  }
+  __syncthreads();
+  if (s_last) {
+    for (int i = tid; i < nt; i += GV_THREADS) ws_tile[i] = 0;
+    for (int i = tid; i < T * IPT1; i += GV_THREADS) ws_cnt[i] = 0;
+    if (tid == 0) *ws_done = 0;
+  }
+}
+
+int decode_max_tokens() { return DEC_MAXT; }
+
+size_t decode_workspace_bytes(int T, int H) {
+  return (static_cast<size_t>(DEC_MAXTILES) + static_cast<size_t>(T) * (H / 32) + 1) * sizeof(int);
+}
+
+static size_t decode_smem_bytes(int G, int E) {
+  return 2 * static_cast<size_t>(G) * GV_THREADS * (2 * 16 + 4) +
+         2 * static_cast<size_t>(GV_WARPS) * GV_MAXN * 32 * sizeof(float) + 3 * static_cast<size_t>(E) * sizeof(int);
+}
+
+cudaError_t launch_decode(const uint16_t* x, const float* logits, const void* w13, const void* w2, int T, int H, int F,
+                          int E, int k, int bn, int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks, uint16_t* h,
+                          uint16_t* y, uint16_t* out, void* ws, unsigned long long wait_ns, int num_sms,
+                          cudaStream_t s) {
+  if (T > DEC_MAXT || k > 32 || bn > GV_MAXN) return cudaErrorInvalidValue;
+  DecParams prm;
+  prm.x = x;
+  prm.logits = logits;
+  prm.w13 = static_cast<const uint8_t*>(w13);
+  prm.w2 = static_cast<const uint8_t*>(w2);
+  prm.topk_ids = topk_ids;
+  prm.topk_w = topk_w;
+  prm.counts = counts;
+  prm.offsets = offsets;
+  prm.perm = perm;
+  prm.inv_perm = inv_perm;
+  prm.block_map = block_map;
+  prm.num_blocks = num_blocks;
+  prm.h = h;
+  prm.y = y;
+  prm.out = out;
+  prm.ws = static_cast<int*>(ws);
+  prm.err = device_error_ptr();
+  prm.wait_cycles = wait_ns > (~0ull) / 3 ? ~0ull : wait_ns * 21 / 10;
+  prm.T = T;
+  prm.H = H;
+  prm.F = F;
+  prm.E = E;
+  prm.k = k;
+  prm.bn = bn;
+  const int g0 = (H / KG + GV_WARPS - 1) / GV_WARPS, g1 = (F / KG + GV_WARPS - 1) / GV_WARPS;
+  prm.G = g0 > g1 ? g0 : g1;
+  if (prm.G > GV_GB) return cudaErrorInvalidValue;
+  const size_t smem = decode_smem_bytes(prm.G, E);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, GV_THREADS, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidValue;
+  if (per_sm > GV_CTAS_PER_SM) per_sm = GV_CTAS_PER_SM;
+  // cooperative launch: every CTA resident at once, which the counters between them rely on
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms * per_sm);
+  cfg.blockDim = dim3(GV_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_kernel, prm);
+  note_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace moe

@@ -35,20 +35,13 @@
 // per item; the partial-sum buffer alternates between items).
 #include "moe_common.cuh"
 #include "moe_ptx.cuh"
+#include "moe_gemv_dev.cuh"
 
 namespace moe {
 
-namespace {
+using namespace gemv_dev;
 
-constexpr int GV_THREADS = 256;
-constexpr int GV_WARPS = GV_THREADS / 32;
-constexpr int GV_MAXN = 8;  // token rows per tile
-constexpr int GV_GB = 8;    // K groups per thread at most (K <= 64 * 8 * 8 = 4096)
-constexpr int GV_CTAS_PER_SM = 2;
-constexpr int KG = 64;
-constexpr int TC_M = 128;
-constexpr int W_PACKED = TC_M * 32;
-constexpr int W_BLOCK = W_PACKED + TC_M * 4;
+namespace {
 
 struct GvParams {
   const uint16_t* act;
@@ -62,50 +55,6 @@ struct GvParams {
   int T, H, F, E, k, bn, cap;
   int G;  // K groups per thread: ceil(K / 64 / 8)
 };
-
-// bf16 pair of weights (element 2j in the low half, 2j+1 in the high half) of
-// a repacked word: 128 + q exactly, minus 128, times scale plus bias, rounded once.
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t word, int j, uint32_t s2, uint32_t b2) {
-  constexpr uint32_t MAGIC = 0x43004300u;
-  uint32_t x = ((word >> (4 * j)) & 0x000f000fu) | MAGIC, r;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(MAGIC));
-  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(r), "r"(s2), "r"(b2));
-  return r;
-}
-
-// acc += w.lo * x.lo + w.hi * x.hi (bf16 operands, FP32 accumulation, products exact)
-__device__ __forceinline__ void dot_pair(float& acc, uint32_t w2, uint32_t x2) {
-  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\tfma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(w2), "r"(x2));
-}
-
-// acc[n] += sum over one K group of w * x[n] for token rows n = N0 .. N0+NT-1:
-// the row's packed words (lo: K 0..31, hi: K 32..63 of the group), its
-// (scale, bias) and the group's activations of each row at xg + xoff[n]
-// (bf16, global, read via L1).
-template <int N0, int NT>
-__device__ __forceinline__ void group_dot(uint4 lo, uint4 hi, uint32_t sb, const uint16_t* xg,
-                                          const uint32_t (&xoff)[GV_MAXN], float (&acc)[GV_MAXN]) {
-  const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
-  const uint32_t b2 = (sb >> 16) * 0x10001u;
-  const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    uint32_t wp[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) wp[j] = dequant_pair(words[w], j, s2, b2);
-#pragma unroll
-    for (int n = N0; n < N0 + NT; ++n) {
-      const uint4 x = __ldg(reinterpret_cast<const uint4*>(xg + xoff[n]) + w);
-      dot_pair(acc[n], wp[0], x.x);
-      dot_pair(acc[n], wp[1], x.y);
-      dot_pair(acc[n], wp[2], x.z);
-      dot_pair(acc[n], wp[3], x.w);
-    }
-  }
-}
 
 // All of this thread's groups of one item from its slots (slot i of the
 // buffer: words at swq[2i], swq[2i+1], (scale, bias) at swsb[i]; one thread's
@@ -132,20 +81,6 @@ __device__ __forceinline__ bool gv_tile(const GvParams& p, int b, Tile* t) {
             t->row0 >= 0;
   if (ok) ok = t->expert < p.E ? (t->row0 + t->rows <= A) : (t->row0 >= A && t->row0 + t->rows <= A + p.T);
   return ok;
-}
-
-// Weight row of item j of a tile for this lane: (M-tile, row within it).
-template <int MODE>
-__device__ __forceinline__ void item_row(int j, int lane, int* mt, int* L) {
-  if (MODE == 0) {
-    const int f = 16 * j + (lane & 15);
-    *mt = 2 * (f / TC_M) + (lane >> 4);  // gate M-tile, or the up M-tile after it
-    *L = f % TC_M;
-  } else {
-    const int c = 32 * j + lane;
-    *mt = c / TC_M;
-    *L = c % TC_M;
-  }
 }
 
 }  // namespace

@@ -622,6 +622,8 @@ static unsigned long long g_wait_ns = 1000000000ull;
 
 void set_wait_limit_ns(unsigned long long ns) { g_wait_ns = ns; }
 
+unsigned long long wait_limit_ns() { return g_wait_ns; }
+
 namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

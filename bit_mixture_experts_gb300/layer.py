@@ -112,9 +112,13 @@ class MoELayerW4:
             "y": torch.empty((A + T, H), dtype=torch.bfloat16, device=dev),
             "workspace": torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev),
         }
+        # counters of the fused decode kernel (used for T <= 8 with the GEMV kernel): zero once, left zero
+        dws = _lib.moe_decode_workspace_size(T, H)
+        t["decode_ws"] = torch.zeros(max(dws, 16), dtype=torch.uint8, device=dev) if dws else None
         t["struct"] = _lib.Buffers(*(t[n].data_ptr() for n in ("topk_ids", "topk_w", "counts", "offsets", "perm",
                                                                  "inv_perm", "block_map", "num_blocks", "h", "y",
-                                                                 "workspace")), wsb)
+                                                                 "workspace")), wsb,
+                                   t["decode_ws"].data_ptr() if dws else None, dws)
         self._bufs[T] = t
         return t
 

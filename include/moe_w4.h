@@ -239,7 +239,18 @@ typedef struct {
   uint16_t* y;         /* bf16 [A+T, H] */
   void* workspace;     /* moe_route_workspace_size bytes */
   size_t workspace_bytes;
+  void* decode_ws;      /* fused decode path: moe_decode_workspace_size bytes, zero before the
+                           first call (every call leaves it zero); NULL: never fuse */
+  size_t decode_ws_bytes;
 } moe_buffers_t;
+
+/*
+ * moe_decode_workspace_size -- bytes of the fused decode path's counters for
+ * T tokens and hidden size H (0 when T is above the fused path's limit of 8
+ * tokens).  The workspace must be zero-filled once by the caller; each call
+ * of the fused path returns it to zero.
+ */
+size_t moe_decode_workspace_size(int T, int H);
 
 /* Weights of one layer: gate/up and down matrices of E+1 experts. */
 typedef struct {
@@ -255,6 +266,14 @@ typedef struct {
  * moe_layer_forward -- the whole hot path on one stream with no host sync:
  * moe_route, gate/up GEMM, down GEMM, moe_combine.  x bf16 [T,H], logits
  * float32 [T,E], out bf16 [T,H] are device pointers.
+ *
+ * Decode: when the GEMV kernel is chosen (impl MOE_IMPL_GEMV, or AUTO with
+ * block_n <= 8), T <= 8, k <= 32 and buffers->decode_ws is set, the four steps
+ * run as one fused kernel (cooperative launch; every CTA recomputes the
+ * routing, then the gate/up and down work items hand over through counters
+ * in decode_ws).  Its results are those of the four calls: the same routing
+ * outputs, h, y and out.  Returns MOE_ERR_WORKSPACE when decode_ws_bytes is
+ * below moe_decode_workspace_size(T, H).
  */
 int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out,
                       int T, int H, int F, int E, int k, int block_n, int impl,

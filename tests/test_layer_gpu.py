@@ -136,3 +136,62 @@ def test_gate_up_intermediate(impl):
     lo, hi = moe_ref.bf16_floor_ceil(exact)
     assert np.all(np.abs(got - exact) <= np.maximum(hi - lo, G.H_ABS_BAND)), f"h {impl}"
     assert (got != want).mean() <= G.H_FLIP_FRAC, f"h {impl}: too many roundings away from nearest"
+
+
+DECODE = [
+    (1, 256, 16, 2, 128, False),
+    (5, 256, 16, 4, 128, False),
+    (8, 128, 64, 8, 128, False),     # 64 assignments over 64 experts
+    (8, 256, 16, 2, 256, True),      # skewed logits, F = 256
+    (3, 128, 8, 8, 128, False),      # k = E: every expert in every token
+    (8, 128, 32, 32, 128, False),    # k = 32: the largest assignment count of the fused path (256)
+]
+
+
+@pytest.mark.parametrize("spec", DECODE, ids=lambda s: "T{}_H{}_E{}_k{}_F{}{}".format(*s[:5], "_skew" if s[5] else ""))
+def test_decode_fused(spec):
+    """The fused decode kernel (T <= 8 with the GEMV kernel): every output against the oracle,
+    and the routing it writes equal to moe_route's (bit-exact ids, counts, offsets,
+    permutations, block map)."""
+    d = G.workload(spec)
+    T, H, E, k, F, _ = spec
+    (got,), layer = run_layer(d, "gemv")
+    G.check_layer(d, layer, got, what=f"fused decode {spec}")
+    b = layer.buffers(T)
+    assert b["decode_ws"] is not None
+    ref = moe_ref.route(d["logits"], k, layer.block_n_for(T))
+    assert np.array_equal(b["topk_ids"].cpu().numpy(), ref["topk_ids"])
+    assert np.allclose(b["topk_w"].cpu().numpy(), ref["topk_w"], rtol=1e-6, atol=float(np.finfo(np.float32).tiny))
+    for n in ("counts", "offsets", "perm", "inv_perm"):
+        assert np.array_equal(b[n].cpu().numpy(), ref[n]), n
+    nb = int(b["num_blocks"].item())
+    assert nb == ref["num_blocks"]
+    assert np.array_equal(b["block_map"].cpu().numpy()[:nb], ref["block_map"])
+
+
+def test_decode_fused_repeatable():
+    """Repeated fused calls (the kernel returns its counters to zero) give bit-identical outputs,
+    equal to those of the four separate kernels."""
+    import torch
+    from bit_mixture_experts_gb300 import _lib
+    d = G.workload((8, 256, 16, 4, 128, False))
+    outs, layer = run_layer(d, "gemv", reps=3)
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    assert int(layer.buffers(8)["decode_ws"].count_nonzero().item()) == 0
+    # the unfused path: route, gate/up, down and combine launched one by one
+    x, logits = G.to_dev_inputs(d)
+    T, H, E, k, F = 8, 256, 16, 4, 128
+    b = layer.buffers(T)
+    w = layer.weights
+    bn = layer.block_n_for(T)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _lib.moe_route(logits, k, bn, b["topk_ids"], b["topk_w"], b["counts"], b["offsets"], b["perm"],
+                   b["inv_perm"], b["block_map"], b["num_blocks"], b["workspace"])
+    _lib.moe_expert_gemm_w4(_lib.GATE_UP, _lib.IMPL_GEMV, x, T, H, F, E, k, w.w13, None, None, b["perm"],
+                            b["topk_w"], b["block_map"], b["num_blocks"], bn, b["h"])
+    _lib.moe_expert_gemm_w4(_lib.DOWN, _lib.IMPL_GEMV, b["h"], T, H, F, E, k, w.w2, None, None, b["perm"],
+                            b["topk_w"], b["block_map"], b["num_blocks"], bn, b["y"])
+    _lib.moe_combine(b["y"], b["inv_perm"], b["topk_w"], out)
+    torch.cuda.synchronize()
+    assert _lib.moe_get_device_error() == 0
+    assert np.array_equal(G.bf16_to_f64(out), outs[0])
