@@ -15,21 +15,21 @@
 //   R  routing, recomputed by every CTA in shared memory from the logits with
 //      the same device code as moe_route (top-k and weights, counts, offsets,
 //      stable permutation, block map); CTA 0 also writes moe_route's outputs.
-//   G  gate/up work items (tile, 16 features), exactly as the GEMV kernel;
-//      after writing its h values an item adds 1 to its tile's counter.
-//   D  down work items (tile, 32 channels): the item's weights are copied in
-//      before it waits (bounded) until every gate/up item of its tile has
-//      finished; h is then read through L2 only.  After writing its y values
-//      it adds 1 to a counter per (token, 32 channels) for each of its rows;
-//      the item that brings a counter to k + 1 (all routed rows and the
-//      shared row of that token) gathers the combine for those 32 channels:
+//   G  gate/up work items (tile, 16 features), exactly as the GEMV kernel
+//      (the first down item's weights are already streaming during the last).
+//   -  grid barrier: every h value is written.
+//   D  down work items (tile, 32 channels); h is read through L2 only.
+//   -  grid barrier: every y value is written.
+//   C  the gather-combine, one warp per (token, 32 channels):
 //      out = bf16(sum_j topk_w[t, j] * y[row(t, j)] + y[shared row]), FP32 in
 //      the same fixed order as moe_combine.
-//   The last CTA to finish resets every counter to zero for the next call.
-// Items are dealt round-robin; each CTA finishes all of its gate/up items
-// before any down item, and only down items wait, so with every CTA resident
-// the waits always end.  Each wait is bounded nonetheless; on expiry it
-// records MOE_DEV_TIMEOUT and skips the item.
+//   The last CTA to finish resets the barrier counters for the next call.
+// The grid barriers are counters in global memory (one fence and one atomic
+// per CTA); they rely on every CTA being resident, which the cooperative
+// launch guarantees.  Each wait is bounded nonetheless; on expiry it records
+// MOE_DEV_TIMEOUT and goes on.  (A first version signalled per work item --
+// a counter per tile for h, per token and 32 channels for y -- and spent
+// most of its time in the fences those signals need.)
 #include "moe_common.cuh"
 #include "moe_gemv_dev.cuh"
 #include "moe_ptx.cuh"
@@ -61,7 +61,7 @@ struct DecParams {
   uint16_t* h;
   uint16_t* y;
   uint16_t* out;
-  int* ws;  // [DEC_MAXTILES] gate/up items done per tile | [T][H/32] combine contributions | [1] CTAs done
+  int* ws;  // grid barrier counters: [0] h written, [1] y written, [2] CTAs done
   int* err;
   unsigned long long wait_cycles;
   int T, H, F, E, k, bn;
@@ -78,7 +78,7 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 template <int N0, int NT, bool COHERENT>
 __device__ __forceinline__ void dec_item_dot(const uint4* swq, const uint32_t* swsb, const uint16_t* act,
                                              const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
-                                             float (&acc)[GV_MAXN]) {
+                                             float (&acc)[GV_MAXN][GV_NACC]) {
 #pragma unroll 1
   for (int i = 0; i < G; ++i) {
     const int kg = warp + GV_WARPS * i;
@@ -91,7 +91,7 @@ __device__ __forceinline__ void dec_item_dot(const uint4* swq, const uint32_t* s
 template <bool COHERENT>
 __device__ __forceinline__ void dec_dot(int nrow, const uint4* swq, const uint32_t* swsb, const uint16_t* act,
                                         const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
-                                        float (&acc)[GV_MAXN]) {
+                                        float (&acc)[GV_MAXN][GV_NACC]) {
   if (nrow == 1) {
     dec_item_dot<0, 1, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
   } else if (nrow == 2) {
@@ -111,8 +111,7 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
   __shared__ int s_tok[DEC_MAXA + DEC_MAXT];     // permuted row -> token
   __shared__ int s_tile[DEC_MAXTILES][3];        // (expert, first row, rows)
   __shared__ uint64_t s_scan[33];
-  __shared__ int s_gather[GV_MAXN];              // tokens whose 32 channels this item completes
-  __shared__ int s_ngather, s_ok, s_last;
+  __shared__ int s_ok;
   extern __shared__ uint4 dec_smem[];
   const int T = p.T, E = p.E, k = p.k, bn = p.bn, H = p.H, F = p.F;
   const int A = T * k;
@@ -126,9 +125,7 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
   int* s_cnt = reinterpret_cast<int*>(spart0 + 2 * GV_WARPS * GV_MAXN * 32);  // [E]
   int* s_off = s_cnt + E;                                                     // [E]
   int* s_tile0 = s_off + E;                                                   // [E]
-  int* ws_tile = p.ws;
-  int* ws_cnt = p.ws + DEC_MAXTILES;
-  int* ws_done = ws_cnt + T * (H / 32);
+  int* ws_bar = p.ws;  // [0] h written, [1] y written, [2] CTAs done
 
   // ---------------------------------------------------------------- R: routing
   if (warp < T) {
@@ -251,35 +248,34 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
     ptx::cp_async_commit();
   };
 
+  // every CTA has passed the barrier once all have arrived; bounded, records a timeout
+  auto grid_barrier = [&](int* bar) {
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();  // this CTA's h / y values before its arrival
+      atomicAdd(bar, 1);
+      const long long t0 = clock64();
+      while (ld_acquire(bar) < static_cast<int>(gridDim.x)) {
+        if (static_cast<unsigned long long>(clock64() - t0) > p.wait_cycles) {
+          set_device_error(p.err, MOE_DEV_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __syncthreads();
+  };
+
   issue(0, 0);
   for (int q = 0; q < myG + myD; ++q) {
     const int buf = q & 1;
+    if (q == myG) grid_barrier(ws_bar);  // all of h is written before any down item reads it
     issue(q + 1, buf ^ 1);  // the next item's weights stream during this one
     const bool down = q >= myG;
     const int u = blockIdx.x + (down ? q - myG : q) * gridDim.x;
     const int ipt = down ? IPT1 : IPT0;
     const int tile = u / ipt, j = u - tile * ipt;
     const int row0 = s_tile[tile][1], nrow = s_tile[tile][2];
-    if (down) {
-      // every gate/up item of this tile has written its h values
-      if (tid == 0) {
-        int ok = 1;
-        if (ld_acquire(ws_tile + tile) < IPT0) {
-          const long long t0 = clock64();
-          while (ld_acquire(ws_tile + tile) < IPT0) {
-            if (static_cast<unsigned long long>(clock64() - t0) > p.wait_cycles) {
-              set_device_error(p.err, MOE_DEV_TIMEOUT);
-              ok = 0;
-              break;
-            }
-            __nanosleep(128);
-          }
-        }
-        s_ok = ok;
-      }
-      __syncthreads();
-      if (!s_ok) continue;
-    }
     // activation row of each tile row (gate/up: x of the row's token; down: the row of h)
     uint32_t xoff[GV_MAXN];
 #pragma unroll
@@ -288,9 +284,11 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
       xoff[n] = down ? static_cast<uint32_t>(r) * static_cast<uint32_t>(F)
                      : static_cast<uint32_t>(s_tok[r]) * static_cast<uint32_t>(H);
     }
-    float acc[GV_MAXN];
+    float acc[GV_MAXN][GV_NACC];
 #pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n) acc[n] = 0.f;
+    for (int n = 0; n < GV_MAXN; ++n)
+#pragma unroll
+      for (int c = 0; c < GV_NACC; ++c) acc[n][c] = 0.f;
     ptx::cp_async_wait<1>();  // this thread's copies of item q have landed
     const uint4* swq = swq0 + buf * slot_q + tid;
     const uint32_t* swsb = swsb0 + buf * slot_sb + tid;
@@ -301,8 +299,7 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
     float* spart = spart0 + buf * (GV_WARPS * GV_MAXN * 32);
 #pragma unroll
     for (int n = 0; n < GV_MAXN; ++n)
-      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + lane] = acc[n];
-    if (tid == 0) s_ngather = 0;
+      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + lane] = acc_total(acc[n]);
     __syncthreads();
     if (!down) {
       if (tid < nrow * 16) {
@@ -314,64 +311,43 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
         }
         p.h[static_cast<size_t>(row0 + n) * F + 16 * j + fi] = float_to_bf16_bits(silu(gs) * us);
       }
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();  // this item's h values before its count
-        atomicAdd(ws_tile + tile, 1);
-      }
-    } else {
-      if (warp < nrow) {
-        float yv = 0.f;
-        for (int w = 0; w < GV_WARPS; ++w) yv += spart[(w * GV_MAXN + warp) * 32 + lane];
-        p.y[static_cast<size_t>(row0 + warp) * H + 32 * j + lane] = float_to_bf16_bits(yv);
-      }
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();  // this item's y values before its counts
-        for (int n = 0; n < nrow; ++n) {
-          const int t = s_tok[row0 + n];
-          if (atomicAdd(ws_cnt + t * IPT1 + j, 1) == k) s_gather[s_ngather++] = t;
-        }
-        __threadfence();  // the other rows' y values, seen through the counts, before the gather
-      }
-      __syncthreads();
-      // combine for the tokens completed here: lane = channel 32 j + lane
-      for (int g = warp; g < s_ngather; g += GV_WARPS) {
-        const int t = s_gather[g];
-        float o = 0.f;
-        for (int jj = 0; jj < k; ++jj) {
-          const uint16_t yb = __ldcg(p.y + static_cast<size_t>(s_inv[t * k + jj]) * H + 32 * j + lane);
-          o = fmaf(s_w[t * k + jj], bf16_bits_to_float(yb), o);
-        }
-        const uint16_t ys = __ldcg(p.y + static_cast<size_t>(A + t) * H + 32 * j + lane);
-        o = fmaf(1.0f, bf16_bits_to_float(ys), o);
-        p.out[static_cast<size_t>(t) * H + 32 * j + lane] = float_to_bf16_bits(o);
-      }
-      __syncthreads();  // s_gather / s_ngather are reused by the next item
+    } else if (warp < nrow) {
+      float yv = 0.f;
+      for (int w = 0; w < GV_WARPS; ++w) yv += spart[(w * GV_MAXN + warp) * 32 + lane];
+      p.y[static_cast<size_t>(row0 + warp) * H + 32 * j + lane] = float_to_bf16_bits(yv);
     }
   }
+  if (myD == 0) grid_barrier(ws_bar);  // CTAs without down items still take part in the first barrier
   ptx::cp_async_wait_all();
+  grid_barrier(ws_bar + 1);  // all of y is written
+
+  // ---------------------------------------------------------------- C: combine, one warp per (token, 32 channels)
+  for (int c = blockIdx.x * GV_WARPS + warp; c < T * IPT1; c += gridDim.x * GV_WARPS) {
+    const int t = c / IPT1, jb = c - t * IPT1;
+    float o = 0.f;
+    for (int jj = 0; jj < k; ++jj) {
+      const uint16_t yb = __ldcg(p.y + static_cast<size_t>(s_inv[t * k + jj]) * H + 32 * jb + lane);
+      o = fmaf(s_w[t * k + jj], bf16_bits_to_float(yb), o);
+    }
+    const uint16_t ys = __ldcg(p.y + static_cast<size_t>(A + t) * H + 32 * jb + lane);
+    o = fmaf(1.0f, bf16_bits_to_float(ys), o);
+    p.out[static_cast<size_t>(t) * H + 32 * jb + lane] = float_to_bf16_bits(o);
+  }
 
   // ---------------------------------------------------------------- the last CTA resets the counters
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(ws_done, 1) == static_cast<int>(gridDim.x) - 1;
-    if (s_last) __threadfence();
-  }
-  __syncthreads();
-  if (s_last) {
-    for (int i = tid; i < nt; i += GV_THREADS) ws_tile[i] = 0;
-    for (int i = tid; i < T * IPT1; i += GV_THREADS) ws_cnt[i] = 0;
-    if (tid == 0) *ws_done = 0;
+    if (atomicAdd(ws_bar + 2, 1) == static_cast<int>(gridDim.x) - 1) {
+      ws_bar[0] = 0;
+      ws_bar[1] = 0;
+      ws_bar[2] = 0;
+    }
   }
 }
 
 int decode_max_tokens() { return DEC_MAXT; }
 
-size_t decode_workspace_bytes(int T, int H) {
-  return (static_cast<size_t>(DEC_MAXTILES) + static_cast<size_t>(T) * (H / 32) + 1) * sizeof(int);
-}
+size_t decode_workspace_bytes(int, int) { return 4 * sizeof(int); }
 
 static size_t decode_smem_bytes(int G, int E) {
   return 2 * static_cast<size_t>(G) * GV_THREADS * (2 * 16 + 4) +

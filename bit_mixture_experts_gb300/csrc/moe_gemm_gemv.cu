@@ -62,7 +62,7 @@ struct GvParams {
 template <int N0, int NT>
 __device__ __forceinline__ void item_dot(const uint4* swq, const uint32_t* swsb, const uint16_t* act,
                                          const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
-                                         float (&acc)[GV_MAXN]) {
+                                         float (&acc)[GV_MAXN][GV_NACC]) {
 #pragma unroll 1
   for (int i = 0; i < G; ++i) {
     const int kg = warp + GV_WARPS * i;
@@ -168,9 +168,11 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) gemv_kernel(const 
       xoff[n] = MODE == 0 ? static_cast<uint32_t>(tk < 0 ? 0 : tk) * static_cast<uint32_t>(K)
                           : static_cast<uint32_t>(t.row0 + (n < nrow ? n : 0)) * static_cast<uint32_t>(K);
     }
-    float acc[GV_MAXN];
+    float acc[GV_MAXN][GV_NACC];
 #pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n) acc[n] = 0.f;
+    for (int n = 0; n < GV_MAXN; ++n)
+#pragma unroll
+      for (int c = 0; c < GV_NACC; ++c) acc[n][c] = 0.f;
     ptx::cp_async_wait<1>();  // this thread's copies of item u have landed
     const uint4* swq = swq0 + buf * slot_q + threadIdx.x;
     const uint32_t* swsb = swsb0 + buf * slot_sb + threadIdx.x;
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) gemv_kernel(const 
     float* spart = spart0 + buf * (GV_WARPS * GV_MAXN * 32);
 #pragma unroll
     for (int n = 0; n < GV_MAXN; ++n)
-      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + lane] = acc[n];
+      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + lane] = acc_total(acc[n]);
     __syncthreads();
     if (MODE == 0) {
       if (threadIdx.x < nrow * 16) {

@@ -34,6 +34,13 @@ __device__ __forceinline__ void dot_pair(float& acc, uint32_t w2, uint32_t x2) {
       : "r"(w2), "r"(x2));
 }
 
+// Partial sums per token row: four independent chains (one per pair slot of a
+// word), so the FMAs of a row do not form one long dependent chain; they are
+// added in a fixed order at the end (acc_total).
+constexpr int GV_NACC = 4;
+
+__device__ __forceinline__ float acc_total(const float (&a)[GV_NACC]) { return (a[0] + a[1]) + (a[2] + a[3]); }
+
 // acc[n] += sum over one K group of w * x[n] for token rows n = N0 .. N0+NT-1:
 // the row's packed words (lo: K 0..31, hi: K 32..63 of the group), its
 // (scale, bias) and the group's activations of each row at xg + xoff[n]
@@ -41,7 +48,7 @@ __device__ __forceinline__ void dot_pair(float& acc, uint32_t w2, uint32_t x2) {
 // activations written earlier by the same kernel).
 template <int N0, int NT, bool COHERENT = false>
 __device__ __forceinline__ void group_dot(uint4 lo, uint4 hi, uint32_t sb, const uint16_t* xg,
-                                          const uint32_t (&xoff)[GV_MAXN], float (&acc)[GV_MAXN]) {
+                                          const uint32_t (&xoff)[GV_MAXN], float (&acc)[GV_MAXN][GV_NACC]) {
   const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
   const uint32_t b2 = (sb >> 16) * 0x10001u;
   const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
@@ -54,10 +61,10 @@ __device__ __forceinline__ void group_dot(uint4 lo, uint4 hi, uint32_t sb, const
     for (int n = N0; n < N0 + NT; ++n) {
       const uint4* xp = reinterpret_cast<const uint4*>(xg + xoff[n]) + w;
       const uint4 x = COHERENT ? __ldcg(xp) : __ldg(xp);
-      dot_pair(acc[n], wp[0], x.x);
-      dot_pair(acc[n], wp[1], x.y);
-      dot_pair(acc[n], wp[2], x.z);
-      dot_pair(acc[n], wp[3], x.w);
+      dot_pair(acc[n][0], wp[0], x.x);
+      dot_pair(acc[n][1], wp[1], x.y);
+      dot_pair(acc[n][2], wp[2], x.z);
+      dot_pair(acc[n][3], wp[3], x.w);
     }
   }
 }
