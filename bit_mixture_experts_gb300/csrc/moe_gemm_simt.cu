@@ -179,14 +179,14 @@ cudaError_t launch_gemm_simt(int mode, const uint16_t* act, int T, int H, int F,
 // combine: out[t] = bf16(sum_j topk_w[t, j] y[inv_perm[t k + j]] + y[A + t])
 // One thread per 8 channels of a token (16-byte loads of each y row), the
 // FP32 sum in the fixed order j = 0 .. k-1, then the shared row.  Rows are
-// taken 8 at a time with all their index and row loads issued before the
-// sums, so the latency of the gather is paid once per 8 rows.
+// taken 16 at a time (k + 1 <= 16 in one batch) with all their index and row
+// loads issued before the sums, so the latency of the gather is paid once.
 // --------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y,
                                                       const int32_t* __restrict__ inv_perm,
                                                       const float* __restrict__ topk_w, uint16_t* __restrict__ out,
                                                       int T, int H, int k, int* err) {
-  constexpr int RB = 8;  // rows per batch
+  constexpr int RB = 16;  // rows per batch
   const int c8 = H / 8;  // 8-channel chunks per row
   const int A = T * k;
   const size_t n = static_cast<size_t>(T) * c8;

@@ -11,9 +11,9 @@
 //
 // Kernels:
 //   route_small_kernel   one CTA does everything (T*k <= 1024; decode)
-//   route_topk_kernel    warp-per-token top-k + per-chunk expert counts
-//   route_scan_kernel    one CTA: counts, offsets, per-chunk bases, block map
-//   route_scatter_kernel per chunk: stable ranks with warp match, no atomics
+//   route_fused_kernel   one CTA per chunk of tokens, one cooperative launch:
+//                        top-k and chunk counts | grid barrier | totals, scan,
+//                        block map | stable scatter (ranks with warp match)
 #include "moe_common.cuh"
 #include "moe_route_dev.cuh"
 
@@ -95,16 +95,43 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
 }
 
 // --------------------------------------------------------------------------
-// Multi-CTA routing.
+// Multi-CTA routing: one cooperative launch of nch CTAs, chunk c = tokens
+// [c*tc, (c+1)*tc), 256 threads.
+//   1. top-k of the chunk's tokens (one warp per token) and the chunk's
+//      per-expert counts cc[c][e] (chunk-major, in the workspace);
+//   -  grid barrier (a counter in the workspace; every CTA is resident);
+//   2. every CTA sums the counts of all chunks per expert (L2 reads), scans
+//      them over the experts (offsets and the first tile of each expert) and
+//      takes its own chunk's start in each expert's run; CTA 0 also writes
+//      counts, offsets, the block map and its length;
+//   3. the stable rank of each of the chunk's assignments among the chunk's
+//      assignments of the same expert, without atomics: __match_any_sync
+//      groups equal experts within a warp, each group's leader publishes its
+//      size per (warp, expert), and a thread adds the sizes of earlier warps.
+//   The last CTA to finish returns the counters to zero for the next call.
 // --------------------------------------------------------------------------
-// Kernel 1: chunk c = tokens [c*tc, (c+1)*tc); one warp per token; per-chunk
-// expert counts go to cc[c][e] (chunk-major).
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E,
-                                                         int k, int tc, int32_t* __restrict__ topk_ids,
-                                                         float* __restrict__ topk_w, int32_t* __restrict__ cc) {
-  extern __shared__ int s_hist[];  // [E]
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(256) route_fused_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                          int tc, int bn, int32_t* topk_ids, float* topk_w,
+                                                          int32_t* cc, int* ctr, int32_t* counts, int32_t* offsets,
+                                                          int32_t* perm, int32_t* inv_perm, int32_t* block_map,
+                                                          int32_t* num_blocks, int* err,
+                                                          unsigned long long wait_cycles) {
+  extern __shared__ int smem_i[];
+  int* s_hist = smem_i;        // [E] chunk counts, then the chunk's next free row per expert
+  int* s_wc = smem_i + E;      // [8][E] per-warp group sizes
+  int* s_tot = s_wc + 8 * E;   // [E] totals over all chunks
+  __shared__ uint64_t s_scan[33];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c = blockIdx.x;
+  const int c = blockIdx.x, nch = gridDim.x;
+  const int A = T * k;
+
+  // ---- 1: top-k and the chunk's counts
   for (int i = threadIdx.x; i < E; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
   const int t0 = c * tc, t1 = min(T, t0 + tc);
@@ -120,115 +147,88 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x) cc[static_cast<size_t>(c) * E + i] = s_hist[i];
-}
 
-// Kernel 2 (one CTA, 1024 threads): per-expert totals over chunks, exclusive
-// scan over experts, the absolute start of every (chunk, expert) run written
-// back into cc, and the block map.
-__global__ void __launch_bounds__(1024) route_scan_kernel(int T, int E, int k, int bn, int nch,
-                                                          int32_t* __restrict__ cc, int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ offsets,
-                                                          int32_t* __restrict__ block_map,
-                                                          int32_t* __restrict__ num_blocks) {
-  __shared__ int s_part[1024];
-  __shared__ int s_off[1024];
-  __shared__ uint64_t s_scan[33];
-  int er = 1;
-  while (er < E) er <<= 1;
-  const int parts = 1024 / er;
-  const int e = threadIdx.x % er, part = threadIdx.x / er;
-  const int cpp = ceil_div(nch, parts);
-  const int c0 = min(nch, part * cpp), c1 = min(nch, c0 + cpp);
-  int sum = 0;
-  if (e < E) {
-    int c = c0;
-    for (; c + 16 <= c1; c += 16) {  // 16 independent loads in flight
-      int v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = cc[static_cast<size_t>(c + i) * E + e];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) sum += v[i];
-    }
-    for (; c < c1; ++c) sum += cc[static_cast<size_t>(c) * E + e];
-  }
-  s_part[threadIdx.x] = sum;
+  // ---- grid barrier: every chunk's counts are written
   __syncthreads();
-  uint64_t mine = 0;
-  int cnt = 0;
-  if (threadIdx.x < E) {
-    for (int p = 0; p < parts; ++p) {
-      int v = s_part[p * er + threadIdx.x];
-      s_part[p * er + threadIdx.x] = cnt;
-      cnt += v;
-    }
-    mine = (static_cast<uint64_t>(cnt) << 32) | static_cast<uint32_t>(ceil_div(cnt, bn));
-  }
-  __syncthreads();
-  uint64_t total;
-  uint64_t ex = block_exclusive_scan(mine, s_scan, &total);
-  const int A = T * k;
-  const int ntiles = static_cast<int>(total & 0xffffffffu);
-  if (threadIdx.x < E) {
-    const int off = static_cast<int>(ex >> 32), tile0 = static_cast<int>(ex & 0xffffffffu);
-    counts[threadIdx.x] = cnt;
-    offsets[threadIdx.x] = off;
-    s_off[threadIdx.x] = off;
-    emit_expert_tiles(block_map, tile0, threadIdx.x, off, cnt, bn);
-  }
   if (threadIdx.x == 0) {
-    offsets[E] = A;
-    num_blocks[0] = ntiles + ceil_div(T, bn);
-  }
-  for (int i = threadIdx.x, r = threadIdx.x * bn; r < T; i += blockDim.x, r += blockDim.x * bn) {
-    int32_t* p = block_map + 3 * (ntiles + i);
-    p[0] = E;
-    p[1] = A + r;
-    p[2] = min(bn, T - r);
+    __threadfence();
+    atomicAdd(ctr, 1);
+    const long long w0 = clock64();
+    while (ld_acquire_gpu(ctr) < nch) {
+      if (static_cast<unsigned long long>(clock64() - w0) > wait_cycles) {
+        set_device_error(err, MOE_DEV_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
   }
   __syncthreads();
-  if (e < E) {
-    int run = s_off[e] + s_part[part * er + e];
-    int c = c0;
-    for (; c + 16 <= c1; c += 16) {
+
+  // ---- 2: totals, this chunk's start per expert, offsets and the block map
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int tot = 0, before = 0;
+    int cq = 0;
+    for (; cq + 16 <= nch; cq += 16) {  // 16 independent loads in flight
       int v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = cc[static_cast<size_t>(c + i) * E + e];
+      for (int i = 0; i < 16; ++i) v[i] = __ldcg(cc + static_cast<size_t>(cq + i) * E + e);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        cc[static_cast<size_t>(c + i) * E + e] = run;
-        run += v[i];
+        tot += v[i];
+        before += cq + i < c ? v[i] : 0;
       }
     }
-    for (; c < c1; ++c) {
-      int32_t* p = cc + static_cast<size_t>(c) * E + e;
-      int v = *p;
-      *p = run;
-      run += v;
+    for (; cq < nch; ++cq) {
+      const int v = __ldcg(cc + static_cast<size_t>(cq) * E + e);
+      tot += v;
+      before += cq < c ? v : 0;
+    }
+    s_tot[e] = tot;
+    s_hist[e] = before;
+  }
+  __syncthreads();
+  {
+    const int per = ceil_div(E, static_cast<int>(blockDim.x));
+    const int e0 = min(E, static_cast<int>(threadIdx.x) * per), e1 = min(E, e0 + per);
+    uint64_t loc = 0;
+    for (int e = e0; e < e1; ++e)
+      loc += (static_cast<uint64_t>(s_tot[e]) << 32) | static_cast<uint32_t>(ceil_div(s_tot[e], bn));
+    uint64_t total;
+    uint64_t run = block_exclusive_scan(loc, s_scan, &total);
+    const int ntiles = static_cast<int>(total & 0xffffffffu);
+    for (int e = e0; e < e1; ++e) {
+      const int cnt = s_tot[e];
+      const int off = static_cast<int>(run >> 32), tile0 = static_cast<int>(run & 0xffffffffu);
+      s_hist[e] += off;
+      if (c == 0) {
+        counts[e] = cnt;
+        offsets[e] = off;
+        emit_expert_tiles(block_map, tile0, e, off, cnt, bn);
+      }
+      run += (static_cast<uint64_t>(cnt) << 32) | static_cast<uint32_t>(ceil_div(cnt, bn));
+    }
+    if (c == 0) {
+      if (threadIdx.x == 0) {
+        offsets[E] = A;
+        num_blocks[0] = ntiles + ceil_div(T, bn);
+      }
+      for (int i = threadIdx.x, r = threadIdx.x * bn; r < T; i += blockDim.x, r += blockDim.x * bn) {
+        int32_t* p = block_map + 3 * (ntiles + i);
+        p[0] = E;
+        p[1] = A + r;
+        p[2] = min(bn, T - r);
+      }
     }
   }
-}
+  __syncthreads();
 
-// Kernel 3: per chunk, the stable rank of each assignment among the chunk's
-// assignments of the same expert, computed without atomics: __match_any_sync
-// groups equal experts within a warp, each group's leader publishes its size
-// per (warp, expert), and a thread adds the sizes of the earlier warps.
-__global__ void __launch_bounds__(256) route_scatter_kernel(const int32_t* __restrict__ topk_ids, int T, int E,
-                                                            int k, int tc, const int32_t* __restrict__ cc,
-                                                            int32_t* __restrict__ perm,
-                                                            int32_t* __restrict__ inv_perm, int* err) {
-  extern __shared__ int smem_i[];
-  int* s_base = smem_i;      // [E] next free position of each expert
-  int* s_wc = smem_i + E;    // [8][E]
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c = blockIdx.x;
-  const int A = T * k;
+  // ---- 3: stable scatter of the chunk's assignments
   const int a0 = c * tc * k, a1 = min(A, a0 + tc * k);
-  for (int i = threadIdx.x; i < E; i += blockDim.x) s_base[i] = cc[static_cast<size_t>(c) * E + i];
   for (int ab = a0; ab < a1; ab += 256) {
     for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) s_wc[i] = 0;
     __syncthreads();
     const int a = ab + threadIdx.x;
-    int e = a < a1 ? topk_ids[a] : -1;
+    int e = a < a1 ? __ldcg(topk_ids + a) : -1;
     if (e >= E || e < -1) {
       set_device_error(err, MOE_DEV_BAD_INDEX);
       e = -1;
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const int32_t* __res
     if (e >= 0) {
       int before = 0;
       for (int w = 0; w < warp; ++w) before += s_wc[w * E + e];
-      const int pos = s_base[e] + before + rank_w;
+      const int pos = s_hist[e] + before + rank_w;
       perm[pos] = a;
       inv_perm[a] = pos;
     }
@@ -248,9 +248,15 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const int32_t* __res
     for (int i = threadIdx.x; i < E; i += blockDim.x) {
       int add = 0;
       for (int w = 0; w < 8; ++w) add += s_wc[w * E + i];
-      s_base[i] += add;
+      s_hist[i] += add;
     }
     __syncthreads();
+  }
+
+  // ---- the last CTA returns the counters to zero
+  if (threadIdx.x == 0 && atomicAdd(ctr + 1, 1) == nch - 1) {
+    ctr[0] = 0;
+    ctr[1] = 0;
   }
 }
 
@@ -265,11 +271,14 @@ int route_chunk_tokens(int T) {
 
 bool route_use_small(int T, int k) { return T * k <= 1024; }
 
+// Multi-CTA path: per-chunk counts [nch][E], then 4 ints of counters (zero between calls).
 size_t route_workspace_bytes(int T, int E, int k) {
   if (route_use_small(T, k)) return 0;
   int tc = route_chunk_tokens(T);
-  return static_cast<size_t>(ceil_div(T, tc)) * E * sizeof(int32_t);
+  return static_cast<size_t>(ceil_div(T, tc)) * E * sizeof(int32_t) + 4 * sizeof(int32_t);
 }
+
+unsigned long long wait_limit_ns();
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32_t* ids, float* w,
                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm,
@@ -287,15 +296,30 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
   const int tc = route_chunk_tokens(T);
   const int nch = ceil_div(T, tc);
   int32_t* cc = static_cast<int32_t*>(ws);
-  route_topk_kernel<<<nch, 256, E * sizeof(int), s>>>(logits, T, E, k, tc, ids, w, cc);
-  route_scan_kernel<<<1, 1024, 0, s>>>(T, E, k, bn, nch, cc, counts, offsets, bm, nb);
-  size_t sm = static_cast<size_t>(9) * E * sizeof(int);
+  int* ctr = reinterpret_cast<int*>(cc + static_cast<size_t>(nch) * E);
+  const size_t sm = static_cast<size_t>(10) * E * sizeof(int);
   if (sm > 48 * 1024) {
-    cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
+    cudaError_t e0 = cudaFuncSetAttribute(route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(sm));
+    if (e0 != cudaSuccess) return e0;
   }
-  route_scatter_kernel<<<nch, 256, sm, s>>>(ids, T, E, k, tc, cc, perm, inv_perm, err);
-  note_launches(3);
-  return cudaGetLastError();
+  const unsigned long long ns = wait_limit_ns();
+  const unsigned long long wait_cycles = ns > (~0ull) / 3 ? ~0ull : ns * 21 / 10;
+  // cooperative launch: the grid barrier needs every chunk's CTA resident (nch <= 256)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nch);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, route_fused_kernel, logits, T, E, k, tc, bn, ids, w, cc, ctr, counts,
+                                     offsets, perm, inv_perm, bm, nb, err, wait_cycles);
+  note_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe
@@ -310,11 +334,11 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
 // 256 chunks x 256 experts of int32 counts: every T this library accepts (at
 // most 256 chunks) with up to 256 routed experts.  Resident on each device
 // that loads the library until the process exits.
-static __device__ __align__(256) int32_t moe_route_scratch[256 * 256];
+static __device__ __align__(256) int32_t moe_route_scratch[256 * 256 + 4];
 
 namespace {
 
-constexpr size_t kRouteScratchBytes = sizeof(int32_t) * 256 * 256;
+constexpr size_t kRouteScratchBytes = sizeof(int32_t) * (256 * 256 + 4);
 
 // Device address of moe_route_scratch on the current device, looked up once
 // per device (the host-side name is only a stand-in for the device symbol).

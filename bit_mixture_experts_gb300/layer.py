@@ -110,7 +110,7 @@ class MoELayerW4:
             "num_blocks": torch.empty(1, dtype=torch.int32, device=dev),
             "h": torch.empty((A + T, F), dtype=torch.bfloat16, device=dev),
             "y": torch.empty((A + T, H), dtype=torch.bfloat16, device=dev),
-            "workspace": torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev),
+            "workspace": torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev),  # zero once, left zero
         }
         # counters of the fused decode kernel (used for T <= 8 with the GEMV kernel): zero once, left zero
         dws = _lib.moe_decode_workspace_size(T, H)

@@ -82,7 +82,8 @@ enum {
 /* Rows of the block map that moe_route may write: ceil(A/block_n) + E + ceil(T/block_n). */
 int moe_block_map_capacity(int T, int E, int k, int block_n);
 
-/* Bytes of scratch moe_route needs (per-chunk expert counts). */
+/* Bytes of scratch moe_route needs (per-chunk expert counts and the
+ * counters of its grid barrier; 0 when one CTA routes everything). */
 size_t moe_route_workspace_size(int T, int E, int k, int block_n);
 
 /*
@@ -106,7 +107,9 @@ size_t moe_route_workspace_size(int T, int E, int k, int block_n);
  *                             (row A+t is token t); only the first
  *                             *num_blocks rows are written
  * num_blocks int32  [1]       number of tiles (device memory)
- * workspace  device scratch of at least moe_route_workspace_size() bytes.
+ * workspace  device scratch of at least moe_route_workspace_size() bytes,
+ *            zero-filled by the caller before its first use (its last 16 bytes
+ *            hold counters that every call leaves at zero).
  * block_n    1..1024.
  */
 int moe_route(const float* logits, int T, int E, int k, int block_n,

@@ -36,7 +36,7 @@ def run_route(logits_np, k, bn):
         "block_map": torch.full((cap, 3), -7, dtype=torch.int32, device=dev),
         "num_blocks": torch.full((1,), -7, dtype=torch.int32, device=dev),
     }
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
     _lib.moe_route(logits, k, bn, o["topk_ids"], o["topk_w"], o["counts"], o["offsets"], o["perm"],
                    o["inv_perm"], o["block_map"], o["num_blocks"], ws)
     torch.cuda.synchronize()
