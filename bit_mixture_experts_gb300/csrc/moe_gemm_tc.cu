@@ -138,9 +138,16 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-// Wait that ignores s_abort (used to drain copies already in flight).
+// Wait that ignores s_abort (used to drain copies and MMAs already in flight
+// before the CTA exits).  Whatever the configured limit, it waits at least
+// DRAIN_MIN_CYCLES (about 10 ms): a copy still landing in shared memory or an
+// MMA still using TMEM must not outlive the CTA, even when a very short wait
+// limit made the kernel give up early.
+constexpr unsigned long long DRAIN_MIN_CYCLES = 20000000ull;
+
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
   if (ptx::mbar_try_wait(bar, parity)) return;
+  if (limit < DRAIN_MIN_CYCLES) limit = DRAIN_MIN_CYCLES;
   const long long t0 = clock64();
   while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (static_cast<unsigned long long>(clock64() - t0) > limit) return;

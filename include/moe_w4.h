@@ -304,9 +304,14 @@ int moe_layer_forward_host(const uint16_t* x_host, const float* logits_host, uin
  * clears it.  Returns MOE_ERR_CUDA if the synchronisation itself failed. */
 int moe_get_device_error(int32_t* code);
 
-/* Time limit of every bounded wait inside the tensor-core kernel (default
- * 1 s).  When a wait runs out the kernel records MOE_DEV_TIMEOUT, drains its
- * copies in flight, frees its tensor memory and returns.  Test hook. */
+/* Time limit of every bounded wait inside the kernels (default 1 s): the
+ * pipeline waits of the tensor-core kernel and the grid barriers of the
+ * routing and fused decode kernels.  When a wait runs out the kernel records
+ * MOE_DEV_TIMEOUT; the tensor-core kernel then leaves its loops, waits (at
+ * least about 10 ms, whatever the limit) for its copies and MMAs in flight,
+ * frees its tensor memory and returns; a grid barrier goes on.  Later kernels
+ * validate every block-map and permutation entry they read, so a routing
+ * result left incomplete by a timeout is reported, not followed.  Test hook. */
 void moe_set_wait_limit_ns(uint64_t ns);
 
 /* Library version, e.g. 0x000100 for 0.1.0. */

@@ -1,0 +1,48 @@
+"""Failure detection without a GPU fault: a wait limit far below the time the
+kernels' waits take makes them run out.  The layer call must come back with
+MOE_DEV_TIMEOUT in the device error word (no hang, no trap), and the same
+context must give correct results again once the limit is restored.
+
+Collected last (file name) so that the short limit, restored in a finally
+block, cannot leak into other tests."""
+import numpy as np
+import pytest
+
+import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+MOE_DEV_TIMEOUT = 3
+DEFAULT_LIMIT_NS = 1_000_000_000
+
+
+@pytest.mark.parametrize("impl", ["tc", "gemv"])
+def test_wait_timeout_reported_and_recovered(impl):
+    import torch
+    from bit_mixture_experts_gb300 import _lib
+    from bit_mixture_experts_gb300.layer import MoELayerW4
+    G.ensure_built()
+    # tc: 300 tokens (multi-CTA routing with its grid barrier, pipeline waits of the GEMM);
+    # gemv: 8 tokens (the fused decode kernel and its grid barriers)
+    spec = (300, 256, 16, 4, 128, False) if impl == "tc" else (8, 256, 16, 4, 128, False)
+    d = G.workload(spec)
+    T, H, E, k, F, _ = spec
+    layer = MoELayerW4(H, E, k, F, d, impl=impl)
+    x, logits = G.to_dev_inputs(d)
+    good = layer.forward(x, logits).clone()
+    torch.cuda.synchronize()
+    assert _lib.moe_get_device_error() == 0
+    _lib.moe_set_wait_limit_ns(200)  # 0.2 us: any wait on memory or another CTA runs out
+    try:
+        for _ in range(3):
+            layer.forward(x, logits)
+        torch.cuda.synchronize()
+        code = _lib.moe_get_device_error()
+    finally:
+        _lib.moe_set_wait_limit_ns(DEFAULT_LIMIT_NS)
+    assert code == MOE_DEV_TIMEOUT, code
+    # the context still works and the results are right again
+    again = layer.forward(x, logits)
+    torch.cuda.synchronize()
+    assert _lib.moe_get_device_error() == 0
+    assert np.array_equal(G.bf16_to_f64(again), G.bf16_to_f64(good))
