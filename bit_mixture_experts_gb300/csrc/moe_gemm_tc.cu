@@ -23,10 +23,10 @@
 //               quant groups of an M-tile are contiguous), completion counted
 //               in bytes on the slot's mbarrier
 //   warp 1      allocates TMEM; issues tcgen05.mma (A from TMEM, B from smem)
-//   warp 2      loads the tile's activation rows into 128B-swizzled smem with
-//               TMA: gate/up gathers token rows of x four at a time
-//               (tile::gather4), down loads contiguous rows of h
-//   warp 3      idle
+//   warps 2-3   load the tile's activation rows into 128B-swizzled smem:
+//               gate/up gathers the token rows of x with cp.async (16 bytes
+//               per copy, completion counted on the stage's mbarrier);
+//               down: warp 2 loads tiles of contiguous h rows with TMA
 //   warps 4-11  two dequant warpgroups (alternate stages): nibbles -> bf16
 //               w = bf16(q*scale + bias) with one fma.rn.bf16x2 per pair,
 //               written to TMEM with tcgen05.st
@@ -78,6 +78,9 @@ constexpr int NBAR = BAR_FIN + 1;
 // smem layout (offsets from a 1024-byte aligned base): B ring | W ring | barriers | misc
 constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
 constexpr int MISC_BYTES = 16;  // abort flag, TMEM base
+constexpr int EPI_ROWS = 32;     // output rows per epilogue chunk (one tcgen05.ld x32)
+constexpr int STAGE_BYTES = 2 * EPI_ROWS * TC_M * 2;  // epilogue staging: two chunks of 32 rows x 128 bf16
+constexpr int EPI_BAR = 1;       // named barrier of the four epilogue warps
 
 // Sizes that depend on MG, the M-tiles per work unit (they share each activation stage).
 template <int MG>
@@ -86,7 +89,7 @@ struct UnitCfg {
   static constexpr int A_COLS = MG * GPS * 32;               // TMEM columns of one dequantised stage
   static constexpr int NW = NWB / MG;                        // weight ring slots
   static constexpr int W_RING_BYTES = NW * W_STAGE;
-  static constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES;
+  static constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES + STAGE_BYTES;
 };
 
 static_assert((GPS * W_BLOCK) % 16 == 0, "bulk copies move multiples of 16 bytes");
@@ -170,6 +173,26 @@ __device__ __forceinline__ bool unit_tile(const TcParams& p, int u, int MGT, Til
 
 __device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
 
+// One quant group of one weight row: 64 nibbles (two uint4 of the repacked
+// block) and its (scale, bias) bf16 pair -> 32 bf16x2 words of
+// w = bf16(q * scale + bias).  128 + q is exact in bf16 (0x4300 | q), the
+// subtraction of 128 is exact, and the fma rounds once.
+__device__ __forceinline__ void expand_group(const uint4 p0, const uint4 p1, uint32_t sb, uint32_t (&v)[32]) {
+  const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
+  const uint32_t b2 = (sb >> 16) * 0x10001u;
+  constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // nibbles of K elements 8w+2j (low half) and 8w+2j+1 (high half): 128+q exactly
+      const uint32_t x = ((words[w] >> (4 * j)) & 0x000f000fu) | MAGIC;
+      v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
+    }
+  }
+}
+
 // silu(g) = g / (1 + e^-g) with the fast exponential and division; the
 // product with u is rounded to bf16 afterwards, which hides their few-ulp
 // error except within a few FP32 ulps of a bf16 rounding boundary.
@@ -214,6 +237,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   auto bar = [bar0](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + off_w + W_RING_BYTES + BAR_BYTES);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + off_w + W_RING_BYTES + BAR_BYTES + 4);
+  uint16_t* s_stage = reinterpret_cast<uint16_t*>(smem + off_w + W_RING_BYTES + BAR_BYTES + MISC_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = MODE == 0 ? p.H : p.F;
@@ -422,14 +446,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ptx::cp_async_wait_all();
     }
   } else if (warp < 12) {
-    // ------------------------------------------------ dequant: warpgroup wg expands the stages it with it % 2 == wg
-    // (every M-tile of the unit), so one warpgroup computes while the other waits.
-    // Each thread owns one weight row of each M-tile (= its TMEM lane).  It loads
-    // its rows of the stage from the W ring into registers and frees the slot
-    // before expanding them.
+    // ------------------------------------------------ dequant: warpgroup wg expands the stages it with
+    // it % 2 == wg (every M-tile of the stage), so one warpgroup computes while
+    // the other waits.  Each thread owns one weight row of each M-tile (= its
+    // TMEM lane).  It loads its rows of the stage from the W ring into
+    // registers, frees the slot, expands the first M-tile's groups and only
+    // then waits for the A slot, so that part of the arithmetic overlaps the
+    // MMAs still reading the slot.
     const int wg = (warp - 4) >> 2;
     const int q = warp & 3;
     const int L = 32 * q + lane;  // weight row within each M-tile = TMEM lane
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16) + A0;
     int it = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
@@ -456,31 +483,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(BAR_WEMPTY + sw));  // this warp's rows are in registers
+        uint32_t v0[GPS][32];
+#pragma unroll
+        for (int g = 0; g < GPS; ++g) expand_group(pk[0][g][0], pk[0][g][1], sbw[0][g], v0[g]);
         if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
           goto dequant_done;
+        const uint32_t ta = trow + sa * A_COLS;
 #pragma unroll
-        for (int m = 0; m < MG; ++m) {
+        for (int g = 0; g < GPS; ++g) ptx::tmem_st_32x32b_x32(ta + g * 32, v0[g]);
+#pragma unroll
+        for (int m = 1; m < MG; ++m) {
           if (m >= nm) break;
 #pragma unroll
           for (int g = 0; g < GPS; ++g) {
-            const uint4 p0 = pk[m][g][0], p1 = pk[m][g][1];
-            const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            const uint32_t s2 = (sbw[m][g] & 0xffffu) * 0x10001u;
-            const uint32_t b2 = (sbw[m][g] >> 16) * 0x10001u;
-            constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
             uint32_t v[32];
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                // nibbles of K elements 8w+2j (low half) and 8w+2j+1 (high half): 128+q exactly
-                const uint32_t x = ((words[w] >> (4 * j)) & 0x000f000fu) | MAGIC;
-                v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
-              }
-            }
-            ptx::tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + A0 + sa * A_COLS +
-                                        m * GPS * 32 + g * 32,
-                                    v);
+            expand_group(pk[m][g][0], pk[m][g][1], sbw[m][g], v);
+            ptx::tmem_st_32x32b_x32(ta + m * GPS * 32 + g * 32, v);
           }
         }
         ptx::tmem_wait_st();
@@ -492,7 +510,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   dequant_done:;
   } else {
     // ------------------------------------------------ epilogue
+    // Chunks of 32 output rows: each thread converts its lane's 32 values
+    // (one feature or channel, 32 rows) into a shared-memory tile of 32 rows
+    // x 128 columns; after a barrier of the four warps the tile goes out as
+    // whole 256-byte row segments, 16 bytes per thread (two staging buffers,
+    // so one barrier per chunk).  The four warps agree on every accumulator
+    // wait (AND-reduction barrier), so none is left waiting at a barrier.
     const int q = warp & 3;
+    const int e = threadIdx.x - 12 * 32;  // 0..127
+    const int cc = e & 15, rr = e >> 4;    // 16-byte column chunk, first row of this thread's copies
+    int sbuf = 0;
     int ui = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
       Tile t;
@@ -503,40 +530,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const int nm = min(MG, MT - grp * MG);
       const int d = ui % ND;
-      if (!wait_warp(bar(BAR_DFULL + d), (ui / ND) & 1, s_abort, p.err, lim)) break;
+      const bool ok = wait_warp(bar(BAR_DFULL + d), (ui / ND) & 1, s_abort, p.err, lim);
+      if (!ptx::named_bar_and(EPI_BAR, 128, ok)) break;
       ptx::tc_fence_after();
       const int N = round16(t.rows);
       const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + d * DBUF;  // this warp's lanes
-      if (MODE == 0) {
-        // M-tile 0 = gate rows, M-tile 1 = up rows of features 128 grp + (0..127)
-        const int f = TC_M * grp + 32 * q + lane;
-        uint16_t* h = static_cast<uint16_t*>(p.out) + static_cast<size_t>(t.row0) * p.F + f;
-        for (int c0 = 0; c0 < N; c0 += 32) {
-          uint32_t g[32], uu[32];
-          ptx::tmem_ld_32x32b_x32(tq + c0, g);
-          ptx::tmem_ld_32x32b_x32(tq + DM + c0, uu);
-          ptx::tmem_wait_ld();
-          const int nv = t.rows - c0;
+      for (int m = 0; m < (MODE == 0 ? 1 : nm); ++m) {
+        // gate/up: M-tile 0 = gate rows, M-tile 1 = up rows of features 128 grp + (0..127);
+        // down: lane = output channel 128 (grp MG + m) + (32 q + lane) of M-tile m
+        const int col0 = TC_M * (grp * MG + m) / (MODE == 0 ? MG : 1);
+        const int ld = MODE == 0 ? p.F : p.H;
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + static_cast<size_t>(t.row0) * ld + col0 + 8 * cc;
+        for (int c0 = 0; c0 < N; c0 += EPI_ROWS, sbuf ^= 1) {
+          uint16_t* st = s_stage + sbuf * (EPI_ROWS * TC_M);
+          if (MODE == 0) {
+            uint32_t g[32], uu[32];
+            ptx::tmem_ld_32x32b_x32(tq + c0, g);
+            ptx::tmem_ld_32x32b_x32(tq + DM + c0, uu);
+            ptx::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nv)
-              h[static_cast<size_t>(c0 + j) * p.F] =
+            for (int j = 0; j < 32; ++j)
+              st[j * TC_M + 32 * q + lane] =
                   float_to_bf16_bits(silu_fast(__uint_as_float(g[j])) * __uint_as_float(uu[j]));
-        }
-      } else {
-        // lane = output channel of M-tile m: y[row0 + n, channel] = bf16(D[channel, n])
-        uint16_t* y = static_cast<uint16_t*>(p.out) + static_cast<size_t>(t.row0) * p.H;
-        for (int m = 0; m < nm; ++m) {
-          const int ch = TC_M * (grp * MG + m) + 32 * q + lane;
-          for (int c0 = 0; c0 < N; c0 += 32) {
+          } else {
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(tq + m * DM + c0, v);
             ptx::tmem_wait_ld();
-            const int nv = t.rows - c0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nv) y[static_cast<size_t>(c0 + j) * p.H + ch] = float_to_bf16_bits(__uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) st[j * TC_M + 32 * q + lane] = float_to_bf16_bits(__uint_as_float(v[j]));
           }
+          ptx::named_bar_sync(EPI_BAR, 128);
+          const uint4* src = reinterpret_cast<const uint4*>(st) + cc;
+#pragma unroll
+          for (int r = rr; r < EPI_ROWS; r += 8)
+            if (c0 + r < t.rows) *reinterpret_cast<uint4*>(dst + static_cast<size_t>(c0 + r) * ld) = src[r * 16];
         }
       }
       ptx::tc_fence_before();

@@ -18,6 +18,27 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// ---------------------------------------------------------------- named CTA barriers
+// bar.sync on barrier `id` (1..15; 0 is __syncthreads) for `n` threads (a
+// multiple of 32), and the same barrier with an AND-reduction of `pred`
+// over the participating threads.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred P1, P2;\n\t"
+      "setp.ne.u32 P1, %1, 0;\n\t"
+      "bar.red.and.pred P2, %2, %3, P1;\n\t"
+      "selp.u32 %0, 1, 0, P2;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
