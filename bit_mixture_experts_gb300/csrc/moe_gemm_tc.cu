@@ -404,23 +404,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Tile t;
         int grp;
         if (!unit_tile(p, u, MGT, &t, &grp)) continue;
-        int tok[128 / 8];  // token row of tile rows row_a + 8j
+        // token row of tile rows row_a + 8j: all permutation entries are loaded
+        // first (independent loads, one round trip), then checked
+        int tok[128 / 8];
 #pragma unroll
         for (int j = 0; j < 128 / 8; ++j) {
           const int i = row_a + 8 * j;
+          const int r = t.row0 + i;
+          tok[j] = (i < t.rows && r < A) ? __ldg(p.perm + r) : 0;
+        }
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < 128 / 8; ++j) {
+          const int i = row_a + 8 * j;
+          const int r = t.row0 + i;
           int tk = -1;
           if (i < t.rows) {
-            const int r = t.row0 + i;
-            if (r < A) {
-              const int a = __ldg(p.perm + r);
-              if (a >= 0 && a < A) tk = a / p.k;
-              else set_device_error(p.err, MOE_DEV_BAD_INDEX);
-            } else {
-              tk = r - A;
-            }
+            if (r >= A) tk = r - A;  // shared-expert rows follow the routed ones, in token order
+            else if (tok[j] >= 0 && tok[j] < A) tk = tok[j] / p.k;
+            else bad = true;
           }
           tok[j] = tk;
         }
+        if (bad) set_device_error(p.err, MOE_DEV_BAD_INDEX);
         for (int ks = 0; ks < NS; ++ks, ++it) {
           const int s = it % NB, r = it / NB;
           if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) {
