@@ -324,12 +324,18 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
   // ---------------------------------------------------------------- C: combine, one warp per (token, 32 channels)
   for (int c = blockIdx.x * GV_WARPS + warp; c < T * IPT1; c += gridDim.x * GV_WARPS) {
     const int t = c / IPT1, jb = c - t * IPT1;
-    float o = 0.f;
-    for (int jj = 0; jj < k; ++jj) {
-      const uint16_t yb = __ldcg(p.y + static_cast<size_t>(s_inv[t * k + jj]) * H + 32 * jb + lane);
-      o = fmaf(s_w[t * k + jj], bf16_bits_to_float(yb), o);
-    }
+    // rows loaded eight at a time before they are summed (one L2 round trip per batch)
     const uint16_t ys = __ldcg(p.y + static_cast<size_t>(A + t) * H + 32 * jb + lane);
+    float o = 0.f;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint16_t yb[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b)
+        yb[b] = j0 + b < k ? __ldcg(p.y + static_cast<size_t>(s_inv[t * k + j0 + b]) * H + 32 * jb + lane) : 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b)
+        if (j0 + b < k) o = fmaf(s_w[t * k + j0 + b], bf16_bits_to_float(yb[b]), o);
+    }
     o = fmaf(1.0f, bf16_bits_to_float(ys), o);
     p.out[static_cast<size_t>(t) * H + 32 * jb + lane] = float_to_bf16_bits(o);
   }

@@ -168,12 +168,12 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int tot = 0, before = 0;
     int cq = 0;
-    for (; cq + 16 <= nch; cq += 16) {  // 16 independent loads in flight
-      int v[16];
+    for (; cq + 64 <= nch; cq += 64) {  // 64 independent loads in flight
+      int v[64];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = __ldcg(cc + static_cast<size_t>(cq + i) * E + e);
+      for (int i = 0; i < 64; ++i) v[i] = __ldcg(cc + static_cast<size_t>(cq + i) * E + e);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 64; ++i) {
         tot += v[i];
         before += cq + i < c ? v[i] : 0;
       }
