@@ -308,7 +308,8 @@ def run_ours(args, rank, world, local_rank):
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
     kname = {_lib.IMPL_TC: "gemm_tc_kernel<0>", _lib.IMPL_GEMV: "gemv_kernel<0>",
              _lib.IMPL_SIMT: "gemm_simt_kernel<0>"}.get(impl, str(impl))
-    traffic = profiled_traffic(wl.name, 0) if impl == _lib.IMPL_TC else None
+    traffic = (profiled_traffic(wl.name, 0) if impl == _lib.IMPL_TC else
+               profiled_traffic(wl.name, 0, kernel="decode_kernel") if fused_decode else None)
     kdesc = ("decode_kernel: the fused layer (routing, gate/up, down and combine in one launch)" if fused_decode
              else f"gate/up grouped GEMM {kname} (moe_expert_gemm_w4, MOE_GATE_UP_SWIGLU)")
     roof = {"kernel": kdesc, "bound": bound,
@@ -347,21 +348,28 @@ def run_ours(args, rank, world, local_rank):
     return res, d, layer
 
 
-def kernel_source_sha():
-    """sha256[:16] of the tensor-core GEMM's sources (the profile summaries record the one they measured)."""
+KERNEL_SOURCES = {
+    "gemm_tc_kernel": ("moe_gemm_tc.cu", "moe_ptx.cuh", "moe_common.cuh"),
+    "decode_kernel": ("moe_decode.cu", "moe_gemv_dev.cuh", "moe_route_dev.cuh", "moe_ptx.cuh", "moe_common.cuh"),
+}
+
+
+def kernel_source_sha(kernel="gemm_tc_kernel"):
+    """sha256[:16] of a kernel's sources (the profile summaries record the one they measured)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_mixture_experts_gb300", "csrc")
-    for f in ("moe_gemm_tc.cu", "moe_ptx.cuh", "moe_common.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, mode):
-    """DRAM bytes per launch of gemm_tc_kernel<mode> from the committed ncu summary of this workload,
-    or None when there is none or the kernel's sources changed since it was taken."""
-    p = os.path.join(ROOT, "profiles", f"gemm_tc_kernel.{workload}.md")
+def profiled_traffic(workload, mode, kernel="gemm_tc_kernel"):
+    """DRAM bytes per launch of the kernel (gemm_tc_kernel<mode>, or decode_kernel with mode 0) from the
+    committed ncu summary of this workload, or None when there is none or the kernel's sources changed
+    since it was taken."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.md")
     if not os.path.exists(p):
         return None
     sha, traffic = None, None
@@ -371,7 +379,7 @@ def profiled_traffic(workload, mode):
                 sha = line.rsplit("`", 2)[-2]
             if line.startswith(f"traffic_bytes_per_launch mode{mode}:"):
                 traffic = int(line.split(":")[1])
-    return traffic if sha == kernel_source_sha() else None
+    return traffic if sha == kernel_source_sha(kernel) else None
 
 
 def load_peaks():
