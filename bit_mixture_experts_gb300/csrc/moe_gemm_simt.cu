@@ -181,12 +181,14 @@ cudaError_t launch_gemm_simt(int mode, const uint16_t* act, int T, int H, int F,
 // FP32 sum in the fixed order j = 0 .. k-1, then the shared row.  Rows are
 // taken 16 at a time (k + 1 <= 16 in one batch) with all their index and row
 // loads issued before the sums, so the latency of the gather is paid once.
+// RB rows per batch: k + 1 rounded up to one of the instantiated sizes, so
+// the rows of a token normally arrive in one batch without idle registers.
 // --------------------------------------------------------------------------
+template <int RB>
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y,
                                                       const int32_t* __restrict__ inv_perm,
                                                       const float* __restrict__ topk_w, uint16_t* __restrict__ out,
                                                       int T, int H, int k, int* err) {
-  constexpr int RB = 16;  // rows per batch
   const int c8 = H / 8;  // 8-channel chunks per row
   const int A = T * k;
   const size_t n = static_cast<size_t>(T) * c8;
@@ -241,17 +243,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   }
 }
 
-cudaError_t launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T,
-                           int H, int k, int num_sms, cudaStream_t s) {
+// Grid of the resident CTAs only (each thread then takes the same number of
+// items, give or take one), from the occupancy of the instantiated kernel.
+template <int RB>
+static cudaError_t launch_combine_rb(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out,
+                                     int T, int H, int k, int num_sms, cudaStream_t s) {
+  static int occ = 0;
+  if (occ == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, combine_kernel<RB>, 256, 0) != cudaSuccess)
+    occ = 0;
+  if (occ <= 0) occ = 2;
   const size_t n = static_cast<size_t>(T) * (H / 8);
   size_t blocks = (n + 255) / 256;
-  const size_t cap = static_cast<size_t>(num_sms) * 8;
+  const size_t cap = static_cast<size_t>(num_sms) * occ;
   if (blocks > cap) blocks = cap;
   if (blocks == 0) blocks = 1;
-  combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(y, inv_perm, topk_w, out, T, H, k,
-                                                               device_error_ptr());
+  combine_kernel<RB><<<static_cast<unsigned>(blocks), 256, 0, s>>>(y, inv_perm, topk_w, out, T, H, k,
+                                                                   device_error_ptr());
   note_launches(1);
   return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T,
+                           int H, int k, int num_sms, cudaStream_t s) {
+  if (k + 1 <= 3) return launch_combine_rb<3>(y, inv_perm, topk_w, out, T, H, k, num_sms, s);
+  if (k + 1 <= 9) return launch_combine_rb<9>(y, inv_perm, topk_w, out, T, H, k, num_sms, s);
+  return launch_combine_rb<16>(y, inv_perm, topk_w, out, T, H, k, num_sms, s);
 }
 
 }  // namespace moe
