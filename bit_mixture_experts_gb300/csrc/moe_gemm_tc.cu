@@ -51,11 +51,9 @@ namespace {
 
 constexpr int TC_M = 128;              // weight rows per M-tile (the MMA's M)
 constexpr int KG = 64;                 // one quantisation group
-constexpr int GPS = 2;                 // quant groups per pipeline stage
-constexpr int KS = KG * GPS;           // K per stage
 constexpr int W_PACKED = TC_M * 32;    // packed nibbles of one M-tile x K group
 constexpr int W_BLOCK = W_PACKED + TC_M * 4;  // + (scale, bias) per row: one repacked block
-constexpr int NWB = 12;                // packed-weight ring bytes, in units of one M-tile's stage
+constexpr int NWB = 12;                // packed-weight ring bytes, in units of one M-tile's 2-group stage
 constexpr int NAMAX = 4;               // dequantised-weight ring (TMEM), run-time depth 2 to 4
 constexpr int NBMAX = 12;              // activation ring (smem), run-time depth <= NBMAX
 constexpr int TMEM_COLS = 512;        // accumulators first, then the A ring
@@ -63,7 +61,7 @@ constexpr int NTHREADS = 512;
 constexpr int GATHER_T = 64;           // threads gathering activation rows (gate/up)
 
 // barrier indices
-constexpr int NWMAX = NWB;             // weight ring slots (NWB / MG)
+constexpr int NWMAX = NWB;             // weight ring slots (at most)
 constexpr int BAR_WFULL = 0;
 constexpr int BAR_WEMPTY = BAR_WFULL + NWMAX;
 constexpr int BAR_AFULL = BAR_WEMPTY + NWMAX;
@@ -82,17 +80,21 @@ constexpr int EPI_ROWS = 32;     // output rows per epilogue chunk (one tcgen05.
 constexpr int STAGE_BYTES = 2 * EPI_ROWS * TC_M * 2;  // epilogue staging: two chunks of 32 rows x 128 bf16
 constexpr int EPI_BAR = 1;       // named barrier of the four epilogue warps
 
-// Sizes that depend on MG, the M-tiles per work unit (they share each activation stage).
-template <int MG>
+// Sizes that depend on MG, the M-tiles per work unit (they share each
+// activation stage), and GPS, the quant groups per pipeline stage.  The weight
+// ring holds NWB two-group M-tile stages' bytes, except for four-group stages
+// (two-stage-deep activation ring of 64 KB stages) where it shrinks to 4 slots.
+template <int MG, int GPS>
 struct UnitCfg {
   static constexpr int W_STAGE = MG * GPS * W_BLOCK;         // packed weights of one stage
   static constexpr int A_COLS = MG * GPS * 32;               // TMEM columns of one dequantised stage
-  static constexpr int NW = NWB / MG;                        // weight ring slots
+  static constexpr int NW = GPS == 4 ? 4 : NWB * 2 / (MG * GPS);  // weight ring slots
+  static_assert(NW <= NWMAX, "weight ring barriers");
+  static_assert((GPS * W_BLOCK) % 16 == 0, "bulk copies move multiples of 16 bytes");
   static constexpr int W_RING_BYTES = NW * W_STAGE;
   static constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES + STAGE_BYTES;
 };
 
-static_assert((GPS * W_BLOCK) % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 struct TcParams {
   const uint16_t* act;
@@ -107,7 +109,7 @@ struct TcParams {
   int T, H, F, E, k, bn, cap;
   int boxr;     // activation rows per stage buffer (block_n rounded up to 16, <= 128)
   int nb;       // activation ring depth
-  int sb;       // bytes of one activation stage: GPS atoms of boxr rows x 128 bytes
+  int sb;       // bytes of one activation stage: one atom of boxr rows x 128 bytes per quant group
   int nd;       // accumulator buffers
   int dm;       // TMEM columns of one M-tile's accumulator (= boxr)
   int na;       // A ring depth
@@ -217,15 +219,17 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f 
 //      gate/up: cp.async gather of token rows (warps 2-3),
 //      down: TMA tiles of contiguous h rows (warp 2)  -> MMA
 //   D  FP32 accumulators, TMEM, MMA -> epilogue (1 or 2 buffers)
-template <int MODE, int MG>
+template <int MODE, int MG, int GPS>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmap_act) {
   static_assert(MODE == 1 || MG == 2, "gate/up pairs the gate and the up M-tile in one unit");
   static_assert(MG == 1 || MG == 2, "one or two M-tiles per unit");
-  constexpr int W_STAGE = UnitCfg<MG>::W_STAGE;
-  constexpr int A_COLS = UnitCfg<MG>::A_COLS;
-  constexpr int W_RING_BYTES = UnitCfg<MG>::W_RING_BYTES;
-  constexpr int NW = UnitCfg<MG>::NW;
+  static_assert(GPS == 2 || (GPS == 4 && MODE == 1 && MG == 1), "2-group stages, or 4 for the one-M-tile down GEMM");
+  constexpr int W_STAGE = UnitCfg<MG, GPS>::W_STAGE;
+  constexpr int A_COLS = UnitCfg<MG, GPS>::A_COLS;
+  constexpr int W_RING_BYTES = UnitCfg<MG, GPS>::W_RING_BYTES;
+  constexpr int NW = UnitCfg<MG, GPS>::NW;
+  constexpr int KS = KG * GPS;               // K per stage
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -489,19 +493,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(BAR_WEMPTY + sw));  // this warp's rows are in registers
-        uint32_t v0[GPS][32];
+        constexpr int PRE = GPS < 2 ? GPS : 2;  // groups expanded before the A slot is free
+        uint32_t v0[PRE][32];
 #pragma unroll
-        for (int g = 0; g < GPS; ++g) expand_group(pk[0][g][0], pk[0][g][1], sbw[0][g], v0[g]);
+        for (int g = 0; g < PRE; ++g) expand_group(pk[0][g][0], pk[0][g][1], sbw[0][g], v0[g]);
         if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
           goto dequant_done;
         const uint32_t ta = trow + sa * A_COLS;
 #pragma unroll
-        for (int g = 0; g < GPS; ++g) ptx::tmem_st_32x32b_x32(ta + g * 32, v0[g]);
+        for (int g = 0; g < PRE; ++g) ptx::tmem_st_32x32b_x32(ta + g * 32, v0[g]);
 #pragma unroll
-        for (int m = 1; m < MG; ++m) {
+        for (int m = 0; m < MG; ++m) {
           if (m >= nm) break;
 #pragma unroll
-          for (int g = 0; g < GPS; ++g) {
+          for (int g = m == 0 ? PRE : 0; g < GPS; ++g) {
             uint32_t v[32];
             expand_group(pk[m][g][0], pk[m][g][1], sbw[m][g], v);
             ptx::tmem_st_32x32b_x32(ta + m * GPS * 32 + g * 32, v);
@@ -722,11 +727,13 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   const int boxr = (bn + 15) & ~15;
   if (boxr > 128) return cudaErrorInvalidValue;
   prm.boxr = boxr;
-  prm.sb = GPS * boxr * 128;
   // M-tiles per unit: gate/up pairs gate and up; the down GEMM keeps two accumulator buffers
   const int MG = (mode == MOE_GATE_UP_SWIGLU || boxr <= 64) ? 2 : 1;
-  const int tail = MG == 2 ? UnitCfg<2>::TAIL_BYTES : UnitCfg<1>::TAIL_BYTES;
-  const int a_cols = MG == 2 ? UnitCfg<2>::A_COLS : UnitCfg<1>::A_COLS;
+  // quant groups per stage: the one-M-tile down GEMM takes 4 (16 MMAs per stage, as the two-M-tile units)
+  const int GPS = (MG == 1 && F % (4 * KG) == 0) ? 4 : 2;
+  prm.sb = GPS * boxr * 128;
+  const int tail = MG == 2 ? UnitCfg<2, 2>::TAIL_BYTES : GPS == 4 ? UnitCfg<1, 4>::TAIL_BYTES : UnitCfg<1, 2>::TAIL_BYTES;
+  const int a_cols = MG == 2 ? UnitCfg<2, 2>::A_COLS : GPS == 4 ? UnitCfg<1, 4>::A_COLS : UnitCfg<1, 2>::A_COLS;
   const int budget = max_dyn_smem() - tail - 1024;
   int nbs = budget / prm.sb;
   if (nbs > NBMAX) nbs = NBMAX;
@@ -758,16 +765,12 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  if (mode == MOE_GATE_UP_SWIGLU) {
-    cudaFuncSetAttribute(gemm_tc_kernel<0, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    gemm_tc_kernel<0, 2><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
-  } else if (MG == 2) {
-    cudaFuncSetAttribute(gemm_tc_kernel<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    gemm_tc_kernel<1, 2><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
-  } else {
-    cudaFuncSetAttribute(gemm_tc_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    gemm_tc_kernel<1, 1><<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
-  }
+  void (*kern)(const TcParams, const CUtensorMap) = mode == MOE_GATE_UP_SWIGLU ? gemm_tc_kernel<0, 2, 2>
+                                                    : MG == 2                    ? gemm_tc_kernel<1, 2, 2>
+                                                    : GPS == 4                   ? gemm_tc_kernel<1, 1, 4>
+                                                                                 : gemm_tc_kernel<1, 1, 2>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  kern<<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
   note_launches(1);
   return cudaGetLastError();
 }
