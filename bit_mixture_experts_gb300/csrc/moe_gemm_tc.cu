@@ -342,23 +342,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // group g's activations are B atom g (K = 64, four K16 steps)
         if (two) {
 #pragma unroll
-          for (int g = 0; g < GPS; ++g) {
-            const uint64_t bd = ptx::smem_desc_sw128(b0 + g * atom_bytes);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t acc = (g == 0 && j == 0) ? acc0 : 1u;
-              ptx::mma_ts_elect(d0, a0 + g * 32 + 8 * j, bd + 2 * j, idesc, acc);
-              ptx::mma_ts_elect(d1, a0 + GPS * 32 + g * 32 + 8 * j, bd + 2 * j, idesc, acc);
-            }
-          }
+          for (int g = 0; g < GPS; ++g)
+            ptx::mma_group_ts_elect<true>(d0, d1, a0 + g * 32, a0 + GPS * 32 + g * 32,
+                                          ptx::smem_desc_sw128(b0 + g * atom_bytes), idesc, g == 0 ? acc0 : 1u);
         } else {
 #pragma unroll
-          for (int g = 0; g < GPS; ++g) {
-            const uint64_t bd = ptx::smem_desc_sw128(b0 + g * atom_bytes);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              ptx::mma_ts_elect(d0, a0 + g * 32 + 8 * j, bd + 2 * j, idesc, (g == 0 && j == 0) ? acc0 : 1u);
-          }
+          for (int g = 0; g < GPS; ++g)
+            ptx::mma_group_ts_elect<false>(d0, d0, a0 + g * 32, a0 + g * 32, ptx::smem_desc_sw128(b0 + g * atom_bytes),
+                                           idesc, g == 0 ? acc0 : 1u);
         }
         ptx::mma_commit_elect(bar(BAR_AEMPTY + sa));
         ptx::mma_commit_elect(bar(BAR_BEMPTY + sb));

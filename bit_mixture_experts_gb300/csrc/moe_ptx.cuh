@@ -266,6 +266,50 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// The four K16 steps of one quant group (K = 64) under one elect.sync: for
+// j = 0..3, D0 += A0[:, 16j : 16j + 16] x B[16j : 16j + 16] (A columns a0 + 8j,
+// B descriptor b_desc + 2j, i.e. 32 bytes further along K in the swizzled
+// atom), and the same into D1 from A1 when PAIR.  The first step keeps the
+// accumulator only if `accumulate` is non-zero; the later ones always do.
+template <bool PAIR>
+__device__ __forceinline__ void mma_group_ts_elect(uint32_t d0, uint32_t d1, uint32_t a0, uint32_t a1, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate) {
+  if (PAIR) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b32 x1, x2, x3, y1, y2, y3;\n\t.reg .b64 c1, c2, c3;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "add.u32 x1, %2, 8;\n\tadd.u32 x2, %2, 16;\n\tadd.u32 x3, %2, 24;\n\t"
+        "add.u32 y1, %3, 8;\n\tadd.u32 y2, %3, 16;\n\tadd.u32 y3, %3, 24;\n\t"
+        "add.s64 c1, %4, 2;\n\tadd.s64 c2, %4, 4;\n\tadd.s64 c3, %4, 6;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %4, %5, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [%3], %4, %5, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], c1, %5, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [y1], c1, %5, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], c2, %5, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [y2], c2, %5, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], c3, %5, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [y3], c3, %5, q;\n\t}" ::"r"(d0),
+        "r"(d1), "r"(a0), "r"(a1), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e;\n\t.reg .b32 x1, x2, x3;\n\t.reg .b64 c1, c2, c3;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.ne.b32 q, %3, 0;\n\t"
+        "add.u32 x1, %1, 8;\n\tadd.u32 x2, %1, 16;\n\tadd.u32 x3, %1, 24;\n\t"
+        "add.s64 c1, %2, 2;\n\tadd.s64 c2, %2, 4;\n\tadd.s64 c3, %2, 6;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x1], c1, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x2], c2, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [x3], c3, %3, q;\n\t}" ::"r"(d0),
+        "r"(a0), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
