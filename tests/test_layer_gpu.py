@@ -42,6 +42,7 @@ SMALL = [
     (1, 256, 16, 2, 128, False),      # a single token
     (77, 128, 64, 8, 128, False),     # many empty experts
     (1000, 256, 16, 4, 384, True),    # skewed logits (Zipf offset), F not a power of two
+    (600, 256, 8, 2, 256, False),     # 128-row tiles, F % 256 == 0: down units of one M-tile, 4-group stages
 ]
 
 
