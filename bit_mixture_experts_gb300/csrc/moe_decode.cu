@@ -102,6 +102,116 @@ __device__ __forceinline__ void dec_dot(int nrow, const uint4* swq, const uint32
   }
 }
 
+// Small-batch routing (at most 64 assignments, T <= bn so that every expert's
+// rows form one tile), by warps 0 and 1, thread a = assignment a: its
+// permuted row is its rank among the keys (expert, assignment) -- by expert,
+// then in assignment order, as moe_route's stable scatter -- and a tile
+// starts wherever the expert changes along the sorted rows (found by warp 0);
+// the shared expert's T rows follow as one tile.  s_ok receives the number
+// of routed tiles.
+__device__ __noinline__ void route_small_batch(const int* s_ids, int* s_inv, int* s_tok, int* s_sorted,
+                                               int (*s_tile)[3], int* s_ok, int A, int T, int E, int k) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int a = 32 * warp + lane;
+  if (a < A) {
+    const int e = s_ids[a];
+    const int key = e * 64 + a;
+    int r = 0;
+    for (int a2 = 0; a2 < A; ++a2) r += s_ids[a2] * 64 + a2 < key;
+    s_inv[a] = r;
+    s_tok[r] = a / k;
+    s_sorted[r] = e;
+  }
+  ptx::named_bar_sync(1, 64);
+  if (warp != 0) return;
+  // a run of one expert starts at sorted row r when r == 0 or the expert changes there
+  unsigned long long starts = 0;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int r = lane + 32 * q;
+    const bool st = r < A && (r == 0 || s_sorted[r] != s_sorted[r - 1]);
+    starts |= static_cast<unsigned long long>(__ballot_sync(0xffffffffu, st)) << (32 * q);
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int r = lane + 32 * q;
+    if ((starts >> r) & 1ull) {
+      const int ti = __popcll(starts & ((1ull << r) - 1ull));
+      const unsigned long long later = r == 63 ? 0ull : starts & ~((2ull << r) - 1ull);
+      s_tile[ti][0] = s_sorted[r];
+      s_tile[ti][1] = r;
+      s_tile[ti][2] = (later ? __ffsll(static_cast<long long>(later)) - 1 : A) - r;
+    }
+  }
+  if (lane == 0) {
+    const int n = __popcll(starts);
+    *s_ok = n;
+    s_tile[n][0] = E;
+    s_tile[n][1] = A;
+    s_tile[n][2] = T;
+  }
+  if (lane < T) s_tok[A + lane] = lane;
+}
+
+// General routing in shared memory, by the whole CTA: per-expert counts,
+// their exclusive scan (offsets and first tiles), the stable permutation and
+// the block map, as moe_route computes them.  s_ok receives the number of
+// routed tiles.
+__device__ __noinline__ void route_general(const int* s_ids, int* s_inv, int* s_tok, int (*s_tile)[3], int* s_cnt,
+                                           int* s_off, int* s_tile0, uint64_t* s_scan, int* s_ok, int A, int T,
+                                           int E, int k, int bn) {
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += GV_THREADS) s_cnt[e] = 0;
+  __syncthreads();
+  for (int a = tid; a < A; a += GV_THREADS) atomicAdd(&s_cnt[s_ids[a]], 1);  // integer counts
+  __syncthreads();
+  {
+    // offsets and first tile of every expert: exclusive scan of (count, tiles) in expert order
+    const int per = ceil_div(E, GV_THREADS);
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    uint64_t loc = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int c = s_cnt[e];
+      loc += (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(ceil_div(c, bn));
+    }
+    uint64_t total;
+    uint64_t run = route_dev::block_exclusive_scan(loc, s_scan, &total);
+    for (int e = e0; e < e1; ++e) {
+      const int c = s_cnt[e];
+      s_off[e] = static_cast<int>(run >> 32);
+      s_tile0[e] = static_cast<int>(run & 0xffffffffu);
+      run += (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(ceil_div(c, bn));
+    }
+    if (tid == 0) *s_ok = static_cast<int>(total & 0xffffffffu);  // routed tiles
+  }
+  __syncthreads();
+  const int ntr = *s_ok;
+  // stable permutation: by expert, then by assignment index
+  for (int a = tid; a < A; a += GV_THREADS) {
+    const int e = s_ids[a];
+    int r = 0;
+    for (int a2 = 0; a2 < a; ++a2) r += s_ids[a2] == e;
+    const int row = s_off[e] + r;
+    s_inv[a] = row;
+    s_tok[row] = a / k;
+  }
+  for (int t = tid; t < T; t += GV_THREADS) s_tok[A + t] = t;
+  for (int e = tid; e < E; e += GV_THREADS) {
+    const int c = s_cnt[e];
+    for (int i = 0, r = 0; r < c; ++i, r += bn) {
+      s_tile[s_tile0[e] + i][0] = e;
+      s_tile[s_tile0[e] + i][1] = s_off[e] + r;
+      s_tile[s_tile0[e] + i][2] = min(bn, c - r);
+    }
+  }
+  for (int i = tid, r = tid * bn; r < T; i += GV_THREADS, r += GV_THREADS * bn) {
+    s_tile[ntr + i][0] = E;
+    s_tile[ntr + i][1] = A + r;
+    s_tile[ntr + i][2] = min(bn, T - r);
+  }
+  __syncthreads();
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(const DecParams p) {
@@ -111,6 +221,7 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
   __shared__ int s_tok[DEC_MAXA + DEC_MAXT];     // permuted row -> token
   __shared__ int s_tile[DEC_MAXTILES][3];        // (expert, first row, rows)
   __shared__ uint64_t s_scan[33];
+  __shared__ int s_sorted[64];                   // small-batch path: expert of each permuted row
   __shared__ int s_ok;
   extern __shared__ uint4 dec_smem[];
   const int T = p.T, E = p.E, k = p.k, bn = p.bn, H = p.H, F = p.F;
@@ -137,56 +248,29 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
       s_w[warp * k + lane] = w;
     }
   }
-  for (int e = tid; e < E; e += GV_THREADS) s_cnt[e] = 0;
-  __syncthreads();
-  for (int a = tid; a < A; a += GV_THREADS) atomicAdd(&s_cnt[s_ids[a]], 1);  // integer counts
-  __syncthreads();
-  {
-    // offsets and first tile of every expert: exclusive scan of (count, tiles) in expert order
-    const int per = ceil_div(E, GV_THREADS);
-    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
-    uint64_t loc = 0;
-    for (int e = e0; e < e1; ++e) {
-      const int c = s_cnt[e];
-      loc += (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(ceil_div(c, bn));
+  // Small batches (at most 64 assignments, every expert's rows in one tile):
+  // two warps rank the assignments and read the tiles off the sorted rows,
+  // with no pass over all E experts (the same result as the general path).
+  if (A <= 64 && T <= bn) {
+    __syncthreads();  // s_ids
+    if (warp < 2) route_small_batch(s_ids, s_inv, s_tok, s_sorted, s_tile, &s_ok, A, T, E, k);
+    if (blockIdx.x == 0) {  // counts and offsets of every expert, for moe_route's outputs
+      for (int e = tid; e < E; e += GV_THREADS) {
+        int c = 0, o = 0;
+        for (int a = 0; a < A; ++a) {
+          c += s_ids[a] == e;
+          o += s_ids[a] < e;
+        }
+        s_cnt[e] = c;
+        s_off[e] = o;
+      }
     }
-    uint64_t total;
-    uint64_t run = route_dev::block_exclusive_scan(loc, s_scan, &total);
-    for (int e = e0; e < e1; ++e) {
-      const int c = s_cnt[e];
-      s_off[e] = static_cast<int>(run >> 32);
-      s_tile0[e] = static_cast<int>(run & 0xffffffffu);
-      run += (static_cast<uint64_t>(c) << 32) | static_cast<uint32_t>(ceil_div(c, bn));
-    }
-    if (tid == 0) s_ok = static_cast<int>(total & 0xffffffffu);  // routed tiles
+    __syncthreads();
+  } else {
+    route_general(s_ids, s_inv, s_tok, s_tile, s_cnt, s_off, s_tile0, s_scan, &s_ok, A, T, E, k, bn);
   }
-  __syncthreads();
   const int ntr = s_ok;
   const int nt = ntr + ceil_div(T, bn);
-  // stable permutation: by expert, then by assignment index
-  for (int a = tid; a < A; a += GV_THREADS) {
-    const int e = s_ids[a];
-    int r = 0;
-    for (int a2 = 0; a2 < a; ++a2) r += s_ids[a2] == e;
-    const int row = s_off[e] + r;
-    s_inv[a] = row;
-    s_tok[row] = a / k;
-  }
-  for (int t = tid; t < T; t += GV_THREADS) s_tok[A + t] = t;
-  for (int e = tid; e < E; e += GV_THREADS) {
-    const int c = s_cnt[e];
-    for (int i = 0, r = 0; r < c; ++i, r += bn) {
-      s_tile[s_tile0[e] + i][0] = e;
-      s_tile[s_tile0[e] + i][1] = s_off[e] + r;
-      s_tile[s_tile0[e] + i][2] = min(bn, c - r);
-    }
-  }
-  for (int i = tid, r = tid * bn; r < T; i += GV_THREADS, r += GV_THREADS * bn) {
-    s_tile[ntr + i][0] = E;
-    s_tile[ntr + i][1] = A + r;
-    s_tile[ntr + i][2] = min(bn, T - r);
-  }
-  __syncthreads();
   if (blockIdx.x == 0) {
     // the outputs of moe_route for the same logits
     for (int a = tid; a < A; a += GV_THREADS) {
