@@ -355,13 +355,26 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_sha(kernel="gemm_tc_kernel"):
-    """sha256[:16] of a kernel's sources (the profile summaries record the one they measured)."""
+    """sha256[:16] of a kernel's source code with comments and blank space removed (the profile
+    summaries record the one they measured, so an edit of comments alone keeps them valid)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_mixture_experts_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        code = []
+        for line in text.split("\n"):
+            # drop a // comment unless the // sits inside a string literal on that line
+            cut = line.find("//")
+            if cut >= 0 and line[:cut].count('"') % 2 == 0:
+                line = line[:cut]
+            line = " ".join(line.split())
+            if line:
+                code.append(line)
+        h.update("\n".join(code).encode())
     return h.hexdigest()[:16]
 
 

@@ -13,9 +13,11 @@
 //   D[m, n] = sum_k W[m, k] * X[n, k]      (swap-AB: weight rows on M, tokens on N)
 //
 //   M = 128 weight rows of one expert (one "M-tile"), N = the tile's token
-//   rows rounded up to 16 (<= 256), K stepped 64 at a time (one quant group).
+//   rows rounded up to 16 (<= 128), K = 16 per MMA; a pipeline stage covers
+//   two quant groups (K = 128), four in the one-M-tile down GEMM.
 //
-// Roles (512 threads, one CTA per SM, persistent over (block-map tile, M-tile)).
+// Roles (512 threads, one CTA per SM, persistent over work units = (block-map
+// tile, group of MG M-tiles), taken round-robin).
 // Warps 0-2 run their loops converged with warp-uniform operands and let
 // elect.sync pick the lane that issues each copy, MMA or commit:
 //   warp 0      streams the packed weights into a shared-memory ring with
@@ -35,6 +37,8 @@
 //                        of the same 128 features, so each thread holds g and
 //                        u of its feature: h = bf16(silu(g) * u) -> h[row, f]
 //               down:    y = bf16(acc) -> y[row, channel]
+//               staged 32 rows at a time in shared memory and written as
+//               whole 256-byte row segments
 //
 // Every mbarrier wait is bounded by a time limit; on expiry the kernel records
 // MOE_DEV_TIMEOUT in the device error word, every role leaves its loop, copies
@@ -203,12 +207,13 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f 
 }  // namespace
 
 // Work unit: one block-map tile (<= 128 token rows) x MG M-tiles (MG x 128
-// weight rows) of one expert.  Each pipeline stage covers K = 128 (two quant
-// groups): the M-tiles' packed blocks, their dequantised bf16 in TMEM and one
-// activation stage read by every M-tile's MMAs.  Gate/up always takes MG = 2
-// (the gate and the up M-tile of the same features); the down GEMM takes MG =
-// 1 for tiles of more than 64 rows, so that two accumulator buffers still fit
-// in TMEM and the epilogue of one unit overlaps the next unit's mainloop.
+// weight rows) of one expert.  Each pipeline stage covers GPS quant groups
+// (K = 64 GPS): the M-tiles' packed blocks, their dequantised bf16 in TMEM and
+// one activation stage read by every M-tile's MMAs.  Gate/up always takes
+// MG = 2 (the gate and the up M-tile of the same features); the down GEMM takes
+// MG = 1 for tiles of more than 64 rows, so that two accumulator buffers still
+// fit in TMEM and the epilogue of one unit overlaps the next unit's mainloop,
+// and then GPS = 4 so that a stage still carries 16 MMAs.
 //
 // Rings (full/empty mbarriers; stage index = running stage count `it` modulo
 // the ring depth):
