@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
                                                           int tc, int bn, int32_t* topk_ids, float* topk_w,
                                                           int32_t* cc, int* ctr, int32_t* counts, int32_t* offsets,
                                                           int32_t* perm, int32_t* inv_perm, int32_t* block_map,
-                                                          int32_t* num_blocks, int* err,
+                                                          int32_t* num_blocks, int cap, int* err,
                                                           unsigned long long wait_cycles) {
   extern __shared__ int smem_i[];
   int* s_hist = smem_i;        // [E] chunk counts, then the chunk's next free row per expert
@@ -186,7 +186,13 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
     s_tot[e] = tot;
     s_hist[e] = before;
   }
-  __syncthreads();
+  // Counts that cannot come from this call (a workspace that was not zero
+  // when the call began breaks the barrier and the per-chunk counts): every
+  // total must be >= 0 and they must add up to T*k with the tiles fitting in
+  // the block map; otherwise nothing below is written and the error is recorded.
+  bool bad = false;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) bad |= s_tot[e] < 0 || s_hist[e] < 0 || s_hist[e] > s_tot[e];
+  bad = __syncthreads_or(bad);
   {
     const int per = ceil_div(E, static_cast<int>(blockDim.x));
     const int e0 = min(E, static_cast<int>(threadIdx.x) * per), e1 = min(E, e0 + per);
@@ -196,7 +202,9 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
     uint64_t total;
     uint64_t run = block_exclusive_scan(loc, s_scan, &total);
     const int ntiles = static_cast<int>(total & 0xffffffffu);
-    for (int e = e0; e < e1; ++e) {
+    bad = bad || static_cast<int>(total >> 32) != A || ntiles + ceil_div(T, bn) > cap;
+    if (bad && c == 0 && threadIdx.x == 0) set_device_error(err, MOE_DEV_BAD_INDEX);
+    for (int e = e0; e < e1 && !bad; ++e) {
       const int cnt = s_tot[e];
       const int off = static_cast<int>(run >> 32), tile0 = static_cast<int>(run & 0xffffffffu);
       s_hist[e] += off;
@@ -207,7 +215,7 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
       }
       run += (static_cast<uint64_t>(cnt) << 32) | static_cast<uint32_t>(ceil_div(cnt, bn));
     }
-    if (c == 0) {
+    if (c == 0 && !bad) {
       if (threadIdx.x == 0) {
         offsets[E] = A;
         num_blocks[0] = ntiles + ceil_div(T, bn);
@@ -222,8 +230,8 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
   }
   __syncthreads();
 
-  // ---- 3: stable scatter of the chunk's assignments
-  const int a0 = c * tc * k, a1 = min(A, a0 + tc * k);
+  // ---- 3: stable scatter of the chunk's assignments (bad is the same in every thread of the CTA)
+  const int a0 = c * tc * k, a1 = bad ? a0 : min(A, a0 + tc * k);
   for (int ab = a0; ab < a1; ab += 256) {
     for (int i = threadIdx.x; i < 8 * E; i += blockDim.x) s_wc[i] = 0;
     __syncthreads();
@@ -241,8 +249,12 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
       int before = 0;
       for (int w = 0; w < warp; ++w) before += s_wc[w * E + e];
       const int pos = s_hist[e] + before + rank_w;
-      perm[pos] = a;
-      inv_perm[a] = pos;
+      if (pos >= 0 && pos < A) {
+        perm[pos] = a;
+        inv_perm[a] = pos;
+      } else {
+        set_device_error(err, MOE_DEV_BAD_INDEX);
+      }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < E; i += blockDim.x) {
@@ -316,8 +328,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  const int cap = moe_block_map_capacity(T, E, k, bn);
   cudaError_t e = cudaLaunchKernelEx(&cfg, route_fused_kernel, logits, T, E, k, tc, bn, ids, w, cc, ctr, counts,
-                                     offsets, perm, inv_perm, bm, nb, err, wait_cycles);
+                                     offsets, perm, inv_perm, bm, nb, cap, err, wait_cycles);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -47,7 +47,8 @@ def _route_both(logits_np, k, bn):
     logits = torch.from_numpy(np.ascontiguousarray(logits_np, np.float32)).to(dev)
     ref = _buffers(T, E, k, bn, dev)
     got = _buffers(T, E, k, bn, dev)
-    ws = torch.empty(max(_lib.moe_route_workspace_size(T, E, k, bn), 16), dtype=torch.uint8, device=dev)
+    # moe_route needs its workspace zero-filled before the first call (its barrier counters start at zero)
+    ws = torch.zeros(max(_lib.moe_route_workspace_size(T, E, k, bn), 16), dtype=torch.uint8, device=dev)
     _lib.moe_route(logits, k, bn, *(ref[n] for n in ("topk_ids", "topk_w", "counts", "offsets", "perm",
                                                      "inv_perm", "block_map", "num_blocks")), ws)
     _lib.moe_route_noalloc(logits, k, bn, *(got[n] for n in ("topk_ids", "topk_w", "counts", "offsets", "perm",
