@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(PKG, "libmoe_w4.so")
 MOE_OK = 0
 ERRORS = {-1: "MOE_ERR_NULL", -2: "MOE_ERR_ALIGN", -3: "MOE_ERR_SHAPE", -4: "MOE_ERR_WORKSPACE",
           -5: "MOE_ERR_CUDA", -6: "MOE_ERR_DEVICE", -7: "MOE_ERR_MODE"}
-DEVICE_ERRORS = {0: "ok", 1: "MOE_DEV_BAD_BLOCK", 2: "MOE_DEV_BAD_INDEX", 3: "MOE_DEV_TIMEOUT"}
+DEVICE_ERRORS = {0: "ok", 1: "MOE_DEV_BAD_BLOCK", 2: "MOE_DEV_BAD_INDEX", 3: "MOE_DEV_TIMEOUT", 4: "MOE_DEV_BAD_WORKSPACE"}
 
 GATE_UP, DOWN = 0, 1
 IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_GEMV = 0, 1, 2, 3

@@ -47,7 +47,7 @@ int num_sms() {
 size_t route_workspace_bytes(int T, int E, int k);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32_t* ids, float* w, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm, int32_t* nb, void* ws,
-                         cudaStream_t s);
+                         size_t ws_bytes, cudaStream_t s);
 cudaError_t launch_gemm_simt(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const uint32_t* wq,
                              const uint16_t* ws, const uint16_t* wb, const int32_t* perm, const float* topk_w,
                              const int32_t* block_map, const int32_t* num_blocks, int bn, int nb_cap, void* out,
@@ -136,7 +136,8 @@ int moe_route(const float* logits, int T, int E, int k, int block_n, int32_t* to
   }
   if (!device_error_ptr()) return MOE_ERR_CUDA;
   return cuda_status(launch_route(logits, T, E, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm,
-                                  block_map, num_blocks, workspace, reinterpret_cast<cudaStream_t>(stream)));
+                                  block_map, num_blocks, workspace, workspace_bytes,
+                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,

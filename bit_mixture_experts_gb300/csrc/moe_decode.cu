@@ -337,7 +337,9 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
     __syncthreads();
     if (tid == 0) {
       __threadfence();  // this CTA's h / y values before its arrival
-      atomicAdd(bar, 1);
+      const int before_me = atomicAdd(bar, 1);
+      if (before_me < 0 || before_me >= static_cast<int>(gridDim.x))
+        set_device_error(p.err, MOE_DEV_BAD_WORKSPACE);  // the workspace was not zero at the start
       const long long t0 = clock64();
       while (ld_acquire(bar) < static_cast<int>(gridDim.x)) {
         if (static_cast<unsigned long long>(clock64() - t0) > p.wait_cycles) {

@@ -152,7 +152,8 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    atomicAdd(ctr, 1);
+    const int before_me = atomicAdd(ctr, 1);
+    if (before_me < 0 || before_me >= nch) set_device_error(err, MOE_DEV_BAD_WORKSPACE);  // counter not zero at the start
     const long long w0 = clock64();
     while (ld_acquire_gpu(ctr) < nch) {
       if (static_cast<unsigned long long>(clock64() - w0) > wait_cycles) {
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
     uint64_t run = block_exclusive_scan(loc, s_scan, &total);
     const int ntiles = static_cast<int>(total & 0xffffffffu);
     bad = bad || static_cast<int>(total >> 32) != A || ntiles + ceil_div(T, bn) > cap;
-    if (bad && c == 0 && threadIdx.x == 0) set_device_error(err, MOE_DEV_BAD_INDEX);
+    if (bad && threadIdx.x == 0) set_device_error(err, MOE_DEV_BAD_WORKSPACE);
     for (int e = e0; e < e1 && !bad; ++e) {
       const int cnt = s_tot[e];
       const int off = static_cast<int>(run >> 32), tile0 = static_cast<int>(run & 0xffffffffu);
@@ -283,7 +284,10 @@ int route_chunk_tokens(int T) {
 
 bool route_use_small(int T, int k) { return T * k <= 1024; }
 
-// Multi-CTA path: per-chunk counts [nch][E], then 4 ints of counters (zero between calls).
+// Multi-CTA path: per-chunk counts [nch][E] at the start of the workspace; 4 ints
+// of counters (zero between calls) in its last 16 bytes, wherever the counts of
+// a call with another T ended, so that a larger earlier call cannot leave counts
+// where a smaller later one keeps its counters.
 size_t route_workspace_bytes(int T, int E, int k) {
   if (route_use_small(T, k)) return 0;
   int tc = route_chunk_tokens(T);
@@ -294,7 +298,7 @@ unsigned long long wait_limit_ns();
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32_t* ids, float* w,
                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm,
-                         int32_t* nb, void* ws, cudaStream_t s) {
+                         int32_t* nb, void* ws, size_t ws_bytes, cudaStream_t s) {
   int* err = device_error_ptr();
   if (route_use_small(T, k)) {
     size_t sm = static_cast<size_t>(33) * E * sizeof(int);
@@ -308,7 +312,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
   const int tc = route_chunk_tokens(T);
   const int nch = ceil_div(T, tc);
   int32_t* cc = static_cast<int32_t*>(ws);
-  int* ctr = reinterpret_cast<int*>(cc + static_cast<size_t>(nch) * E);
+  int* ctr = reinterpret_cast<int*>(static_cast<char*>(ws) + ((ws_bytes - 16) & ~static_cast<size_t>(3)));
   const size_t sm = static_cast<size_t>(10) * E * sizeof(int);
   if (sm > 48 * 1024) {
     cudaError_t e0 = cudaFuncSetAttribute(route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -393,7 +397,7 @@ extern "C" int moe_route_noalloc(const float* logits, int T, int E, int k, int b
   }
   if (!moe::device_error_ptr()) return MOE_ERR_CUDA;
   const cudaError_t e = moe::launch_route(logits, T, E, k, block_n, topk_ids, topk_w, counts, offsets, perm,
-                                          inv_perm, block_map, num_blocks, scratch,
+                                          inv_perm, block_map, num_blocks, scratch, kRouteScratchBytes,
                                           reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -58,7 +58,10 @@ enum {
   MOE_DEV_OK = 0,
   MOE_DEV_BAD_BLOCK = 1,  /* a block-map entry outside [0, E] x [0, A+T) */
   MOE_DEV_BAD_INDEX = 2,  /* a permutation entry outside [0, A) */
-  MOE_DEV_TIMEOUT = 3     /* a bounded device wait ran out */
+  MOE_DEV_TIMEOUT = 3,    /* a bounded device wait ran out */
+  MOE_DEV_BAD_WORKSPACE = 4 /* a routing or decode workspace was not zero-filled when the call
+                               began (a barrier counter already counted, or per-expert totals
+                               that cannot come from this call); nothing was written from them */
 };
 
 /* GEMM modes. */
@@ -108,8 +111,13 @@ size_t moe_route_workspace_size(int T, int E, int k, int block_n);
  *                             *num_blocks rows are written
  * num_blocks int32  [1]       number of tiles (device memory)
  * workspace  device scratch of at least moe_route_workspace_size() bytes,
- *            zero-filled by the caller before its first use (its last 16 bytes
- *            hold counters that every call leaves at zero).
+ *            zero-filled by the caller before its first use: the per-chunk
+ *            counts go at its start, and its last 16 bytes (of workspace_bytes)
+ *            hold counters that every call leaves at zero, so one workspace
+ *            serves calls with any T it is large enough for.  A workspace
+ *            whose counters are not zero when a call begins is reported as
+ *            MOE_DEV_BAD_WORKSPACE; no output is written from counts that do
+ *            not add up.
  * block_n    1..1024.
  */
 int moe_route(const float* logits, int T, int E, int k, int block_n,

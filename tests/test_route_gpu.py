@@ -103,3 +103,83 @@ def test_route_deterministic():
     b = run_route(tok["logits"], 8, 256)
     for n in a:
         assert np.array_equal(a[n], b[n]), n
+
+
+def test_route_reports_a_workspace_that_was_not_zeroed():
+    """A workspace holding stale bytes (here 0x01 in every byte: the barrier counter already
+    past the chunk count, per-chunk counts that cannot come from the call) makes moe_route
+    report MOE_DEV_BAD_WORKSPACE.  Without the barrier the chunks' counts may or may not be
+    complete when they are summed; a CTA that finds them inconsistent writes nothing from them,
+    one that finds them complete writes the true result, so every output entry is either
+    untouched or in range.  With a zero-filled workspace the outputs are exact again."""
+    import torch
+    from bit_mixture_experts_gb300 import _lib
+    dev = G.torch_dev()
+    wl = workloads.WORKLOADS["prefill512"]
+    tok = workloads.make_tokens(wl.shape, wl.T, 0, wl.skew)
+    T, E, k, bn = wl.T, wl.shape.E, wl.shape.k, 64
+    logits = torch.from_numpy(np.ascontiguousarray(tok["logits"], np.float32)).to(dev)
+    A = T * k
+    cap = _lib.moe_block_map_capacity(T, E, k, bn)
+    o = {"topk_ids": torch.full((T, k), -7, dtype=torch.int32, device=dev),
+         "topk_w": torch.full((T, k), -1.0, dtype=torch.float32, device=dev),
+         "counts": torch.full((E,), -7, dtype=torch.int32, device=dev),
+         "offsets": torch.full((E + 1,), -7, dtype=torch.int32, device=dev),
+         "perm": torch.full((A,), -7, dtype=torch.int32, device=dev),
+         "inv_perm": torch.full((A,), -7, dtype=torch.int32, device=dev),
+         "block_map": torch.full((cap, 3), -7, dtype=torch.int32, device=dev),
+         "num_blocks": torch.full((1,), -7, dtype=torch.int32, device=dev)}
+    names = ("topk_ids", "topk_w", "counts", "offsets", "perm", "inv_perm", "block_map", "num_blocks")
+    wsb = max(_lib.moe_route_workspace_size(T, E, k, bn), 16)
+    assert wsb > 16  # the multi-CTA path, which has the barrier
+    _lib.moe_get_device_error()  # clear
+    ws = torch.full((wsb,), 1, dtype=torch.uint8, device=dev)
+    _lib.moe_route(logits, k, bn, *(o[n] for n in names), ws)
+    torch.cuda.synchronize()
+    assert _lib.moe_get_device_error() == 4  # MOE_DEV_BAD_WORKSPACE
+    perm = o["perm"].cpu().numpy()
+    assert np.all((perm == -7) | ((perm >= 0) & (perm < A)))
+    nb = int(o["num_blocks"].item())
+    assert nb == -7 or 0 < nb <= cap
+    ws.zero_()
+    _lib.moe_route(logits, k, bn, *(o[n] for n in names), ws)
+    torch.cuda.synchronize()
+    assert _lib.moe_get_device_error() == 0
+    ref = moe_ref.route(tok["logits"], k, bn)
+    assert np.array_equal(o["perm"].cpu().numpy(), ref["perm"])
+    assert int(o["num_blocks"].item()) == ref["num_blocks"]
+
+
+def test_route_one_workspace_for_two_token_counts():
+    """One zero-filled workspace sized for 4096 tokens serves a 4096-token call and then a
+    512-token call: the counters sit in the workspace's last 16 bytes, away from the per-chunk
+    counts the larger call left behind."""
+    import torch
+    from bit_mixture_experts_gb300 import _lib
+    dev = G.torch_dev()
+    shape = workloads.FULL
+    E, k, bn = shape.E, shape.k, 128
+    ws = torch.zeros(_lib.moe_route_workspace_size(4096, E, k, bn), dtype=torch.uint8, device=dev)
+    names = ("topk_ids", "topk_w", "counts", "offsets", "perm", "inv_perm", "block_map", "num_blocks")
+    _lib.moe_get_device_error()
+    for T in (4096, 512):
+        tok = workloads.make_tokens(shape, T, seed=3)
+        A = T * k
+        cap = _lib.moe_block_map_capacity(T, E, k, bn)
+        o = {"topk_ids": torch.full((T, k), -7, dtype=torch.int32, device=dev),
+             "topk_w": torch.full((T, k), -1.0, dtype=torch.float32, device=dev),
+             "counts": torch.full((E,), -7, dtype=torch.int32, device=dev),
+             "offsets": torch.full((E + 1,), -7, dtype=torch.int32, device=dev),
+             "perm": torch.full((A,), -7, dtype=torch.int32, device=dev),
+             "inv_perm": torch.full((A,), -7, dtype=torch.int32, device=dev),
+             "block_map": torch.full((cap, 3), -7, dtype=torch.int32, device=dev),
+             "num_blocks": torch.full((1,), -7, dtype=torch.int32, device=dev)}
+        logits = torch.from_numpy(np.ascontiguousarray(tok["logits"], np.float32)).to(dev)
+        _lib.moe_route(logits, k, bn, *(o[n] for n in names), ws)
+        torch.cuda.synchronize()
+        assert _lib.moe_get_device_error() == 0
+        ref = moe_ref.route(tok["logits"], k, bn)
+        assert np.array_equal(o["perm"].cpu().numpy(), ref["perm"])
+        nb = int(o["num_blocks"].item())
+        assert nb == ref["num_blocks"]
+        assert np.array_equal(o["block_map"].cpu().numpy()[:nb], ref["block_map"])
