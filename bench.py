@@ -2,14 +2,17 @@
 """Benchmark of the W4 MoE FFN layer forward (routing + grouped GEMMs + combine).
 
 One step = one pass of the whole hot path over one batch of synthetic tokens:
-moe_route -> gate/up GEMM (+SwiGLU) -> down GEMM (+weighted combine) ->
-moe_combine.  The default workload is the 512-token prefill through the
-full-width layer (H=2048, 256 experts top-8 + 1 shared, F=512).  Weights
-(455 MB packed) exceed the 126 MB L2, so every step streams them from HBM.
+moe_route -> gate/up GEMM (+SwiGLU) -> down GEMM -> moe_combine (at decode
+sizes the fused decode kernel runs all four in one launch).  The default
+workload is the 512-token prefill through the full-width layer (H=2048, 256
+experts top-8 + 1 shared, F=512).  Weights (455 MB packed) exceed the 126 MB
+L2, so every step streams them from HBM; decode workloads flush L2 between
+steps instead.  The timed steps replay a CUDA graph of the layer call.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload prefill512|prefill4k|decode1|decode8|skew16k|tiny]
-                  [--kernels auto|tc|simt|gemv] [--no-extra]
+                  [--kernels auto|tc|simt|gemv] [--block-n B] [--no-cpu-baseline]
+                  [--no-e2e] [--no-graph]
 
 Under torchrun each rank runs the same workload on its own GPU with its own
 tokens (weak scaling, no collective on the data path); rank 0 prints one JSON
@@ -474,7 +477,6 @@ def main():
     ap.add_argument("--block-n", type=int, default=None, help="rows per GEMM tile (default: per kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a captured CUDA graph")
     args = ap.parse_args()
 
