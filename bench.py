@@ -445,6 +445,9 @@ def run_reference(args):
     wl = workloads.WORKLOADS[args.workload]
     d = workloads.make_workload(wl, seed=0)
     n = oracle_sample_tokens(wl)
+    # warm-up: W untimed runs of the same code on one token each (imports, BLAS threads, caches)
+    for _ in range(max(0, args.warmup)):
+        time_oracle(d, 1)
     vals = []
     t0 = time.perf_counter()
     for _ in range(max(1, args.steps)):   # each step one bounded sample; stop after ~90 s of CPU work
@@ -457,7 +460,7 @@ def run_reference(args):
     cb["value"] = v
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
-        "steps": len(vals), "warmup": 0, "ms_per_step": 1e3 * n / v, "higher_is_better": True, "scaling": "weak",
+        "steps": len(vals), "warmup": max(0, args.warmup), "ms_per_step": 1e3 * n / v, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": {"workload": wl.name, "desc": wl.desc, "T": wl.T, "sample_tokens": n},
         "cpu_baseline": cb,
