@@ -74,34 +74,6 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
-// Groups of this thread's row of one item from its slots (see the GEMV kernel).
-template <int N0, int NT, bool COHERENT>
-__device__ __forceinline__ void dec_item_dot(const uint4* swq, const uint32_t* swsb, const uint16_t* act,
-                                             const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
-                                             float (&acc)[GV_MAXN][GV_NACC]) {
-#pragma unroll 1
-  for (int i = 0; i < G; ++i) {
-    const int kg = warp + GV_WARPS * i;
-    if (kg >= KT) break;
-    group_dot<N0, NT, COHERENT>(swq[(2 * i) * GV_THREADS], swq[(2 * i + 1) * GV_THREADS], swsb[i * GV_THREADS],
-                                act + kg * KG, xoff, acc);
-  }
-}
-
-template <bool COHERENT>
-__device__ __forceinline__ void dec_dot(int nrow, const uint4* swq, const uint32_t* swsb, const uint16_t* act,
-                                        const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
-                                        float (&acc)[GV_MAXN][GV_NACC]) {
-  if (nrow == 1) {
-    dec_item_dot<0, 1, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
-  } else if (nrow == 2) {
-    dec_item_dot<0, 2, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
-  } else {
-    dec_item_dot<0, 4, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
-    if (nrow > 4) dec_item_dot<4, 4, COHERENT>(swq, swsb, act, xoff, warp, KT, G, acc);
-  }
-}
-
 // Small-batch routing (at most 64 assignments, T <= bn so that every expert's
 // rows form one tile), by warps 0 and 1, thread a = assignment a: its
 // permuted row is its rank among the keys (expert, assignment) -- by expert,
@@ -362,30 +334,22 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
     const int ipt = down ? IPT1 : IPT0;
     const int tile = u / ipt, j = u - tile * ipt;
     const int row0 = s_tile[tile][1], nrow = s_tile[tile][2];
-    // activation row of each tile row (gate/up: x of the row's token; down: the row of h)
-    uint32_t xoff[GV_MAXN];
-#pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n) {
-      const int r = row0 + (n < nrow ? n : 0);
-      xoff[n] = down ? static_cast<uint32_t>(r) * static_cast<uint32_t>(F)
-                     : static_cast<uint32_t>(s_tok[r]) * static_cast<uint32_t>(H);
-    }
-    float acc[GV_MAXN][GV_NACC];
-#pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n)
-#pragma unroll
-      for (int c = 0; c < GV_NACC; ++c) acc[n][c] = 0.f;
+    // activation row of this lane's token column (gate/up: x of the row's token; down: the row of h);
+    // columns past the tile read the tile's first row
+    const int r = row0 + ((lane >> 2) < nrow ? (lane >> 2) : 0);
+    const uint32_t xo = down ? static_cast<uint32_t>(r) * static_cast<uint32_t>(F)
+                             : static_cast<uint32_t>(s_tok[r]) * static_cast<uint32_t>(H);
+    float d[2][4] = {};
     ptx::cp_async_wait<1>();  // this thread's copies of item q have landed
-    const uint4* swq = swq0 + buf * slot_q + tid;
-    const uint32_t* swsb = swsb0 + buf * slot_sb + tid;
-    if (down) dec_dot<true>(nrow, swq, swsb, p.h, xoff, warp, KT1, G, acc);
-    else dec_dot<false>(nrow, swq, swsb, p.x, xoff, warp, KT0, G, acc);
+    __syncwarp();             // ... and those of the warp's other lanes, whose rows this lane reads
+    const uint4* sw = swq0 + buf * slot_q + 32 * warp;
+    const uint32_t* ssbw = swsb0 + buf * slot_sb + 32 * warp;
+    if (down) item_mma<true>(sw, ssbw, p.h, xo, warp, lane, KT1, G, d);
+    else item_mma<false>(sw, ssbw, p.x, xo, warp, lane, KT0, G, d);
 
     // reduce the warps' partial sums (fixed order) and write the item's outputs
     float* spart = spart0 + buf * (GV_WARPS * GV_MAXN * 32);
-#pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n)
-      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + lane] = acc_total(acc[n]);
+    store_partials(spart, d, warp, lane, nrow);
     __syncthreads();
     if (!down) {
       if (tid < nrow * 16) {

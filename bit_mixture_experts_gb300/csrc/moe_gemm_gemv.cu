@@ -1,12 +1,12 @@
-// CUDA-core grouped GEMV over groupwise-affine 4-bit weights, for decode-sized
-// tiles (at most GV_MAXN token rows per block-map tile).
+// Grouped GEMV over groupwise-affine 4-bit weights, for decode-sized tiles (at
+// most GV_MAXN token rows per block-map tile).
 //
 // "Perplexity Open Sources Lily" (aitrending.vip), Technical Details: at batch
 // 1 every routed expert's weights are read once per token, so the layer is a
 // stream of the 8 + 1 selected experts' packed weights and the work per weight
-// is a handful of ALU operations.  There is nothing for the tensor cores to do
-// here; what matters is keeping that stream in flight on every SM and keeping
-// the chain of dependent steps per work item short.
+// is a handful of operations.  What matters is keeping that stream in flight
+// on every SM, spending few instructions per weight and keeping the chain of
+// dependent steps per work item short.
 //
 // Weights use the repacked layout of the tensor-core kernel (per matrix, per
 // 128-row M-tile, per 64-wide K group: [2 halves][128 rows][16 B] nibbles +
@@ -15,24 +15,27 @@
 //
 // Work item (persistent grid, GV_CTAS_PER_SM CTAs of 256 threads per SM; 32
 // weight rows per item so that a batch-1 layer still gives every CTA work):
-//   gate/up: (tile, 16 features): lanes 0-15 take the gate rows and lanes
-//            16-31 the up rows of those features (M-tiles 2j, 2j+1 of the
-//            repacked pair layout); warp w takes K groups w, w+8, ...
+//   gate/up: (tile, 16 features): rows 0-15 are the gate rows and rows 16-31
+//            the up rows of those features (M-tiles 2j, 2j+1 of the repacked
+//            pair layout); warp w takes K groups w, w+8, ...
 //   down:    (tile, 32 output channels); warp w takes K groups w, w+8, ...
-// Each thread owns one weight row of the item.  It copies its row's groups (36
-// bytes each) into its own shared-memory slots with cp.async one item ahead
-// (two slot buffers), so the next item's weights stream while this one is
-// computed, and it waits only for its own copies: no barrier guards the weight
-// stream.  The activations (a few rows, shared by every warp) are read straight
-// from global memory through L1 in the inner loop.  Each word is expanded to
-// bf16 pairs exactly as the tensor-core kernel does (w = bf16(q * scale +
-// bias), one fma.rn.bf16x2 per pair) and multiplied into FP32 accumulators with
-// mixed-precision FMAs (bf16 x bf16 -> FP32, full rate on the FMA pipe).  The
-// group loop is not unrolled and the token count is a template parameter
-// picked per tile (1, 2 or 4 rows per pass), which keeps the code small: a fully
-// unrolled version spent most of its time on instruction-cache misses.  The
-// warps' partial sums are added in shared memory in a fixed order (one barrier
-// per item; the partial-sum buffer alternates between items).
+// Thread r of a warp copies row r's groups (36 bytes each) into its own
+// shared-memory slots with cp.async one item ahead (two slot buffers), so the
+// next item's weights stream while this one is computed; it waits for its own
+// copies and a warp barrier makes the warp's rows visible to all its lanes
+// (no CTA barrier guards the weight stream).  The products run on the tensor
+// cores with mma.sync m16n8k16 (bf16 operands, FP32 accumulation): the item's
+// 32 rows are two 16-row A blocks and the tile's token rows (at most 8) the
+// columns of B, read straight from global memory through L1.  Each lane
+// expands only the weight pairs of its own A fragments, exactly as the
+// tensor-core kernel expands them (w = bf16(q * scale + bias), one
+// fma.rn.bf16x2 per pair), so every weight is expanded once per item whatever
+// the tile's row count; a first version multiplied on the FMA pipe with
+// bf16 x bf16 -> FP32 FMAs and spent more instructions converting their
+// operands than on the dequantisation (decode of 8 tokens: 76 -> 62 µs per
+// step with the MMAs).  The warps' partial sums are added in shared memory in
+// a fixed order (one barrier per item; the partial-sum buffer alternates
+// between items).
 #include "moe_common.cuh"
 #include "moe_ptx.cuh"
 #include "moe_gemv_dev.cuh"
@@ -55,22 +58,6 @@ struct GvParams {
   int T, H, F, E, k, bn, cap;
   int G;  // K groups per thread: ceil(K / 64 / 8)
 };
-
-// All of this thread's groups of one item from its slots (slot i of the
-// buffer: words at swq[2i], swq[2i+1], (scale, bias) at swsb[i]; one thread's
-// slots are GV_THREADS apart).
-template <int N0, int NT>
-__device__ __forceinline__ void item_dot(const uint4* swq, const uint32_t* swsb, const uint16_t* act,
-                                         const uint32_t (&xoff)[GV_MAXN], int warp, int KT, int G,
-                                         float (&acc)[GV_MAXN][GV_NACC]) {
-#pragma unroll 1
-  for (int i = 0; i < G; ++i) {
-    const int kg = warp + GV_WARPS * i;
-    if (kg >= KT) break;
-    group_dot<N0, NT>(swq[(2 * i) * GV_THREADS], swq[(2 * i + 1) * GV_THREADS], swsb[i * GV_THREADS], act + kg * KG,
-                  xoff, acc);
-  }
-}
 
 __device__ __forceinline__ bool gv_tile(const GvParams& p, int b, Tile* t) {
   t->expert = __ldg(p.block_map + 3 * b);
@@ -159,38 +146,22 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) gemv_kernel(const 
         tok_l = r - A;
       }
     }
-    // element offset of each row's activations in act (below 2^32: T x H and (A+T) x F are checked on the host)
-    uint32_t xoff[GV_MAXN];
-#pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n) {
-      const int tk = __shfl_sync(0xffffffffu, tok_l, n);
-      // MODE 0: token row of x (rows past the tile, or a bad index, read token 0); MODE 1: row of h
-      xoff[n] = MODE == 0 ? static_cast<uint32_t>(tk < 0 ? 0 : tk) * static_cast<uint32_t>(K)
-                          : static_cast<uint32_t>(t.row0 + (n < nrow ? n : 0)) * static_cast<uint32_t>(K);
-    }
-    float acc[GV_MAXN][GV_NACC];
-#pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n)
-#pragma unroll
-      for (int c = 0; c < GV_NACC; ++c) acc[n][c] = 0.f;
+    // element offset of the activations of this lane's token column (lane / 4) in act (below 2^32:
+    // T x H and (A+T) x F are checked on the host); columns past the tile read a valid row
+    const int col = lane >> 2;
+    const int tk = __shfl_sync(0xffffffffu, tok_l, col);
+    // MODE 0: token row of x (a bad index reads token 0); MODE 1: row of h
+    const uint32_t xo = MODE == 0 ? static_cast<uint32_t>(tk < 0 ? 0 : tk) * static_cast<uint32_t>(K)
+                                  : static_cast<uint32_t>(t.row0 + (col < nrow ? col : 0)) * static_cast<uint32_t>(K);
+    float d[2][4] = {};
     ptx::cp_async_wait<1>();  // this thread's copies of item u have landed
-    const uint4* swq = swq0 + buf * slot_q + threadIdx.x;
-    const uint32_t* swsb = swsb0 + buf * slot_sb + threadIdx.x;
-    if (nrow == 1) {
-      item_dot<0, 1>(swq, swsb, p.act, xoff, warp, KT, G, acc);
-    } else if (nrow == 2) {
-      item_dot<0, 2>(swq, swsb, p.act, xoff, warp, KT, G, acc);
-    } else {
-      // up to 4 rows per pass (more would spill registers); 5-8 rows expand the weights twice
-      item_dot<0, 4>(swq, swsb, p.act, xoff, warp, KT, G, acc);
-      if (nrow > 4) item_dot<4, 4>(swq, swsb, p.act, xoff, warp, KT, G, acc);
-    }
+    __syncwarp();             // ... and those of the warp's other lanes, whose rows this lane reads
+    item_mma<false>(swq0 + buf * slot_q + 32 * warp, swsb0 + buf * slot_sb + 32 * warp, p.act, xo, warp, lane, KT,
+                    G, d);
 
     // reduce the warps' partial sums (fixed order) and finish the item
     float* spart = spart0 + buf * (GV_WARPS * GV_MAXN * 32);
-#pragma unroll
-    for (int n = 0; n < GV_MAXN; ++n)
-      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + lane] = acc_total(acc[n]);
+    store_partials(spart, d, warp, lane, nrow);
     __syncthreads();
     if (MODE == 0) {
       if (threadIdx.x < nrow * 16) {

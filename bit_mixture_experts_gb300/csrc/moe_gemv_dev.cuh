@@ -1,4 +1,4 @@
-// Device helpers of the CUDA-core GEMV over repacked 4-bit weights, shared by
+// Device helpers of the decode GEMV over repacked 4-bit weights, shared by
 // the GEMV kernel and the fused decode kernel (see moe_gemm_gemv.cu).
 #pragma once
 #include "moe_common.cuh"
@@ -16,57 +16,86 @@ constexpr int TC_M = 128;
 constexpr int W_PACKED = TC_M * 32;
 constexpr int W_BLOCK = W_PACKED + TC_M * 4;
 
-// bf16 pair of weights (element 2j in the low half, 2j+1 in the high half) of
-// a repacked word: 128 + q exactly, minus 128, times scale plus bias, rounded once.
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t word, int j, uint32_t s2, uint32_t b2) {
+// bf16 pair of weights sh / 4 of a repacked word (element 2j in the low half,
+// 2j + 1 in the high half, j = sh / 4): 128 + q exactly, minus 128, times scale
+// plus bias, rounded once.
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t word, int sh, uint32_t s2, uint32_t b2) {
   constexpr uint32_t MAGIC = 0x43004300u;
-  uint32_t x = ((word >> (4 * j)) & 0x000f000fu) | MAGIC, r;
+  uint32_t x = ((word >> sh) & 0x000f000fu) | MAGIC, r;
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(MAGIC));
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(r), "r"(s2), "r"(b2));
   return r;
 }
 
-// acc += w.lo * x.lo + w.hi * x.hi (bf16 operands, FP32 accumulation, products exact)
-__device__ __forceinline__ void dot_pair(float& acc, uint32_t w2, uint32_t x2) {
-  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
-      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\tfma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
-      : "+f"(acc)
-      : "r"(w2), "r"(x2));
+// d += A (16 x 16, bf16, row-major fragments a0..a3) * B (16 x 8, bf16, b0, b1), FP32 accumulation.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Partial sums per token row: four independent chains (one per pair slot of a
-// word), so the FMAs of a row do not form one long dependent chain; they are
-// added in a fixed order at the end (acc_total).
-constexpr int GV_NACC = 4;
-
-__device__ __forceinline__ float acc_total(const float (&a)[GV_NACC]) { return (a[0] + a[1]) + (a[2] + a[3]); }
-
-// acc[n] += sum over one K group of w * x[n] for token rows n = N0 .. N0+NT-1:
-// the row's packed words (lo: K 0..31, hi: K 32..63 of the group), its
-// (scale, bias) and the group's activations of each row at xg + xoff[n]
-// (bf16, global; read through L1, or through L2 only when COHERENT, for
-// activations written earlier by the same kernel).
-template <int N0, int NT, bool COHERENT = false>
-__device__ __forceinline__ void group_dot(uint4 lo, uint4 hi, uint32_t sb, const uint16_t* xg,
-                                          const uint32_t (&xoff)[GV_MAXN], float (&acc)[GV_MAXN][GV_NACC]) {
-  const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
-  const uint32_t b2 = (sb >> 16) * 0x10001u;
-  const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+// One work item's share of warp `warp`: its K groups kg = warp + GV_WARPS * i
+// (i < G, kg < KT) of the item's 32 weight rows against the tile's token rows,
+// on the tensor cores (mma.sync m16n8k16, bf16 operands, FP32 accumulation).
+// Rows 0-15 and 16-31 of the item are the two 16-row A blocks; the tile's
+// token rows are the 8 columns of B (columns past the tile's rows read a valid
+// row and are ignored).  The weights come from the slots of the warp's 32
+// threads (thread 32 warp + r holds row r's group: words at sw[(2 i) *
+// GV_THREADS + r] and sw[(2 i + 1) * GV_THREADS + r], (scale, bias) at
+// ssbw[i * GV_THREADS + r]).  Lane (g, t) = (lane / 4, lane % 4) expands pair
+// t of every word of rows g, g + 8, 16 + g, 24 + g: for k-step m (16 K values)
+// its A registers are pair t of words 2m and 2m + 1 of two rows, which is the
+// fragment layout of K = 16m + 2t and 16m + 8 + 2t, and its B registers are
+// the activations of the same K for token column g, read from `act` at
+// element offset xo (+ 64 kg): no element is expanded twice and no
+// conversion of a product operand to FP32 is needed.  d[mb][0..3] receive
+// rows 16 mb + g (d0, d1) and 16 mb + g + 8 (d2, d3), columns 2t and 2t + 1.
+template <bool COHERENT>
+__device__ __forceinline__ void item_mma(const uint4* sw, const uint32_t* ssbw, const uint16_t* act, uint32_t xo,
+                                         int warp, int lane, int KT, int G, float (&d)[2][4]) {
+  const int g = lane >> 2, sh = 4 * (lane & 3);
+#pragma unroll 1
+  for (int i = 0; i < G; ++i) {
+    const int kg = warp + GV_WARPS * i;
+    if (kg >= KT) break;
+    // B: the activation pairs K = 8w + 2t (w = 0..7) of the group, token column g
+    const uint32_t* xp = reinterpret_cast<const uint32_t*>(act + xo + kg * KG) + (lane & 3);
+    uint32_t b[8];
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    uint32_t wp[4];
+    for (int w = 0; w < 8; ++w) b[w] = COHERENT ? __ldcg(xp + 4 * w) : __ldg(xp + 4 * w);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) wp[j] = dequant_pair(words[w], j, s2, b2);
+    for (int mb = 0; mb < 2; ++mb) {
+      const int r0 = 16 * mb + g, r1 = r0 + 8;
+      const uint4 lo0 = sw[(2 * i) * GV_THREADS + r0], hi0 = sw[(2 * i + 1) * GV_THREADS + r0];
+      const uint4 lo1 = sw[(2 * i) * GV_THREADS + r1], hi1 = sw[(2 * i + 1) * GV_THREADS + r1];
+      const uint32_t sb0 = ssbw[i * GV_THREADS + r0], sb1 = ssbw[i * GV_THREADS + r1];
+      const uint32_t s20 = (sb0 & 0xffffu) * 0x10001u, b20 = (sb0 >> 16) * 0x10001u;
+      const uint32_t s21 = (sb1 & 0xffffu) * 0x10001u, b21 = (sb1 >> 16) * 0x10001u;
+      const uint32_t w0[8] = {lo0.x, lo0.y, lo0.z, lo0.w, hi0.x, hi0.y, hi0.z, hi0.w};
+      const uint32_t w1[8] = {lo1.x, lo1.y, lo1.z, lo1.w, hi1.x, hi1.y, hi1.z, hi1.w};
 #pragma unroll
-    for (int n = N0; n < N0 + NT; ++n) {
-      const uint4* xp = reinterpret_cast<const uint4*>(xg + xoff[n]) + w;
-      const uint4 x = COHERENT ? __ldcg(xp) : __ldg(xp);
-      dot_pair(acc[n][0], wp[0], x.x);
-      dot_pair(acc[n][1], wp[1], x.y);
-      dot_pair(acc[n][2], wp[2], x.z);
-      dot_pair(acc[n][3], wp[3], x.w);
+      for (int m = 0; m < 4; ++m)
+        mma_16816(d[mb], dequant_pair(w0[2 * m], sh, s20, b20), dequant_pair(w1[2 * m], sh, s21, b21),
+                  dequant_pair(w0[2 * m + 1], sh, s20, b20), dequant_pair(w1[2 * m + 1], sh, s21, b21), b[2 * m],
+                  b[2 * m + 1]);
     }
   }
+}
+
+// The warp's partial sums of one item into spart[(warp * GV_MAXN + n) * 32 + row] for the
+// tile's token rows n < nrow (the layout the items' reductions read).
+__device__ __forceinline__ void store_partials(float* spart, const float (&d)[2][4], int warp, int lane, int nrow) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = 2 * t + (e & 1), row = 16 * mb + g + 8 * (e >> 1);
+      if (n < nrow) spart[(warp * GV_MAXN + n) * 32 + row] = d[mb][e];
+    }
 }
 
 // Weight row of item j of a tile for this lane: (M-tile, row within it).

@@ -75,7 +75,7 @@ enum {
   MOE_IMPL_AUTO = 0,      /* GEMV when block_n <= 8, else the tensor-core kernel */
   MOE_IMPL_SIMT = 1,      /* CUDA-core tiled kernel (canonical weight layout) */
   MOE_IMPL_TC = 2,        /* tcgen05 kernel (repacked weight layout) */
-  MOE_IMPL_GEMV = 3       /* CUDA-core decode kernel (repacked weight layout) */
+  MOE_IMPL_GEMV = 3       /* decode GEMV kernel, mma.sync (repacked weight layout) */
 };
 
 /* ------------------------------------------------------------------------ */
