@@ -16,9 +16,9 @@ constexpr int TC_M = 128;
 constexpr int W_PACKED = TC_M * 32;
 constexpr int W_BLOCK = W_PACKED + TC_M * 4;
 
-// bf16 pair of weights sh / 4 of a repacked word (element 2j in the low half,
-// 2j + 1 in the high half, j = sh / 4): 128 + q exactly, minus 128, times scale
-// plus bias, rounded once.
+// Weight pair j = sh / 4 of a repacked word as bf16x2 (element 2j in the low
+// half, 2j + 1 in the high half): 128 + q exactly, minus 128, times scale plus
+// bias, rounded once.
 __device__ __forceinline__ uint32_t dequant_pair(uint32_t word, int sh, uint32_t s2, uint32_t b2) {
   constexpr uint32_t MAGIC = 0x43004300u;
   uint32_t x = ((word >> sh) & 0x000f000fu) | MAGIC, r;
