@@ -87,3 +87,63 @@ def test_combine_argument_errors(lib):
     assert lib.moe_combine(p, p, p, p, 4, 128, 33, None) == -3      # k > 32
     assert lib.moe_combine(None, p, p, p, 4, 128, 2, None) == -1
     assert lib.moe_combine(p, p, ctypes.c_void_p(20), p, 4, 128, 2, None) == -2
+
+
+def test_repacked_bytes(lib):
+    # one 4608-byte block (2 halves x 128 rows x 16 B of nibbles, then 128 x (scale, bias)) per
+    # 128-row tile and 64-wide K group: exactly the bytes of the canonical layout of the matrix
+    assert lib.moe_repacked_bytes(1, 128, 64) == 4608
+    assert lib.moe_repacked_bytes(1, 1024, 2048) == 1_179_648     # gate/up of one expert, H=2048 F=512
+    assert lib.moe_repacked_bytes(1, 2048, 512) == 589_824        # down of one expert
+    for n, rows, K in ((3, 1024, 2048), (17, 256, 256), (2, 2048, 512)):
+        canonical = rows * (K // 8) * 4 + 2 * rows * (K // 64) * 2   # packed words + bf16 scale and bias
+        assert lib.moe_repacked_bytes(n, rows, K) == n * canonical
+    assert lib.moe_repacked_bytes(1, 100, 2048) == 0
+    assert lib.moe_repacked_bytes(1, 128, 96) == 0
+    assert lib.moe_repacked_bytes(0, 128, 64) == 0
+
+
+def test_decode_workspace_size(lib):
+    for T in range(1, 9):
+        n = lib.moe_decode_workspace_size(T, 2048)
+        assert n > 0 and n % 4 == 0
+    assert lib.moe_decode_workspace_size(0, 2048) == 0
+    assert lib.moe_decode_workspace_size(9, 2048) == 0          # above the fused path's 8 tokens
+
+
+def test_repack_argument_errors(lib):
+    p = ctypes.c_void_p(256)
+    rp = lambda rows, K, gate_up, ptr=p: lib.moe_repack_w4(ptr, ptr, ptr, 2, rows, K, gate_up, ptr, None)
+    assert rp(100, 2048, 0) == -3
+    assert rp(128, 96, 0) == -3
+    assert rp(128, 2048, 1) == -3       # gate/up tile pairs need rows / 2 % 128 == 0
+    assert rp(256, 2048, 1, ptr=None) == -1
+    assert rp(256, 2048, 1, ptr=ctypes.c_void_p(264)) == -2
+
+
+def test_route_noalloc_argument_errors(lib):
+    p = ctypes.c_void_p(16)
+    r = lambda T=8, E=16, k=2, bn=128, ptr=p: lib.moe_route_noalloc(ptr, T, E, k, bn, *([ptr] * 8), None)
+    assert r(T=0) == -3
+    assert r(k=17, E=16) == -3
+    assert r(bn=0) == -3
+    assert r(ptr=None) == -1
+    assert r(ptr=ctypes.c_void_p(8)) == -2
+    # per-chunk counts of 256 chunks x 1024 experts exceed the library's fixed 256 KiB array
+    assert lib.moe_route_workspace_size(1 << 20, 1024, 8, 128) > 256 * 1024
+    assert r(T=1 << 20, E=1024, k=8) == -4
+
+
+def test_layer_forward_argument_errors(lib):
+    from bit_mixture_experts_gb300 import _lib
+    p = 256
+    w = _lib.Weights(p, None, None, p, None, None)
+    small_ws = _lib.Buffers(*([p] * 10), p, 0, p, 1)            # decode workspace of 1 byte
+    fwd = lambda T, H, bufs, weights=w: lib.moe_layer_forward(
+        ctypes.c_void_p(p), ctypes.c_void_p(p), ctypes.c_void_p(p), T, H, 512, 256, 8, 8, 3,
+        ctypes.byref(weights) if weights is not None else None, ctypes.byref(bufs) if bufs is not None else None,
+        None)
+    assert fwd(1, 2048, None) == -1
+    assert fwd(1, 2048, small_ws, weights=None) == -1
+    assert fwd(1, 100, small_ws) == -3                          # H % 64 on the fused decode path
+    assert fwd(1, 2048, small_ws) == -4                         # decode workspace below its size
