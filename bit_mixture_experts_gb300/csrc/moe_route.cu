@@ -303,7 +303,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
   if (route_use_small(T, k)) {
     size_t sm = static_cast<size_t>(33) * E * sizeof(int);
     if (sm > 48 * 1024) {
-      cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
+      const cudaError_t e0 = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(sm));
+      if (e0 != cudaSuccess) return e0;
     }
     route_small_kernel<<<1, 1024, sm, s>>>(logits, T, E, k, bn, ids, w, counts, offsets, perm, inv_perm, bm, nb);
     note_launches(1);
@@ -373,27 +375,28 @@ void* route_scratch_address() {
   return addr[dev];
 }
 
-bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" int moe_route_noalloc(const float* logits, int T, int E, int k, int block_n, int32_t* topk_ids,
                                  float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm,
                                  int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks,
                                  moe_stream_t stream) {
-  if (T < 1 || T > (1 << 20) || E < 1 || E > 1024 || k < 1 || k > 32 || k > E || block_n < 1 || block_n > 1024)
-    return MOE_ERR_SHAPE;
-  const void* ptrs[] = {logits, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks};
-  for (const void* q : ptrs)
-    if (!q) return MOE_ERR_NULL;
-  for (const void* q : ptrs)
-    if (!aligned16(q)) return MOE_ERR_ALIGN;
+  int rc = moe::check_route_shape(T, E, k, block_n);
+  if (rc) return rc;
+  rc = moe::check_ptrs(logits, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks);
+  if (rc) return rc;
   const size_t need = moe::route_workspace_bytes(T, E, k);
   if (need > kRouteScratchBytes) return MOE_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (need > 0) {
     scratch = route_scratch_address();
     if (!scratch) return MOE_ERR_CUDA;
+    // The grid barrier's counters (the array's last 16 bytes) are cleared before every multi-CTA
+    // call, in stream order: a call that overlapped another one on the GPU, or one whose barrier
+    // gave up, cannot leave them counted for the calls after it.
+    if (cudaMemsetAsync(static_cast<char*>(scratch) + kRouteScratchBytes - 16, 0, 16,
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
   }
   if (!moe::device_error_ptr()) return MOE_ERR_CUDA;
   const cudaError_t e = moe::launch_route(logits, T, E, k, block_n, topk_ids, topk_w, counts, offsets, perm,

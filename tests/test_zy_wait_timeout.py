@@ -3,8 +3,8 @@ kernels' waits take makes them run out.  The layer call must come back with
 MOE_DEV_TIMEOUT in the device error word (no hang, no trap), and the same
 context must give correct results again once the limit is restored.
 
-Collected last (file name) so that the short limit, restored in a finally
-block, cannot leak into other tests."""
+Collected after the other layer tests (file name) and the short limit is
+restored in a finally block, so it cannot leak into other tests."""
 import numpy as np
 import pytest
 
