@@ -20,8 +20,8 @@ ERRORS = {-1: "MOE_ERR_NULL", -2: "MOE_ERR_ALIGN", -3: "MOE_ERR_SHAPE", -4: "MOE
 DEVICE_ERRORS = {0: "ok", 1: "MOE_DEV_BAD_BLOCK", 2: "MOE_DEV_BAD_INDEX", 3: "MOE_DEV_TIMEOUT", 4: "MOE_DEV_BAD_WORKSPACE"}
 
 GATE_UP, DOWN = 0, 1
-IMPL_AUTO, IMPL_SIMT, IMPL_TC, IMPL_GEMV = 0, 1, 2, 3
-IMPLS = {"auto": IMPL_AUTO, "simt": IMPL_SIMT, "tc": IMPL_TC, "gemv": IMPL_GEMV}
+IMPL_AUTO, IMPL_TC, IMPL_GEMV = 0, 2, 3
+IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV}
 
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
 SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
@@ -39,7 +39,7 @@ _vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 
 
 class Weights(ctypes.Structure):
-    _fields_ = [("w13", _vp), ("s13", _vp), ("b13", _vp), ("w2", _vp), ("s2", _vp), ("b2", _vp)]
+    _fields_ = [("w13", _vp), ("w2", _vp)]
 
 
 class Buffers(ctypes.Structure):
@@ -57,7 +57,7 @@ _SIGS = {
     "moe_route_noalloc": ([_vp, _i, _i, _i, _i] + [_vp] * 9, _i),
     "moe_repacked_bytes": ([_i, _i, _i], _sz),
     "moe_repack_w4": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
-    "moe_expert_gemm_w4": ([_i, _i, _vp, _i, _i, _i, _i, _i] + [_vp] * 7 + [_i, _vp, _vp], _i),
+    "moe_expert_gemm_w4": ([_i, _i, _vp, _i, _i, _i, _i, _i] + [_vp] * 5 + [_i, _vp, _vp], _i),
     "moe_combine": ([_vp, _vp, _vp, _vp, _i, _i, _i, _vp], _i),
     "moe_decode_workspace_size": ([_i, _i], _sz),
     "moe_layer_forward": ([_vp, _vp, _vp] + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
@@ -151,10 +151,10 @@ def moe_repack_w4(packed, scale, bias, gate_up, out, stream=None):
           _stream(stream))
 
 
-def moe_expert_gemm_w4(mode, impl, act, T, H, F, E, k, w_packed, w_scale, w_bias, perm, topk_w, block_map,
-                       num_blocks, block_n, out, stream=None):
-    _call("moe_expert_gemm_w4", mode, impl, _ptr(act), T, H, F, E, k, _ptr(w_packed), _ptr(w_scale), _ptr(w_bias),
-          _ptr(perm), _ptr(topk_w), _ptr(block_map), _ptr(num_blocks), block_n, _ptr(out), _stream(stream))
+def moe_expert_gemm_w4(mode, impl, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks, block_n, out,
+                       stream=None):
+    _call("moe_expert_gemm_w4", mode, impl, _ptr(act), T, H, F, E, k, _ptr(w_packed), _ptr(perm), _ptr(topk_w),
+          _ptr(block_map), _ptr(num_blocks), block_n, _ptr(out), _stream(stream))
 
 
 def moe_combine(y, inv_perm, topk_w, out, stream=None):

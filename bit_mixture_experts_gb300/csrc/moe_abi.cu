@@ -1,7 +1,7 @@
 // extern "C" entry points of libmoe_w4.so: argument checks, the device error
 // word, and the launch sequence of the layer.  Every compute step runs in the
-// kernels of moe_route.cu, moe_gemm_simt.cu, moe_gemm_tc.cu and
-// moe_gemm_gemv.cu; nothing here touches tensor data on the host.
+// kernels of moe_route.cu, moe_gemm_tc.cu, moe_gemm_gemv.cu, moe_decode.cu and
+// moe_combine.cu; nothing here touches tensor data on the host.
 #include <atomic>
 #include <mutex>
 
@@ -48,10 +48,6 @@ size_t route_workspace_bytes(int T, int E, int k);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32_t* ids, float* w, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm, int32_t* nb, void* ws,
                          size_t ws_bytes, cudaStream_t s);
-cudaError_t launch_gemm_simt(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const uint32_t* wq,
-                             const uint16_t* ws, const uint16_t* wb, const int32_t* perm, const float* topk_w,
-                             const int32_t* block_map, const int32_t* num_blocks, int bn, int nb_cap, void* out,
-                             cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T,
                            int H, int k, int num_sms, cudaStream_t s);
 size_t repacked_bytes(int n_mat, int rows, int K);
@@ -75,26 +71,6 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
 void set_wait_limit_ns(unsigned long long ns);
 
 namespace {
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int check_shape(int T, int H, int F, int E, int k, int bn) {
-  if (T < 1 || T > (1 << 20)) return MOE_ERR_SHAPE;
-  if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return MOE_ERR_SHAPE;
-  if (H < 64 || H % 64 != 0 || F < 64 || F % 64 != 0) return MOE_ERR_SHAPE;
-  if (bn < 1 || bn > 1024) return MOE_ERR_SHAPE;
-  return MOE_OK;
-}
-
-template <typename... P>
-int check_ptrs(P... ps) {
-  const void* arr[] = {static_cast<const void*>(ps)...};
-  for (const void* p : arr)
-    if (!p) return MOE_ERR_NULL;
-  for (const void* p : arr)
-    if (!aligned16(p)) return MOE_ERR_ALIGN;
-  return MOE_OK;
-}
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -124,7 +100,7 @@ size_t moe_route_workspace_size(int T, int E, int k, int block_n) {
 int moe_route(const float* logits, int T, int E, int k, int block_n, int32_t* topk_ids, float* topk_w,
               int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* block_map,
               int32_t* num_blocks, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-  int rc = check_shape(T, 64, 64, E, k, block_n);
+  int rc = check_route_shape(T, E, k, block_n);
   if (rc) return rc;
   rc = check_ptrs(logits, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks);
   if (rc) return rc;
@@ -141,36 +117,26 @@ int moe_route(const float* logits, int T, int E, int k, int block_n, int32_t* to
 }
 
 int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,
-                       const void* w_packed, const uint16_t* w_scale, const uint16_t* w_bias, const int32_t* perm,
-                       const float* topk_w, const int32_t* block_map, const int32_t* num_blocks, int block_n,
-                       void* out, moe_stream_t stream) {
+                       const void* w_packed, const int32_t* perm, const float* topk_w, const int32_t* block_map,
+                       const int32_t* num_blocks, int block_n, void* out, moe_stream_t stream) {
   int rc = check_shape(T, H, F, E, k, block_n);
   if (rc) return rc;
   if (mode != MOE_GATE_UP_SWIGLU && mode != MOE_DOWN) return MOE_ERR_MODE;
   rc = check_ptrs(act, w_packed, perm, topk_w, block_map, num_blocks, out);
   if (rc) return rc;
+  if (impl == MOE_IMPL_AUTO) impl = block_n <= gemv_max_rows() ? MOE_IMPL_GEMV : MOE_IMPL_TC;
+  if (impl != MOE_IMPL_GEMV && impl != MOE_IMPL_TC) return MOE_ERR_MODE;
+  // both kernels step K and M by 128; the GEMV takes tiles of at most 8 rows, the tensor-core kernel 128
+  if (H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
+  if (block_n > (impl == MOE_IMPL_GEMV ? gemv_max_rows() : 128)) return MOE_ERR_SHAPE;
   if (!device_error_ptr()) return MOE_ERR_CUDA;
   const int cap = moe_block_map_capacity(T, E, k, block_n);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (impl == MOE_IMPL_AUTO) impl = block_n <= gemv_max_rows() ? MOE_IMPL_GEMV : MOE_IMPL_TC;
-  switch (impl) {
-    case MOE_IMPL_GEMV:
-      if (block_n > gemv_max_rows() || H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
-      return cuda_status(launch_gemm_gemv(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
-                                          block_n, cap, out, num_sms(), s));
-    case MOE_IMPL_TC:
-      if (block_n > 128 || H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
-      return cuda_status(launch_gemm_tc(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
+  if (impl == MOE_IMPL_GEMV)
+    return cuda_status(launch_gemm_gemv(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
                                         block_n, cap, out, num_sms(), s));
-    case MOE_IMPL_SIMT:
-      if (block_n > 128) return MOE_ERR_SHAPE;
-      rc = check_ptrs(w_scale, w_bias);
-      if (rc) return rc;
-      return cuda_status(launch_gemm_simt(mode, act, T, H, F, E, k, static_cast<const uint32_t*>(w_packed), w_scale,
-                                          w_bias, perm, topk_w, block_map, num_blocks, block_n, cap, out, s));
-    default:
-      return MOE_ERR_MODE;
-  }
+  return cuda_status(launch_gemm_tc(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
+                                    block_n, cap, out, num_sms(), s));
 }
 
 int moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T, int H,
@@ -210,11 +176,11 @@ int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out, int
   int rc = moe_route(logits, T, E, k, block_n, b->topk_ids, b->topk_w, b->counts, b->offsets, b->perm, b->inv_perm,
                      b->block_map, b->num_blocks, b->workspace, b->workspace_bytes, stream);
   if (rc) return rc;
-  rc = moe_expert_gemm_w4(MOE_GATE_UP_SWIGLU, impl, x, T, H, F, E, k, w->w13, w->s13, w->b13, b->perm, b->topk_w,
-                          b->block_map, b->num_blocks, block_n, b->h, stream);
+  rc = moe_expert_gemm_w4(MOE_GATE_UP_SWIGLU, impl, x, T, H, F, E, k, w->w13, b->perm, b->topk_w, b->block_map,
+                          b->num_blocks, block_n, b->h, stream);
   if (rc) return rc;
-  rc = moe_expert_gemm_w4(MOE_DOWN, impl, b->h, T, H, F, E, k, w->w2, w->s2, w->b2, b->perm, b->topk_w,
-                          b->block_map, b->num_blocks, block_n, b->y, stream);
+  rc = moe_expert_gemm_w4(MOE_DOWN, impl, b->h, T, H, F, E, k, w->w2, b->perm, b->topk_w, b->block_map,
+                          b->num_blocks, block_n, b->y, stream);
   if (rc) return rc;
   return moe_combine(b->y, b->inv_perm, b->topk_w, out, T, H, k, stream);
 }

@@ -22,6 +22,34 @@ void note_launches(int n);
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Host-side argument checks shared by the entry points (moe_abi.cu and the
+// no-allocation routing entry point in moe_route.cu), so their limits agree.
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Sizes every layer call must satisfy (the GEMM kernels add their own: H and
+// F multiples of 128, block_n within the chosen kernel's tile height).
+inline int check_shape(int T, int H, int F, int E, int k, int bn) {
+  if (T < 1 || T > (1 << 20)) return MOE_ERR_SHAPE;
+  if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E) return MOE_ERR_SHAPE;
+  if (H < 64 || H % 64 != 0 || F < 64 || F % 64 != 0) return MOE_ERR_SHAPE;
+  if (bn < 1 || bn > 1024) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+// Routing-only sizes (no H or F involved).
+inline int check_route_shape(int T, int E, int k, int bn) { return check_shape(T, 64, 64, E, k, bn); }
+
+// MOE_ERR_NULL for any null pointer, then MOE_ERR_ALIGN for any pointer not 16-byte aligned.
+template <typename... P>
+int check_ptrs(P... ps) {
+  const void* arr[] = {static_cast<const void*>(ps)...};
+  for (const void* p : arr)
+    if (!p) return MOE_ERR_NULL;
+  for (const void* p : arr)
+    if (!aligned16(p)) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
 // bf16 bits -> float (exact).
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);

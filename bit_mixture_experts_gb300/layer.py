@@ -9,7 +9,7 @@ import numpy as np
 
 from . import _lib
 
-DEFAULT_BLOCK_N = {_lib.IMPL_SIMT: 128, _lib.IMPL_TC: 128, _lib.IMPL_GEMV: 8}
+DEFAULT_BLOCK_N = {_lib.IMPL_TC: 128, _lib.IMPL_GEMV: 8}
 DECODE_MAX_T = 16  # token counts up to this take the GEMV kernel under impl="auto"
 
 
@@ -52,23 +52,15 @@ class MoELayerW4:
         self.H, self.E, self.k, self.F = H, E, k, F
         self.device = torch.device(device)
         self.impl = _lib.IMPLS[impl] if isinstance(impl, str) else int(impl)
-        if self.impl == _lib.IMPL_AUTO and not (H % 128 == 0 and F % 128 == 0):
-            # the tensor-core and GEMV kernels take K in steps of 128; other shapes use the tiled CUDA-core kernel
-            self.impl = _lib.IMPL_SIMT
+        if H % 128 or F % 128:
+            raise ValueError(f"H={H} and F={F} must be multiples of 128 (the kernels' K and M steps)")
         self.block_n = block_n  # None: chosen per token count by default_block_n
         _lib.load()
         w = {n: (v if isinstance(v, torch.Tensor) else _dev(v, self.device)) for n, v in weights.items()
              if n.startswith(("w13_", "w2_"))}
-        self.canonical = w
-        if self.impl == _lib.IMPL_SIMT:
-            self.weights = _lib.Weights(w["w13_packed"].data_ptr(), w["w13_scale"].data_ptr(),
-                                        w["w13_bias"].data_ptr(), w["w2_packed"].data_ptr(),
-                                        w["w2_scale"].data_ptr(), w["w2_bias"].data_ptr())
-            self._keep = w
-        else:
-            self.w13_r = self._repack(w["w13_packed"], w["w13_scale"], w["w13_bias"], gate_up=True)
-            self.w2_r = self._repack(w["w2_packed"], w["w2_scale"], w["w2_bias"], gate_up=False)
-            self.weights = _lib.Weights(self.w13_r.data_ptr(), None, None, self.w2_r.data_ptr(), None, None)
+        self.w13_r = self._repack(w["w13_packed"], w["w13_scale"], w["w13_bias"], gate_up=True)
+        self.w2_r = self._repack(w["w2_packed"], w["w2_scale"], w["w2_bias"], gate_up=False)
+        self.weights = _lib.Weights(self.w13_r.data_ptr(), self.w2_r.data_ptr())
         self._bufs = {}
 
     def _repack(self, packed, scale, bias, gate_up):

@@ -27,7 +27,8 @@
  * Sizes: T tokens, H hidden, E routed experts (the shared expert is index E of
  * every weight array), k experts per token, F expert FFN width, A = T*k
  * assignments, block_n rows per GEMM tile.  Limits: 1 <= k <= 32, k <= E,
- * E <= 1024, H % 64 == 0, F % 64 == 0, 1 <= T <= 2^20.
+ * E <= 1024, 1 <= T <= 2^20; the grouped GEMMs and the layer also need
+ * H % 128 == 0 and F % 128 == 0.
  */
 #ifndef MOE_W4_H
 #define MOE_W4_H
@@ -70,12 +71,15 @@ enum {
   MOE_DOWN = 1            /* y = bf16(h Wd^T) per routed row */
 };
 
-/* GEMM implementations. */
+/* GEMM kernels.  The layer has two regimes and one kernel for each: the
+ * tensor-core grouped GEMM for prefill-sized tiles and the GEMV for decode
+ * tiles of at most 8 token rows.  Both read the same repacked weights and
+ * compute the same values; AUTO picks by block_n, the others force one (the
+ * tests run each kernel over every shape it accepts). */
 enum {
   MOE_IMPL_AUTO = 0,      /* GEMV when block_n <= 8, else the tensor-core kernel */
-  MOE_IMPL_SIMT = 1,      /* CUDA-core tiled kernel (canonical weight layout) */
-  MOE_IMPL_TC = 2,        /* tcgen05 kernel (repacked weight layout) */
-  MOE_IMPL_GEMV = 3       /* decode GEMV kernel, mma.sync (repacked weight layout) */
+  MOE_IMPL_TC = 2,        /* tcgen05 kernel */
+  MOE_IMPL_GEMV = 3       /* decode GEMV kernel, mma.sync */
 };
 
 /* ------------------------------------------------------------------------ */
@@ -142,11 +146,12 @@ int moe_route(const float* logits, int T, int E, int k, int block_n,
  * For T*k <= 1024 no scratch is used.  Nothing is allocated or freed.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  The routing kernels overwrite every scratch
- * entry before reading it, so nothing needs clearing between calls, but all
- * calls share the one array: calls that can overlap on the GPU (different
- * streams, or different host threads) race and must be serialised by the
- * caller.
+ * before any stream capture.  Each call that uses the array first clears the
+ * counters of its grid barrier (16 bytes, cudaMemsetAsync on `stream`), and
+ * the routing kernel overwrites every count before reading it.  All calls
+ * share the one array: calls that can overlap on the GPU (different streams,
+ * or different host threads) race and must be serialised by the caller; a
+ * call after such a race, on its own, gives correct results again.
  */
 int moe_route_noalloc(const float* logits, int T, int E, int k, int block_n,
                       int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
@@ -158,7 +163,7 @@ int moe_route_noalloc(const float* logits, int T, int E, int k, int block_n,
 /* ------------------------------------------------------------------------ */
 
 /*
- * Canonical weight layout (what moe_repack_w4 reads and the SIMT kernel uses):
+ * Canonical weight layout (what moe_repack_w4 reads):
  *   packed uint32 [n_mat, rows, K/8]: K element 8*w+i in bits [4i, 4i+4) of word w
  *   scale, bias   bf16   [n_mat, rows, K/64]: w = bf16(q * scale + bias)
  * Gate/up matrices have rows = 2F (F gate rows, then F up rows) and K = H;
@@ -203,17 +208,17 @@ int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t*
  *   act  bf16 [A+T, F] the h of the gate/up call;
  *   out  bf16 [A+T, H]: y[r] = bf16(h[r] Wd^T) accumulated in FP32, in the
  *        same permuted row order (perm and topk_w are not read).
- * weights: canonical layout for MOE_IMPL_SIMT, repacked layout otherwise.
+ * w_packed: the matrix set in the repacked layout of moe_repack_w4 (packed
+ *        nibbles with each 64-group's bf16 scale and bias in the same block).
  * block_map / num_blocks: moe_route's outputs for the same block_n.
- * impl: MOE_IMPL_*.  AUTO takes GEMV for block_n <= 8 and TC otherwise
- * (both read the repacked layout).  TC needs block_n <= 128, H % 128 == 0
- * and F % 128 == 0; GEMV (decode: tiles of at most 8 token rows) needs
- * block_n <= 8, H % 128 == 0 and F % 128 == 0; SIMT needs block_n <= 128.
- * Returns MOE_ERR_SHAPE when the chosen kernel cannot take the shape.
+ * impl: MOE_IMPL_*.  AUTO takes GEMV for block_n <= 8 and TC otherwise.  TC
+ * needs block_n <= 128; GEMV (decode: tiles of at most 8 token rows) needs
+ * block_n <= 8; both need H % 128 == 0 and F % 128 == 0.  Returns
+ * MOE_ERR_SHAPE when the chosen kernel cannot take the shape and
+ * MOE_ERR_MODE for an unknown mode or impl.
  */
 int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,
-                       const void* w_packed, const uint16_t* w_scale, const uint16_t* w_bias,
-                       const int32_t* perm, const float* topk_w,
+                       const void* w_packed, const int32_t* perm, const float* topk_w,
                        const int32_t* block_map, const int32_t* num_blocks, int block_n,
                        void* out, moe_stream_t stream);
 
@@ -263,14 +268,11 @@ typedef struct {
  */
 size_t moe_decode_workspace_size(int T, int H);
 
-/* Weights of one layer: gate/up and down matrices of E+1 experts. */
+/* Weights of one layer: gate/up and down matrices of E+1 experts in the
+ * repacked layout of moe_repack_w4 (gate_up = 1 for w13, 0 for w2). */
 typedef struct {
-  const void* w13;        /* packed (canonical or repacked, matching impl) */
-  const uint16_t* s13;    /* canonical scale (SIMT only, else NULL) */
-  const uint16_t* b13;    /* canonical bias (SIMT only, else NULL) */
+  const void* w13;
   const void* w2;
-  const uint16_t* s2;
-  const uint16_t* b2;
 } moe_weights_t;
 
 /*

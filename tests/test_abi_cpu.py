@@ -72,12 +72,17 @@ def test_route_argument_errors(lib):
 def test_gemm_argument_errors(lib):
     p = ctypes.c_void_p(256)
     args = lambda mode, impl, H, F, bn, ptr=p: lib.moe_expert_gemm_w4(
-        mode, impl, ptr, 16, H, F, 8, 2, ptr, ptr, ptr, ptr, ptr, ptr, ptr, bn, ptr, None)
-    assert args(0, 1, 100, 64, 128) == -3       # H % 64
-    assert args(0, 1, 128, 96, 128) == -3       # F % 64
-    assert args(5, 1, 128, 64, 128) == -7       # mode
-    assert args(0, 1, 128, 64, 128, ptr=None) == -1
-    assert args(0, 1, 128, 64, 128, ptr=ctypes.c_void_p(260)) == -2
+        mode, impl, ptr, 16, H, F, 8, 2, ptr, ptr, ptr, ptr, ptr, bn, ptr, None)
+    assert args(0, 2, 100, 128, 128) == -3      # H % 64
+    assert args(0, 2, 128, 96, 128) == -3       # F % 64
+    assert args(0, 2, 192, 128, 128) == -3      # H % 128 (tensor-core kernel)
+    assert args(1, 3, 128, 192, 8) == -3        # F % 128 (GEMV kernel)
+    assert args(0, 2, 128, 128, 129) == -3      # tile height above the tensor-core kernel's 128
+    assert args(0, 3, 128, 128, 9) == -3        # tile height above the GEMV kernel's 8
+    assert args(5, 2, 128, 128, 128) == -7      # mode
+    assert args(0, 1, 128, 128, 128) == -7      # no kernel 1 (the CUDA-core GEMM is not part of the library)
+    assert args(0, 2, 128, 128, 128, ptr=None) == -1
+    assert args(0, 2, 128, 128, 128, ptr=ctypes.c_void_p(260)) == -2
 
 
 def test_combine_argument_errors(lib):
@@ -137,7 +142,7 @@ def test_route_noalloc_argument_errors(lib):
 def test_layer_forward_argument_errors(lib):
     from bit_mixture_experts_gb300 import _lib
     p = 256
-    w = _lib.Weights(p, None, None, p, None, None)
+    w = _lib.Weights(p, p)
     small_ws = _lib.Buffers(*([p] * 10), p, 0, p, 1)            # decode workspace of 1 byte
     fwd = lambda T, H, bufs, weights=w: lib.moe_layer_forward(
         ctypes.c_void_p(p), ctypes.c_void_p(p), ctypes.c_void_p(p), T, H, 512, 256, 8, 8, 3,
