@@ -10,11 +10,15 @@ L2, so every step streams them from HBM; decode workloads flush L2 between
 steps instead.  The timed steps replay a CUDA graph of the layer call.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload prefill512|prefill4k|decode1|decode8|skew16k|tiny]
-                  [--kernels auto|tc|simt|gemv] [--block-n B] [--no-cpu-baseline]
+                  [--workload prefill512|prefill4k|decode1|decode8|skew16k|tiny] [--only]
+                  [--kernels auto|tc|gemv] [--block-n B] [--no-cpu-baseline]
                   [--no-e2e] [--no-graph]
 
-Under torchrun each rank runs the same workload on its own GPU with its own
+The JSON line's top-level value is the chosen workload (default prefill512);
+unless --only is given, the other workloads of the metric (4K-token prefill,
+batch-1 and 8-token decode, the skewed 16K-token prefill) are timed the same
+way in the same run and reported under "workloads", each with its roofline.
+Under torchrun each rank runs the same workloads on its own GPU with its own
 tokens (weak scaling, no collective on the data path); rank 0 prints one JSON
 line.  `--impl reference` times the CPU oracle on a bounded sample instead.
 """
@@ -143,28 +147,32 @@ class ClockSampler:
 # --------------------------------------------------------------------------- #
 # our implementation
 # --------------------------------------------------------------------------- #
-def run_ours(args, rank, world, local_rank):
+EXTRA_WORKLOADS = ("prefill4k", "decode1", "decode8", "skew16k")
+
+
+def tensor_bound(T):
+    """Above ~2K tokens the gate/up GEMM does enough FLOP per weight byte to be tensor-core bound."""
+    return T >= 2048
+
+
+def measure_workload(args, wl, layer, d, rank, world, dev):
+    """Warm-up, a per-stage breakdown (eager launches with events), then the timed region: K replays of
+    the layer step captured once as a CUDA graph (L2 flushed between steps when the step's bytes fit in
+    L2), and the end-to-end number through moe_layer_forward_host.  Returns the workload's result."""
     import torch
 
-    from bit_mixture_experts_gb300 import _lib, build
-    from bit_mixture_experts_gb300.layer import MoELayerW4
+    from bit_mixture_experts_gb300 import _lib
 
-    build.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    wl = workloads.WORKLOADS[args.workload]
     s = wl.shape
     T = wl.T
-    d = workloads.make_workload(wl, seed=0, with_weights=True)
-    if rank:  # each rank its own tokens (weights are the same replica)
-        d.update(rank_tokens(s, T, rank, wl.skew))
-    layer = MoELayerW4(s.H, s.E, s.k, s.F, d, device=dev, impl=args.kernels, block_n=args.block_n)
-    x = torch.from_numpy(d["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
-    logits = torch.from_numpy(d["logits"]).to(dev)
+    tok = rank_tokens(s, T, rank, wl.skew) if rank else d
+    x = torch.from_numpy(tok["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.from_numpy(tok["logits"]).to(dev)
     out = torch.empty((T, s.H), dtype=torch.bfloat16, device=dev)
     b = layer.buffers(T)
     stream = torch.cuda.current_stream()
     impl, bn = layer.impl_for(T), layer.block_n_for(T)
+    w = layer.weights
 
     def step(ev=None):
         if ev is not None:
@@ -173,13 +181,12 @@ def run_ours(args, rank, world, local_rank):
                        b["inv_perm"], b["block_map"], b["num_blocks"], b["workspace"])
         if ev is not None:
             ev[1].record(stream)
-        w = layer.weights
-        _lib.moe_expert_gemm_w4(_lib.GATE_UP, impl, x, T, s.H, s.F, s.E, s.k, w.w13, w.s13, w.b13, b["perm"],
-                                b["topk_w"], b["block_map"], b["num_blocks"], bn, b["h"])
+        _lib.moe_expert_gemm_w4(_lib.GATE_UP, impl, x, T, s.H, s.F, s.E, s.k, w.w13, b["perm"], b["topk_w"],
+                                b["block_map"], b["num_blocks"], bn, b["h"])
         if ev is not None:
             ev[2].record(stream)
-        _lib.moe_expert_gemm_w4(_lib.DOWN, impl, b["h"], T, s.H, s.F, s.E, s.k, w.w2, w.s2, w.b2, b["perm"],
-                                b["topk_w"], b["block_map"], b["num_blocks"], bn, b["y"])
+        _lib.moe_expert_gemm_w4(_lib.DOWN, impl, b["h"], T, s.H, s.F, s.E, s.k, w.w2, b["perm"], b["topk_w"],
+                                b["block_map"], b["num_blocks"], bn, b["y"])
         if ev is not None:
             ev[3].record(stream)
         _lib.moe_combine(b["y"], b["inv_perm"], b["topk_w"], out)
@@ -210,19 +217,18 @@ def run_ours(args, rank, world, local_rank):
         step(events[i])
     torch.cuda.synchronize()
     seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)])
-    eager_ms = float(seg.sum(1).mean())
     assert _lib.moe_get_device_error() == 0, "device error word set"
 
-    # the step captured once as a CUDA graph (the library launches only on the given stream and
-    # never synchronises, so the whole layer is capturable); the timed region replays it
+    # the step captured once as a CUDA graph (the library launches only on the given stream and never
+    # synchronises, so the whole layer is capturable); the timed region replays it
     graph, per_step_launches = None, None
     if not args.no_graph:
         try:
             g = torch.cuda.CUDAGraph()
             n_cap = _lib.moe_launch_count()
             with torch.cuda.graph(g):
-                # the layer's public entry point (moe_layer_forward): at decode sizes with the
-                # GEMV kernel this is the fused single-launch decode kernel
+                # the layer's public entry point (moe_layer_forward): at decode sizes with the GEMV
+                # kernel this is the fused single-launch decode kernel
                 layer.forward(x, logits, out)
             per_step_launches = _lib.moe_launch_count() - n_cap
             g.replay()
@@ -235,120 +241,154 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank) if rank == 0 else None
-    time.sleep(0.3)
+    time.sleep(0.1)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     n0 = _lib.moe_launch_count()
-    if clocks:
-        clocks.mark_start()
     hold_stream()
     for i in range(args.steps):
         if flush is not None:
             flush.zero_()
+        ev[i][0].record(stream)
         if graph is not None:
-            ev[i][0].record(stream)
             graph.replay()
-            ev[i][1].record(stream)
         else:
-            ev[i][0].record(stream)
             layer.forward(x, logits, out)
-            ev[i][1].record(stream)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
-    if clocks:
-        clocks.mark_end()
     launches = (_lib.moe_launch_count() - n0) if graph is None else per_step_launches * args.steps
     if world > 1:
         torch.distributed.barrier()
-    if clocks:
-        clocks.stop()
-    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    ms = float(np.mean([a.elapsed_time(b_) for a, b_ in ev]))
     ms = max_over_ranks(ms, world, dev)
     assert _lib.moe_get_device_error() == 0, "device error word set"
 
-    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    # end to end through the C ABI with host buffers (pinned): H2D of x and logits, the layer, D2H of
+    # out and a stream synchronisation in each step's wall-clock window; the L2 flush between steps
+    # runs (and is waited for) outside the window
     e2e = None
     if not args.no_e2e:
-        xh = torch.from_numpy(d["x_bits"].view(np.int16)).pin_memory()
-        lh = torch.from_numpy(d["logits"]).pin_memory()
+        xh = torch.from_numpy(tok["x_bits"].view(np.int16)).pin_memory()
+        lh = torch.from_numpy(tok["logits"]).pin_memory()
         oh = torch.empty((T, s.H), dtype=torch.int16).pin_memory()
         stage = {"x": torch.empty_like(x), "logits": torch.empty_like(logits), "out": torch.empty_like(out)}
         for _ in range(max(1, args.warmup)):
             layer.forward_host(xh, lh, oh, stage)
         torch.cuda.synchronize()
         ne = max(3, min(args.steps, 50))
-        t0 = time.perf_counter()
+        tot = 0.0
         for _ in range(ne):
             if flush is not None:
                 flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
             layer.forward_host(xh, lh, oh, stage)
             torch.cuda.synchronize()
-        t1 = time.perf_counter()
-        e2e_ms = (t1 - t0) * 1e3 / ne
+            tot += time.perf_counter() - t0
+        e2e_ms = tot * 1e3 / ne
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
         e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(xh.numel() * 2 + lh.numel() * 4),
                "d2h_bytes_per_step": int(oh.numel() * 2), "ms_per_step": e2e_ms,
-               "note": "wall clock incl. pinned H2D of x+logits, layer, D2H of out, and a stream sync"}
+               "note": "wall clock per step: pinned H2D of x + logits, the layer, D2H of out, stream sync"}
 
-    # roofline of the dominant kernel (the gate/up GEMM)
+    # roofline of the dominant kernel: the gate/up GEMM (the fused decode kernel at decode sizes)
     gu_ms = float(seg[:, 1].mean())
-    dn_ms = float(seg[:, 2].mean())
     peaks = load_peaks()
-    tensor_bound = T >= 2048
     fused_decode = impl == _lib.IMPL_GEMV and T <= 8
     if fused_decode:
         # one kernel is the whole step: its bytes (weights of the touched experts, x, logits, out)
         # over the step time
         achieved = work["step_bytes"] / (ms * 1e-3) / 1e9
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
-    elif tensor_bound:
+    elif tensor_bound(T):
         achieved = work["flops_gate_up"] / (gu_ms * 1e-3) / 1e12
         peak, unit, bound = peaks["bf16_tflops"], "TFLOP/s", "tensor"
     else:
         achieved = work["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
-    kname = {_lib.IMPL_TC: "gemm_tc_kernel<0>", _lib.IMPL_GEMV: "gemv_kernel<0>",
-             _lib.IMPL_SIMT: "gemm_simt_kernel<0>"}.get(impl, str(impl))
+    kname = {_lib.IMPL_TC: "gemm_tc_kernel<0>", _lib.IMPL_GEMV: "gemv_kernel<0>"}.get(impl, str(impl))
     traffic = (profiled_traffic(wl.name, 0) if impl == _lib.IMPL_TC else
                profiled_traffic(wl.name, 0, kernel="decode_kernel") if fused_decode else None)
     kdesc = ("decode_kernel: the fused layer (routing, gate/up, down and combine in one launch)" if fused_decode
              else f"gate/up grouped GEMM {kname} (moe_expert_gemm_w4, MOE_GATE_UP_SWIGLU)")
-    roof = {"kernel": kdesc, "bound": bound,
-            "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-            "peak_source": peaks["source"], "traffic": traffic,
+    roof = {"kernel": kdesc, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_source": peaks["source"], "traffic": traffic,
             "algorithmic_per_launch": (work["step_bytes"] if fused_decode else
-                                       work["flops_gate_up"] if tensor_bound else work["gate_up_bytes"]),
+                                       work["flops_gate_up"] if tensor_bound(T) else work["gate_up_bytes"]),
             "launch_ms": ms if fused_decode else gu_ms}
-
-    res = {
-        "metric": METRIC, "value": world * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x uint4 (fp32 accumulate)",
-        "data": "synthetic (seeded; random-init uint4 weights, bf16 scales/biases)",
-        "config": {"workload": wl.name, "desc": wl.desc, "T": T, "H": s.H, "E": s.E, "k": s.k, "F": s.F,
-                   "shared_experts": 1, "group": 64, "block_n": bn, "kernels": args.kernels,
-                   "touched_experts": touched,
-                   "l2": "L2 flushed between steps" if flush is not None else
-                   f"inputs larger than L2 ({work['step_bytes'] / 1e6:.0f} MB streamed per step)",
-                   "parallelism": f"replicas x{world} (tokens sharded, no collective)"},
+    layer_tflops = work["step_flops"] / (ms * 1e-3) / 1e12
+    layer_gbs = work["step_bytes"] / (ms * 1e-3) / 1e9
+    return {
+        "workload": wl.name, "desc": wl.desc, "T": T, "value": world * T / (ms * 1e-3), "unit": "tokens/s",
+        "ms_per_step": ms, "steps": args.steps, "block_n": bn, "touched_experts": touched,
+        "l2": ("L2 flushed between steps" if flush is not None else
+               f"inputs larger than L2 ({work['step_bytes'] / 1e6:.0f} MB streamed per step)"),
         "stages_note": ("eager launches of the four entry points (moe_route, gate/up and down moe_expert_gemm_w4, "
                         "moe_combine); the timed step is the fused decode kernel") if fused_decode else
                        "eager launches of the four entry points; the timed step replays the same launches",
-        "stages_ms": {"route": float(seg[:, 0].mean()), "gate_up": gu_ms, "down": dn_ms,
+        "stages_ms": {"route": float(seg[:, 0].mean()), "gate_up": gu_ms, "down": float(seg[:, 2].mean()),
                       "combine": float(seg[:, 3].mean())},
-        "hbm_GBps_step": work["step_bytes"] / (ms * 1e-3) / 1e9,
-        "tflops_step": work["step_flops"] / (ms * 1e-3) / 1e12,
         "roofline": roof,
-        "gpu_launches": int(launches),
-        "launch": "cuda_graph" if graph is not None else "eager",
-        "eager_ms_per_step": eager_ms,
+        "layer_roofline": {"tflops": layer_tflops, "frac_bf16": layer_tflops / peaks["bf16_tflops"],
+                           "hbm_gbs": layer_gbs, "frac_hbm": layer_gbs / peaks["hbm_gbs"],
+                           "note": "whole step: 56.6 MFLOP per token, bytes of the touched experts + x, logits, out"},
+        "gpu_launches": int(launches), "launch": "cuda_graph" if graph is not None else "eager",
         "e2e": e2e,
+    }
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from bit_mixture_experts_gb300 import build
+    from bit_mixture_experts_gb300.layer import MoELayerW4
+
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    names = [args.workload] + ([] if args.only else [n for n in EXTRA_WORKLOADS if n != args.workload])
+    layers = {}
+    results = {}
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    primary_d = None
+    for name in names:
+        wl = workloads.WORKLOADS[name]
+        s = wl.shape
+        d = workloads.make_workload(wl, seed=0, with_weights=s not in layers)
+        if s not in layers:
+            layers[s] = (MoELayerW4(s.H, s.E, s.k, s.F, d, device=dev, impl=args.kernels, block_n=args.block_n), d)
+        layer, wd = layers[s]
+        d.update({n_: v for n_, v in wd.items() if n_.startswith(("w13_", "w2_"))})
+        if name == args.workload:
+            primary_d = d
+        results[name] = measure_workload(args, wl, layer, d, rank, world, dev)
+    if clocks:
+        clocks.stop()
+    p = results[args.workload]
+    wl = workloads.WORKLOADS[args.workload]
+    s = wl.shape
+    res = {
+        "metric": METRIC, "value": p["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": p["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x uint4 (fp32 accumulate)",
+        "data": "synthetic (seeded; random-init uint4 weights, bf16 scales/biases)",
+        "config": {"workload": wl.name, "desc": wl.desc, "T": wl.T, "H": s.H, "E": s.E, "k": s.k, "F": s.F,
+                   "shared_experts": 1, "group": 64, "block_n": p["block_n"], "kernels": args.kernels,
+                   "touched_experts": p["touched_experts"], "l2": p["l2"],
+                   "parallelism": f"replicas x{world} (tokens sharded, no collective)"},
+        "stages_note": p["stages_note"], "stages_ms": p["stages_ms"],
+        "roofline": p["roofline"], "layer_roofline": p["layer_roofline"],
+        "gpu_launches": p["gpu_launches"], "launch": p["launch"], "e2e": p["e2e"],
+        "workloads": {n: r for n, r in results.items() if n != args.workload},
+        "workloads_note": ("the other workloads of the metric, each timed the same way right after the primary "
+                           "one (same clocks record); prefill4k and skew16k report the gate/up kernel against the "
+                           "bf16 tensor peak, decode1/decode8 the fused decode kernel against HBM"),
     }
     if clocks:
         res["clocks"] = clocks.summary()
-    return res, d, layer
+    return res, primary_d
 
 
 KERNEL_SOURCES = {
@@ -437,6 +477,36 @@ def time_oracle(d, n_tokens, budget_s=20.0):
                       f"dequantised and multiplied in float64 NumPy ({dt:.1f} s)", "seconds": dt}
 
 
+ONE_CORE_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                "BLIS_NUM_THREADS": "1", "VECLIB_MAXIMUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1"}
+
+
+def time_oracle_one_core(workload, n_tokens):
+    """The same oracle sample in a fresh interpreter whose BLAS is limited to one thread (the
+    thread count is fixed when NumPy loads its BLAS, so it cannot be lowered in this process)."""
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, workloads; "
+            "d = workloads.make_workload(%r, 0); print(json.dumps(bench.time_oracle(d, %d)))"
+            % (ROOT, workload, n_tokens))
+    env = dict(os.environ)
+    env.update(ONE_CORE_ENV)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc {r.returncode}"}
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    res["cores"] = 1
+    return res
+
+
+def cpu_baseline(d):
+    """The oracle on a bounded sample of the workload, with all host cores (BLAS threads) and with one."""
+    wl = d["workload"]
+    n = oracle_sample_tokens(wl)
+    allc = time_oracle(d, n)
+    one = time_oracle_one_core(wl.name, n)
+    allc["one_core"] = one
+    return allc
+
+
 def oracle_sample_tokens(wl):
     return {"tiny": 64, "decode1": 1, "decode8": 8, "prefill512": 16, "prefill4k": 16, "skew16k": 16}[wl.name]
 
@@ -472,11 +542,12 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill512", choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--kernels", default="auto", choices=["auto", "tc", "simt", "gemv"])
+    ap.add_argument("--kernels", default="auto", choices=["auto", "tc", "gemv"])
+    ap.add_argument("--only", action="store_true", help="time the chosen workload alone (no per-workload extras)")
     ap.add_argument("--block-n", type=int, default=None, help="rows per GEMM tile (default: per kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -496,10 +567,10 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    res, d, layer = run_ours(args, rank, world, local_rank)
+    res, d = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            res["cpu_baseline"] = time_oracle(d, oracle_sample_tokens(d["workload"]))
+            res["cpu_baseline"] = cpu_baseline(d)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch

@@ -200,8 +200,8 @@ def expert_weights(wts: dict, e: int):
     return w13, w2
 
 
-def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = False, h_given=None,
-                want_y: bool = False, y_given=None) -> dict:
+def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = False,
+                want_y: bool = False) -> dict:
     """The layer: out[t] = bf16( sum_j w[t,j] * y_{e_j}(x_t) + y_shared(x_t) ), y = bf16(h Wd^T).
 
     ``tokens`` restricts the computation to a subset of token indices (routing
@@ -209,12 +209,8 @@ def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = F
     workloads are checked on sampled outputs.  With ``want_h`` the bf16
     intermediate h of every (token, routed expert) and of the shared expert is
     returned as well, keyed by (t, e), together with its unrounded value
-    (key "h_exact").  ``h_given(t, e)``, when set, supplies h instead of the
-    gate/up projection: the down projection and combine are then evaluated
-    exactly on that h (used to check a rounding of h that differs from
-    round-to-nearest on values next to a rounding midpoint).  ``want_y`` and
-    ``y_given`` do the same for the bf16 rows y of the down projection (keys
-    "y" and "y_exact"; with ``y_given`` only the combine is evaluated).
+    (key "h_exact"); ``want_y`` does the same for the bf16 rows y of the down
+    projection (keys "y" and "y_exact").
     """
     logits = np.asarray(logits, dtype=np.float32)
     T, E = logits.shape
@@ -230,26 +226,17 @@ def moe_forward(x_bits, logits, wts: dict, k: int, tokens=None, want_h: bool = F
         else:
             rows, cols = np.nonzero(ids == e)
             wt = w[rows, cols]
-        if y_given is not None:
-            y = np.stack([np.asarray(y_given(int(sel[r]), int(e)), dtype=np.float64) for r in rows])
-            acc[rows] += wt[:, None] * y
-            continue
         w13, w2 = expert_weights(wts, e)
-        if h_given is not None:
-            h = np.stack([np.asarray(h_given(int(sel[r]), int(e)), dtype=np.float64) for r in rows])
-        else:
-            v = expert_swiglu_exact(x[rows], w13)
-            h = round_bf16(v)
-            if want_h:
-                for i, r in enumerate(rows):
-                    hs[(int(sel[r]), int(e))] = h[i]
-                    hx[(int(sel[r]), int(e))] = v[i]
+        v = expert_swiglu_exact(x[rows], w13)
+        h = round_bf16(v)
         yv = expert_down_exact(h, w2)
         y = down_output(yv)
-        if want_y:
-            for i, r in enumerate(rows):
-                ys[(int(sel[r]), int(e))] = y[i]
-                yx[(int(sel[r]), int(e))] = yv[i]
+        for i, r in enumerate(rows):
+            key = (int(sel[r]), int(e))
+            if want_h:
+                hs[key], hx[key] = h[i], v[i]
+            if want_y:
+                ys[key], yx[key] = y[i], yv[i]
         acc[rows] += wt[:, None] * y
     res = {"out": round_bf16(acc), "topk_ids": ids, "topk_w": w, "tokens": sel}
     if want_h:

@@ -243,8 +243,8 @@ def pin_closed_form_constant(T=5, H=128, E=4, k=2, F=64):
         assert np.all(out[t] == expect), (t, out[t][:4], expect)
 
 
-def closed_form_perm_inputs(T=6, E=3, k=2, H=128, F=128, seed=8):
-    """Diagonal gate with per-group scales, up = c_e * identity, down = a permutation."""
+def closed_form_perm_inputs(T=6, E=3, k=2, H=128, F=128, seed=8, down_scale=1.0):
+    """Diagonal gate with per-group scales, up = c_e * identity, down = down_scale times a permutation."""
     assert H == F
     r = np.random.default_rng(seed)
     x_bits = workloads.f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
@@ -256,7 +256,7 @@ def closed_form_perm_inputs(T=6, E=3, k=2, H=128, F=128, seed=8):
     q13 = np.zeros((E + 1, 2 * F, H), np.int64)
     s13 = np.zeros((E + 1, 2 * F, H // 64), np.uint16)
     q2 = np.zeros((E + 1, H, F), np.int64)
-    s2 = np.full((E + 1, H, F // 64), bf16_bits(1.0), np.uint16)
+    s2 = np.full((E + 1, H, F // 64), bf16_bits(down_scale), np.uint16)
     for e in range(E + 1):
         q13[e, :F] = eye
         q13[e, F:] = up_c[e] * eye
@@ -289,6 +289,32 @@ def pin_closed_form_permutation(T=6, E=3, k=2, H=128):
             assert out[t, c] == brute.rne_bf16(tot), (t, c)
 
 
+def pin_closed_form_scaled_down(T=6, E=3, k=2, H=128):
+    """The permutation closed form with a down weight of 3 * 2^-7: y_c = bf16(3 * 2^-7 * h_{pi_e(c)})
+    needs up to 10 significant bits before its rounding, so y is not bf16-exact and the rounding of
+    the down projection's output to bf16 is pinned: out = bf16(sum_j w_j y_{e_j} + y_shared)."""
+    a = 3.0 * 2.0 ** -7
+    x_bits, logits, wts, up_c, g_scale, perms = closed_form_perm_inputs(T, E, k, H, H, down_scale=a)
+    out = moe_ref.moe_forward(x_bits, logits, wts, k)["out"]
+    inexact = 0
+    for t in range(T):
+        x = workloads.bf16_bits_to_f32(x_bits[t]).astype(np.float64)
+        order = sorted(range(E), key=lambda e: (-float(logits[t, e]), e))[:k]
+        z = [math.exp(float(logits[t, e]) - float(logits[t, order[0]])) for e in order]
+        terms = [(e, zz / sum(z)) for e, zz in zip(order, z)] + [(E, 1.0)]
+        for c in range(H):
+            tot = 0.0
+            for e, wt in terms:
+                f = perms[e][c]
+                g = g_scale[e][f // 64] * x[f]
+                h = brute.rne_bf16(g / (1.0 + math.exp(-g)) * up_c[e] * x[f])
+                y = brute.rne_bf16(a * h)
+                inexact += y != a * h
+                tot += wt * y
+            assert out[t, c] == brute.rne_bf16(tot), (t, c)
+    assert inexact > T * H  # most y values really are rounded
+
+
 def pin_bruteforce_layer(shape=None, T=None, seed=0):
     """The vectorised oracle equals the per-token brute force on the tiny workload."""
     wl = workloads.WORKLOADS["tiny"] if shape is None else workloads.custom(T, *shape)
@@ -303,5 +329,5 @@ def pin_bruteforce_layer(shape=None, T=None, seed=0):
 ALL_PINS = [
     pin_round_bf16_library, pin_round_bf16_bitlevel, pin_dequant_golden, pin_dequant_exact_fraction,
     pin_unpack_order, pin_routing_golden, pin_topk_bruteforce, pin_topk_softmax_library,
-    pin_routing_invariants, pin_closed_form_constant, pin_closed_form_permutation,
+    pin_routing_invariants, pin_closed_form_constant, pin_closed_form_permutation, pin_closed_form_scaled_down,
 ]

@@ -40,25 +40,29 @@ def test_bf16_floor_ceil():
     assert np.array_equal(lo2, b) and np.array_equal(hi2, b)
 
 
-def test_given_h_reproduces_layer():
-    """Evaluating down + combine on the oracle's own h reproduces the layer output."""
+def test_intermediates_are_roundings_of_their_exact_values():
+    """The h and y rows the oracle returns are the bf16 roundings of their exact values, and the
+    layer output is the bf16 rounding of the weighted sum of its y rows."""
     d = workloads.make_workload(workloads.custom(9, 128, 4, 2, 64), 2)
-    ref = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, want_h=True)
-    again = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, h_given=lambda t, e: ref["h"][(t, e)])
-    assert np.array_equal(ref["out"], again["out"])
+    ref = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, want_h=True, want_y=True)
     for key, h in ref["h"].items():
         assert np.array_equal(h, moe_ref.round_bf16(ref["h_exact"][key]))
-
-
-def test_given_y_reproduces_layer():
-    """The combine evaluated on the oracle's own bf16 y rows reproduces the layer output, and y is
-    the bf16 rounding of the exact down projection of h."""
-    d = workloads.make_workload(workloads.custom(9, 128, 4, 2, 64), 2)
-    ref = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, want_y=True)
-    again = moe_ref.moe_forward(d["x_bits"], d["logits"], d, 2, y_given=lambda t, e: ref["y"][(t, e)])
-    assert np.array_equal(ref["out"], again["out"])
     for key, y in ref["y"].items():
         assert np.array_equal(y, moe_ref.round_bf16(ref["y_exact"][key]))
+    acc = np.zeros_like(ref["out"])
+    for t in range(9):
+        for j in range(2):
+            acc[t] += ref["topk_w"][t, j] * ref["y"][(t, int(ref["topk_ids"][t, j]))]
+        acc[t] += ref["y"][(t, 4)]
+    assert np.array_equal(ref["out"], moe_ref.round_bf16(acc))
+
+
+def test_y_rounding_pinned_by_closed_form(monkeypatch):
+    """Dropping the bf16 rounding of the down projection's output fails the scaled-down closed
+    form (not only the brute force)."""
+    monkeypatch.setattr(moe_ref, "down_output", lambda y: np.asarray(y, dtype=np.float64))
+    with pytest.raises(AssertionError):
+        P.pin_closed_form_scaled_down()
 
 
 def test_skew_calibration():
