@@ -508,7 +508,7 @@ def cpu_baseline(d):
 
 
 def oracle_sample_tokens(wl):
-    return {"tiny": 64, "decode1": 1, "decode8": 8, "prefill512": 16, "prefill4k": 16, "skew16k": 16}[wl.name]
+    return {"tiny": 64, "decode1": 1, "decode8": 8, "prefill512": 64, "prefill4k": 64, "skew16k": 64}[wl.name]
 
 
 def run_reference(args):
