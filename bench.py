@@ -308,7 +308,8 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
     else:
         achieved = work["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
-    kname = {_lib.IMPL_TC: "gemm_tc_kernel<0>", _lib.IMPL_GEMV: "gemv_kernel<0>"}.get(impl, str(impl))
+    kname = {_lib.IMPL_TC: "gemm_tc_kernel<0>", _lib.IMPL_TC2: "gemm_pair_kernel<0>",
+             _lib.IMPL_GEMV: "gemv_kernel<0>"}.get(impl, str(impl))
     traffic = (profiled_traffic(wl.name, 0) if impl == _lib.IMPL_TC else
                profiled_traffic(wl.name, 0, kernel="decode_kernel") if fused_decode else None)
     kdesc = ("decode_kernel: the fused layer (routing, gate/up, down and combine in one launch)" if fused_decode
@@ -546,7 +547,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="prefill512", choices=sorted(workloads.WORKLOADS))
-    ap.add_argument("--kernels", default="auto", choices=["auto", "tc", "gemv"])
+    ap.add_argument("--kernels", default="auto", choices=["auto", "tc", "tc2", "gemv"])
     ap.add_argument("--only", action="store_true", help="time the chosen workload alone (no per-workload extras)")
     ap.add_argument("--block-n", type=int, default=None, help="rows per GEMM tile (default: per kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

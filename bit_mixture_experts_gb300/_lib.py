@@ -20,8 +20,8 @@ ERRORS = {-1: "MOE_ERR_NULL", -2: "MOE_ERR_ALIGN", -3: "MOE_ERR_SHAPE", -4: "MOE
 DEVICE_ERRORS = {0: "ok", 1: "MOE_DEV_BAD_BLOCK", 2: "MOE_DEV_BAD_INDEX", 3: "MOE_DEV_TIMEOUT", 4: "MOE_DEV_BAD_WORKSPACE"}
 
 GATE_UP, DOWN = 0, 1
-IMPL_AUTO, IMPL_TC, IMPL_GEMV = 0, 2, 3
-IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV}
+IMPL_AUTO, IMPL_TC, IMPL_GEMV, IMPL_TC2 = 0, 2, 3, 4
+IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV, "tc2": IMPL_TC2}
 
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
 SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",

@@ -68,6 +68,9 @@ unsigned long long wait_limit_ns();
 cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                            const int32_t* perm, const float* topk_w, const int32_t* block_map,
                            const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s);
+cudaError_t launch_gemm_pair(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
+                             const int32_t* perm, const int32_t* block_map, const int32_t* num_blocks, int bn, int cap,
+                             void* out, cudaStream_t s);
 void set_wait_limit_ns(unsigned long long ns);
 
 namespace {
@@ -125,16 +128,20 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
   rc = check_ptrs(act, w_packed, perm, topk_w, block_map, num_blocks, out);
   if (rc) return rc;
   if (impl == MOE_IMPL_AUTO) impl = block_n <= gemv_max_rows() ? MOE_IMPL_GEMV : MOE_IMPL_TC;
-  if (impl != MOE_IMPL_GEMV && impl != MOE_IMPL_TC) return MOE_ERR_MODE;
-  // both kernels step K and M by 128; the GEMV takes tiles of at most 8 rows, the tensor-core kernel 128
+  if (impl != MOE_IMPL_GEMV && impl != MOE_IMPL_TC && impl != MOE_IMPL_TC2) return MOE_ERR_MODE;
+  // the kernels step K and M by 128; the GEMV takes tiles of at most 8 rows, the tensor-core kernel
+  // 128, the CTA-pair kernel 256
   if (H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
-  if (block_n > (impl == MOE_IMPL_GEMV ? gemv_max_rows() : 128)) return MOE_ERR_SHAPE;
+  if (block_n > (impl == MOE_IMPL_GEMV ? gemv_max_rows() : impl == MOE_IMPL_TC ? 128 : 256)) return MOE_ERR_SHAPE;
   if (!device_error_ptr()) return MOE_ERR_CUDA;
   const int cap = moe_block_map_capacity(T, E, k, block_n);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (impl == MOE_IMPL_GEMV)
     return cuda_status(launch_gemm_gemv(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
                                         block_n, cap, out, num_sms(), s));
+  if (impl == MOE_IMPL_TC2)
+    return cuda_status(launch_gemm_pair(mode, act, T, H, F, E, k, w_packed, perm, block_map, num_blocks, block_n,
+                                        cap, out, s));
   return cuda_status(launch_gemm_tc(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
                                     block_n, cap, out, num_sms(), s));
 }
@@ -223,10 +230,12 @@ size_t moe_repacked_bytes(int n_mat, int rows, int K) {
 int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias, int n_mat, int rows, int K,
                   int gate_up, void* out, moe_stream_t stream) {
   if (n_mat < 1 || rows < 128 || rows % 128 != 0 || K < 64 || K % 64 != 0) return MOE_ERR_SHAPE;
-  if (gate_up && (rows / 2) % 128 != 0) return MOE_ERR_SHAPE;
+  if (gate_up < 0 || gate_up > 2) return MOE_ERR_MODE;
+  if (gate_up == 1 && (rows / 2) % 128 != 0) return MOE_ERR_SHAPE;
+  if (gate_up == 2 && (rows / 2) % 64 != 0) return MOE_ERR_SHAPE;
   int rc = check_ptrs(packed, scale, bias, out);
   if (rc) return rc;
-  return cuda_status(launch_repack(packed, scale, bias, n_mat, rows, K, gate_up ? 1 : 0, out,
+  return cuda_status(launch_repack(packed, scale, bias, n_mat, rows, K, gate_up, out,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -48,24 +48,22 @@
 
 #include "moe_common.cuh"
 #include "moe_ptx.cuh"
+#include "moe_tc_dev.cuh"
 
 namespace moe {
 
+using namespace tc_dev;
+
 namespace {
 
-constexpr int TC_M = 128;              // weight rows per M-tile (the MMA's M)
-constexpr int KG = 64;                 // one quantisation group
-constexpr int W_PACKED = TC_M * 32;    // packed nibbles of one M-tile x K group
-constexpr int W_BLOCK = W_PACKED + TC_M * 4;  // + (scale, bias) per row: one repacked block
-constexpr int NWB = 12;                // packed-weight ring bytes, in units of one M-tile's 2-group stage
+constexpr int NWMAX = 12;              // packed-weight ring slots (run-time depth, at least 4)
 constexpr int NAMAX = 4;               // dequantised-weight ring (TMEM), run-time depth 2 to 4
-constexpr int NBMAX = 12;              // activation ring (smem), run-time depth <= NBMAX
+constexpr int NBMAX = 12;              // activation ring (smem), run-time depth 2 to NBMAX
 constexpr int TMEM_COLS = 512;        // accumulators first, then the A ring
 constexpr int NTHREADS = 512;
 constexpr int GATHER_T = 64;           // threads gathering activation rows (gate/up)
 
 // barrier indices
-constexpr int NWMAX = NWB;             // weight ring slots (at most)
 constexpr int BAR_WFULL = 0;
 constexpr int BAR_WEMPTY = BAR_WFULL + NWMAX;
 constexpr int BAR_AFULL = BAR_WEMPTY + NWMAX;
@@ -85,18 +83,13 @@ constexpr int STAGE_BYTES = 2 * EPI_ROWS * TC_M * 2;  // epilogue staging: two c
 constexpr int EPI_BAR = 1;       // named barrier of the four epilogue warps
 
 // Sizes that depend on MG, the M-tiles per work unit (they share each
-// activation stage), and GPS, the quant groups per pipeline stage.  The weight
-// ring holds NWB two-group M-tile stages' bytes, except for four-group stages
-// (two-stage-deep activation ring of 64 KB stages) where it shrinks to 4 slots.
+// activation stage), and GPS, the quant groups per pipeline stage.  The ring
+// depths are chosen at launch from the shared memory available.
 template <int MG, int GPS>
 struct UnitCfg {
   static constexpr int W_STAGE = MG * GPS * W_BLOCK;         // packed weights of one stage
   static constexpr int A_COLS = MG * GPS * 32;               // TMEM columns of one dequantised stage
-  static constexpr int NW = GPS == 4 ? 4 : NWB * 2 / (MG * GPS);  // weight ring slots
-  static_assert(NW <= NWMAX, "weight ring barriers");
   static_assert((GPS * W_BLOCK) % 16 == 0, "bulk copies move multiples of 16 bytes");
-  static constexpr int W_RING_BYTES = NW * W_STAGE;
-  static constexpr int TAIL_BYTES = W_RING_BYTES + BAR_BYTES + MISC_BYTES + STAGE_BYTES;
 };
 
 
@@ -110,9 +103,11 @@ struct TcParams {
   void* out;
   int* err;
   unsigned long long wait_cycles;
+  uint32_t sleep_ns;  // suspend hint of the waits: min(20 us, the wait limit)
   int T, H, F, E, k, bn, cap;
   int boxr;     // activation rows per stage buffer (block_n rounded up to 16, <= 128)
   int nb;       // activation ring depth
+  int nw;       // packed-weight ring depth
   int sb;       // bytes of one activation stage: one atom of boxr rows x 128 bytes per quant group
   int nd;       // accumulator buffers
   int dm;       // TMEM columns of one M-tile's accumulator (= boxr)
@@ -127,12 +122,14 @@ struct TcParams {
 // timeout or when another role has already given up (s_abort); the decision
 // is warp-uniform (lane 0's clock).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
-                                          unsigned long long limit) {
+                                          unsigned long long limit, uint32_t sleep_ns) {
   if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
   const long long t0 = clock64();
   for (;;) {
     // sleep until the phase completes (or 20 us pass) rather than polling
-    const bool done = ptx::mbar_try_wait_sleep(bar, parity, 20000u);
+    // the hardware suspends the thread until the phase completes or sleep_ns pass; sleep_ns never
+    // exceeds the limit, so a short limit is checked after at most that long
+    const bool done = ptx::mbar_try_wait_sleep(bar, parity, sleep_ns);
     if (__all_sync(0xffffffffu, done)) return true;
     int give_up = *s_abort;
     if (!give_up && static_cast<unsigned long long>(clock64() - t0) > limit) give_up = 2;
@@ -177,33 +174,6 @@ __device__ __forceinline__ bool unit_tile(const TcParams& p, int u, int MGT, Til
   return ok;
 }
 
-__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
-
-// One quant group of one weight row: 64 nibbles (two uint4 of the repacked
-// block) and its (scale, bias) bf16 pair -> 32 bf16x2 words of
-// w = bf16(q * scale + bias).  128 + q is exact in bf16 (0x4300 | q), the
-// subtraction of 128 is exact, and the fma rounds once.
-__device__ __forceinline__ void expand_group(const uint4 p0, const uint4 p1, uint32_t sb, uint32_t (&v)[32]) {
-  const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-  const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
-  const uint32_t b2 = (sb >> 16) * 0x10001u;
-  constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      // nibbles of K elements 8w+2j (low half) and 8w+2j+1 (high half): 128+q exactly
-      const uint32_t x = ((words[w] >> (4 * j)) & 0x000f000fu) | MAGIC;
-      v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
-    }
-  }
-}
-
-// silu(g) = g / (1 + e^-g) with the fast exponential and division; the
-// product with u is rounded to bf16 afterwards, which hides their few-ulp
-// error except within a few FP32 ulps of a bf16 rounding boundary.
-__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
-
 }  // namespace
 
 // Work unit: one block-map tile (<= 128 token rows) x MG M-tiles (MG x 128
@@ -232,8 +202,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   static_assert(GPS == 2 || (GPS == 4 && MODE == 1 && MG == 1), "2-group stages, or 4 for the one-M-tile down GEMM");
   constexpr int W_STAGE = UnitCfg<MG, GPS>::W_STAGE;
   constexpr int A_COLS = UnitCfg<MG, GPS>::A_COLS;
-  constexpr int W_RING_BYTES = UnitCfg<MG, GPS>::W_RING_BYTES;
-  constexpr int NW = UnitCfg<MG, GPS>::NW;
+  const int NW = p.nw;
+  const int W_RING_BYTES = NW * W_STAGE;
   constexpr int KS = KG * GPS;               // K per stage
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -309,7 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint8_t* g0 = p.w + (static_cast<size_t>(t.expert) * MT + grp * MG) * KT * static_cast<size_t>(W_BLOCK);
       for (int ks = 0; ks < NS; ++ks, ++it) {
         const int s = it % NW, r = it / NW;
-        if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto wprod_done;
+        if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim, p.sleep_ns)) goto wprod_done;
         const uint32_t dst = sbase + off_w + s * W_STAGE;
         ptx::mbar_arrive_expect_tx_elect(bar(BAR_WFULL + s), static_cast<uint32_t>(nm * GPS * W_BLOCK));
         for (int m = 0; m < nm; ++m)
@@ -332,12 +302,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool two = MG == 2 && grp * MG + 1 < MT;
       const uint32_t idesc = ptx::idesc_bf16_f32(TC_M, round16(t.rows));
       const int d = ui % ND, rd = ui / ND;
-      if (rd > 0 && !wait_warp(bar(BAR_DEMPTY + d), (rd - 1) & 1, s_abort, p.err, lim)) goto mma_done;
+      if (rd > 0 && !wait_warp(bar(BAR_DEMPTY + d), (rd - 1) & 1, s_abort, p.err, lim, p.sleep_ns)) goto mma_done;
       ptx::tc_fence_after();
       const uint32_t d0 = tmem + d * DBUF, d1 = d0 + DM;
       for (int ks = 0; ks < NS; ++ks) {
-        if (!wait_warp(bar(BAR_AFULL + sa), pa, s_abort, p.err, lim)) goto mma_done;
-        if (!wait_warp(bar(BAR_BFULL + sb), pb, s_abort, p.err, lim)) goto mma_done;
+        if (!wait_warp(bar(BAR_AFULL + sa), pa, s_abort, p.err, lim, p.sleep_ns)) goto mma_done;
+        if (!wait_warp(bar(BAR_BFULL + sb), pb, s_abort, p.err, lim, p.sleep_ns)) goto mma_done;
         if (MODE == 0) ptx::fence_proxy_async_smem();  // cp.async-written rows, read by the tensor core
         ptx::tc_fence_after();
         const uint32_t a0 = tmem + A0 + sa * A_COLS;
@@ -385,7 +355,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!unit_tile(p, u, MGT, &t, &grp)) continue;
           for (int ks = 0; ks < NS; ++ks, ++it) {
             const int s = it % NB, r = it / NB;
-            if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) goto bprod_done;
+            if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim, p.sleep_ns)) goto bprod_done;
             const uint32_t dst = sbase + s * SB;
             ptx::mbar_arrive_expect_tx_elect(bar(BAR_BFULL + s), static_cast<uint32_t>(SB));
             for (int a = 0; a < GPS; ++a)
@@ -429,7 +399,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (bad) set_device_error(p.err, MOE_DEV_BAD_INDEX);
         for (int ks = 0; ks < NS; ++ks, ++it) {
           const int s = it % NB, r = it / NB;
-          if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim)) {
+          if (r > 0 && !wait_warp(bar(BAR_BEMPTY + s), (r - 1) & 1, s_abort, p.err, lim, p.sleep_ns)) {
             aborted = true;
             break;
           }
@@ -472,7 +442,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int ks = 0; ks < NS; ++ks, ++it) {
         if ((it & 1) != wg) continue;
         const int sa = it % NA, sw = it % NW;
-        if (!wait_warp(bar(BAR_WFULL + sw), (it / NW) & 1, s_abort, p.err, lim)) goto dequant_done;
+        if (!wait_warp(bar(BAR_WFULL + sw), (it / NW) & 1, s_abort, p.err, lim, p.sleep_ns)) goto dequant_done;
         const uint8_t* ws = smem + off_w + sw * W_STAGE;
         uint4 pk[MG][GPS][2];
         uint32_t sbw[MG][GPS];
@@ -493,7 +463,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t v0[PRE][32];
 #pragma unroll
         for (int g = 0; g < PRE; ++g) expand_group(pk[0][g][0], pk[0][g][1], sbw[0][g], v0[g]);
-        if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim))
+        if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim, p.sleep_ns))
           goto dequant_done;
         const uint32_t ta = trow + sa * A_COLS;
 #pragma unroll
@@ -537,7 +507,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const int nm = min(MG, MT - grp * MG);
       const int d = ui % ND;
-      const bool ok = wait_warp(bar(BAR_DFULL + d), (ui / ND) & 1, s_abort, p.err, lim);
+      const bool ok = wait_warp(bar(BAR_DFULL + d), (ui / ND) & 1, s_abort, p.err, lim, p.sleep_ns);
       if (!ptx::named_bar_and(EPI_BAR, 128, ok)) break;
       ptx::tc_fence_after();
       const int N = round16(t.rows);
@@ -603,8 +573,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // [2 halves][128 rows][4 words] packed nibbles + [128 rows] (scale, bias).
 // Within a word the nibbles are reordered so that (word >> 4j) & 0x000f000f
 // yields K elements 2j (low half) and 2j+1 (high half) of that word's eight.
-// Gate/up M-tiles come in pairs: M-tile 2j holds the gate rows and M-tile
-// 2j+1 the up rows of features 128j .. 128j+127 (needs F % 128 == 0).
+// Gate/up M-tiles come in pairs (gate_up = 1): M-tile 2j holds the gate rows
+// and M-tile 2j+1 the up rows of features 128j .. 128j+127 (needs F % 128 == 0);
+// or interleaved (gate_up = 2, for the CTA-pair kernel): M-tile j holds the
+// gate rows of features 64j .. 64j+63 in rows 0-63 and their up rows in rows
+// 64-127.
 // --------------------------------------------------------------------------
 __global__ void repack_kernel(const uint32_t* __restrict__ packed, const uint16_t* __restrict__ scale,
                               const uint16_t* __restrict__ bias, int n_mat, int rows, int K, int gate_up,
@@ -620,7 +593,11 @@ __global__ void repack_kernel(const uint32_t* __restrict__ packed, const uint16_
     const int mt = static_cast<int>(rest % MT);
     const int mat = static_cast<int>(rest / MT);
     int row;
-    if (gate_up) {
+    if (gate_up == 2) {
+      // interleaved: rows 0-63 of M-tile mt are the gate rows, rows 64-127 the up rows of
+      // features 64 mt .. 64 mt + 63
+      row = (L < TC_M / 2 ? 0 : rows / 2) + (TC_M / 2) * mt + (L & (TC_M / 2 - 1));
+    } else if (gate_up) {
       row = (mt & 1) * (rows / 2) + TC_M * (mt >> 1) + L;
     } else {
       row = TC_M * mt + L;
@@ -713,6 +690,7 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   prm.err = device_error_ptr();
   // the limit is applied in SM cycles; 2.1 cycles per ns bounds the fastest SM clock
   prm.wait_cycles = g_wait_ns > (~0ull) / 3 ? ~0ull : g_wait_ns * 21 / 10;
+  prm.sleep_ns = g_wait_ns < 20000ull ? static_cast<uint32_t>(g_wait_ns > 0 ? g_wait_ns : 1) : 20000u;
   prm.T = T;
   prm.H = H;
   prm.F = F;
@@ -728,22 +706,32 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   // quant groups per stage: the one-M-tile down GEMM takes 4 (16 MMAs per stage, as the two-M-tile units)
   const int GPS = (MG == 1 && F % (4 * KG) == 0) ? 4 : 2;
   prm.sb = GPS * boxr * 128;
-  const int tail = MG == 2 ? UnitCfg<2, 2>::TAIL_BYTES : GPS == 4 ? UnitCfg<1, 4>::TAIL_BYTES : UnitCfg<1, 2>::TAIL_BYTES;
+  const int w_stage = MG == 2 ? UnitCfg<2, 2>::W_STAGE : GPS == 4 ? UnitCfg<1, 4>::W_STAGE : UnitCfg<1, 2>::W_STAGE;
   const int a_cols = MG == 2 ? UnitCfg<2, 2>::A_COLS : GPS == 4 ? UnitCfg<1, 4>::A_COLS : UnitCfg<1, 2>::A_COLS;
-  const int budget = max_dyn_smem() - tail - 1024;
-  int nbs = budget / prm.sb;
+  const int fixed = BAR_BYTES + MISC_BYTES + STAGE_BYTES;
+  const int total = max_dyn_smem() - 1024 - fixed;
+  // shared memory: three activation stages when that leaves four weight slots (else two), the
+  // weight ring up to NWMAX slots, then more activation stages with what is left
+  int nbs = 0, nws = 0;
+  for (int want = 3; want >= 2 && nws < 4; --want) {
+    nbs = want;
+    nws = (total - nbs * prm.sb) / w_stage;
+  }
+  if (nws < 4 || nbs < 2) return cudaErrorInvalidValue;
+  if (nws > NWMAX) nws = NWMAX;
+  nbs = (total - nws * w_stage) / prm.sb;
   if (nbs > NBMAX) nbs = NBMAX;
-  if (nbs < 2) return cudaErrorInvalidValue;
   prm.nb = nbs;
+  prm.nw = nws;
   prm.dm = boxr;
-  // TMEM: accumulators (nd buffers x 2 M-tiles x boxr columns), then the A ring
+  // TMEM: accumulators (nd buffers x MG M-tiles x boxr columns), then the A ring
   // a second accumulator buffer (the epilogue of one unit overlaps the next
   // unit's mainloop) when at least two A slots remain
   prm.nd = 2 * (MG * boxr) + 2 * a_cols <= TMEM_COLS ? 2 : 1;
   prm.a0 = prm.nd * MG * boxr;
   prm.na = (TMEM_COLS - prm.a0) / a_cols;
   if (prm.na > NAMAX) prm.na = NAMAX;
-  const int smem = nbs * prm.sb + tail + 1024;
+  const int smem = nbs * prm.sb + nws * w_stage + fixed + 1024;
 
   // activation tensor map (down only): tiles of boxr contiguous rows of h [A+T, F]
   CUtensorMap tmap;
@@ -765,7 +753,8 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
                                                     : MG == 2                    ? gemm_tc_kernel<1, 2, 2>
                                                     : GPS == 4                   ? gemm_tc_kernel<1, 1, 4>
                                                                                  : gemm_tc_kernel<1, 1, 2>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (ea != cudaSuccess) return ea;
   kern<<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
   note_launches(1);
   return cudaGetLastError();

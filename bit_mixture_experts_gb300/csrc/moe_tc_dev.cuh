@@ -1,0 +1,44 @@
+// Device helpers shared by the tensor-core grouped GEMMs (moe_gemm_tc.cu, one
+// CTA per work unit, and moe_gemm_pair.cu, a CTA pair per work unit): the
+// repacked weight block and its expansion to bf16.
+#pragma once
+#include "moe_common.cuh"
+#include "moe_ptx.cuh"
+
+namespace moe {
+namespace tc_dev {
+
+constexpr int TC_M = 128;              // weight rows per M-tile (the MMA's M on one SM)
+constexpr int KG = 64;                 // one quantisation group
+constexpr int W_PACKED = TC_M * 32;    // packed nibbles of one M-tile x K group
+constexpr int W_BLOCK = W_PACKED + TC_M * 4;  // + (scale, bias) per row: one repacked block
+
+__device__ __forceinline__ int round16(int n) { return (n + 15) & ~15; }
+
+// One quant group of one weight row: 64 nibbles (two uint4 of the repacked
+// block) and its (scale, bias) bf16 pair -> 32 bf16x2 words of
+// w = bf16(q * scale + bias).  128 + q is exact in bf16 (0x4300 | q), the
+// subtraction of 128 is exact, and the fma rounds once.
+__device__ __forceinline__ void expand_group(const uint4 p0, const uint4 p1, uint32_t sb, uint32_t (&v)[32]) {
+  const uint32_t words[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+  const uint32_t s2 = (sb & 0xffffu) * 0x10001u;
+  const uint32_t b2 = (sb >> 16) * 0x10001u;
+  constexpr uint32_t MAGIC = 0x43004300u;  // bf16 pair (128, 128)
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // nibbles of K elements 8w+2j (low half) and 8w+2j+1 (high half): 128+q exactly
+      const uint32_t x = ((words[w] >> (4 * j)) & 0x000f000fu) | MAGIC;
+      v[4 * w + j] = ptx::bf16x2_fma(ptx::bf16x2_sub(x, MAGIC), s2, b2);
+    }
+  }
+}
+
+// silu(g) = g / (1 + e^-g) with the fast exponential and division; the
+// product with u is rounded to bf16 afterwards, which hides their few-ulp
+// error except within a few FP32 ulps of a bf16 rounding boundary.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+}  // namespace tc_dev
+}  // namespace moe

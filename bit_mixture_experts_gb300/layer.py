@@ -9,7 +9,7 @@ import numpy as np
 
 from . import _lib
 
-DEFAULT_BLOCK_N = {_lib.IMPL_TC: 128, _lib.IMPL_GEMV: 8}
+DEFAULT_BLOCK_N = {_lib.IMPL_TC: 128, _lib.IMPL_GEMV: 8, _lib.IMPL_TC2: 128}
 DECODE_MAX_T = 16  # token counts up to this take the GEMV kernel under impl="auto"
 
 
@@ -23,7 +23,7 @@ def default_block_n(impl: int, T: int, E: int, k: int) -> int:
     give the grid more tiles; from there on 128-row tiles halve the
     dequantisation per token.  The GEMV kernel takes tiles of up to 8 rows.
     """
-    if impl == _lib.IMPL_TC and T * k < 64 * E:
+    if impl in (_lib.IMPL_TC, _lib.IMPL_TC2) and T * k < 64 * E:
         return 64
     return DEFAULT_BLOCK_N[impl]
 
@@ -58,7 +58,9 @@ class MoELayerW4:
         _lib.load()
         w = {n: (v if isinstance(v, torch.Tensor) else _dev(v, self.device)) for n, v in weights.items()
              if n.startswith(("w13_", "w2_"))}
-        self.w13_r = self._repack(w["w13_packed"], w["w13_scale"], w["w13_bias"], gate_up=True)
+        # the CTA-pair kernel reads interleaved gate/up tiles, every other kernel the paired ones
+        self.w13_r = self._repack(w["w13_packed"], w["w13_scale"], w["w13_bias"],
+                                  gate_up=2 if self.impl == _lib.IMPL_TC2 else 1)
         self.w2_r = self._repack(w["w2_packed"], w["w2_scale"], w["w2_bias"], gate_up=False)
         self.weights = _lib.Weights(self.w13_r.data_ptr(), self.w2_r.data_ptr())
         self._bufs = {}

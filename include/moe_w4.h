@@ -78,8 +78,10 @@ enum {
  * tests run each kernel over every shape it accepts). */
 enum {
   MOE_IMPL_AUTO = 0,      /* GEMV when block_n <= 8, else the tensor-core kernel */
-  MOE_IMPL_TC = 2,        /* tcgen05 kernel */
-  MOE_IMPL_GEMV = 3       /* decode GEMV kernel, mma.sync */
+  MOE_IMPL_TC = 2,        /* tcgen05 kernel, one CTA per work unit */
+  MOE_IMPL_GEMV = 3,      /* decode GEMV kernel, mma.sync */
+  MOE_IMPL_TC2 = 4        /* tcgen05 kernel on CTA pairs (.cta_group::2): gate/up weights repacked
+                             with gate_up = 2 (interleaved tiles); tiles of up to 256 rows */
 };
 
 /* ------------------------------------------------------------------------ */
@@ -182,8 +184,11 @@ size_t moe_repacked_bytes(int n_mat, int rows, int K);
  * so that (word >> 4j) & 0x000f000f holds elements 2j and 2j+1 of its eight)
  * followed by [128 rows] x (scale bf16, bias bf16).  With gate_up = 1 the
  * tiles come in pairs: tile 2j holds the gate rows and tile 2j+1 the up rows
- * of features 128j .. 128j+127 (rows = 2F, F % 128 == 0).  Needs rows % 128
- * == 0 and K % 64 == 0; returns MOE_ERR_SHAPE otherwise.
+ * of features 128j .. 128j+127 (rows = 2F, F % 128 == 0).  With gate_up = 2
+ * (the layout MOE_IMPL_TC2 reads) tile j holds the gate rows of features
+ * 64j .. 64j+63 in its rows 0-63 and their up rows in rows 64-127 (F % 64 ==
+ * 0).  gate_up = 0 is any other matrix (the down projection).  Needs rows %
+ * 128 == 0 and K % 64 == 0; returns MOE_ERR_SHAPE otherwise.
  */
 int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias,
                   int n_mat, int rows, int K, int gate_up, void* out, moe_stream_t stream);
@@ -212,8 +217,9 @@ int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t*
  *        nibbles with each 64-group's bf16 scale and bias in the same block).
  * block_map / num_blocks: moe_route's outputs for the same block_n.
  * impl: MOE_IMPL_*.  AUTO takes GEMV for block_n <= 8 and TC otherwise.  TC
- * needs block_n <= 128; GEMV (decode: tiles of at most 8 token rows) needs
- * block_n <= 8; both need H % 128 == 0 and F % 128 == 0.  Returns
+ * needs block_n <= 128, TC2 block_n <= 256 (and gate/up weights repacked with
+ * gate_up = 2); GEMV (decode: tiles of at most 8 token rows) needs block_n <=
+ * 8; all need H % 128 == 0 and F % 128 == 0.  Returns
  * MOE_ERR_SHAPE when the chosen kernel cannot take the shape and
  * MOE_ERR_MODE for an unknown mode or impl.
  */

@@ -13,7 +13,7 @@ import gpu_util as G
 
 pytestmark = pytest.mark.gpu
 
-IMPLS = ["tc", "gemv"]
+IMPLS = ["tc", "tc2", "gemv"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -75,6 +75,16 @@ def test_layer_repeatable(impl):
     G.check_layer(d, layer, b, what="second call")
 
 
+@pytest.mark.parametrize("block_n", [32, 64, 96, 128, 160, 192, 224, 256])
+def test_layer_tc2_block_sizes(block_n):
+    """The CTA-pair kernel with tile heights across its range (N = rows rounded up to 32, half in each
+    CTA): four-group stages up to 128 rows, two accumulator buffers up to 192, one above."""
+    spec = (700, 256, 16, 4, 128, False)
+    d = G.workload(spec)
+    (got,), layer = run_layer(d, "tc2", block_n=block_n)
+    G.check_layer(d, layer, got, what=f"tc2 block_n={block_n}")
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("name", ["decode1", "decode8", "prefill512", "prefill4k", "skew16k"])
 def test_layer_full_size_every_tile(name, impl):
@@ -87,6 +97,19 @@ def test_layer_full_size_every_tile(name, impl):
     a = G.gpu_arrays(layer, wl.T, got)
     toks = parity.tile_tokens(a["block_map"], a["num_blocks"], a["perm"], wl.T, wl.shape.k)
     G.check_layer(d, layer, got, tokens=toks, what=f"{name} {impl}, {toks.size} tokens (one per tile)")
+
+
+@pytest.mark.parametrize("name", ["prefill4k", "skew16k"])
+@pytest.mark.parametrize("block_n", [192, 256])
+def test_layer_tc2_full_size_tall_tiles(name, block_n):
+    """The CTA-pair kernel with 192- and 256-row tiles at full size, one token per tile."""
+    import parity
+    d = G.workload(name)
+    wl = d["workload"]
+    (got,), layer = run_layer(d, "tc2", block_n=block_n)
+    a = G.gpu_arrays(layer, wl.T, got)
+    toks = parity.tile_tokens(a["block_map"], a["num_blocks"], a["perm"], wl.T, wl.shape.k)
+    G.check_layer(d, layer, got, tokens=toks, what=f"{name} tc2 block_n={block_n}, {toks.size} tokens (one per tile)")
 
 
 @pytest.mark.parametrize("impl", IMPLS)
