@@ -24,7 +24,7 @@ IMPL_AUTO, IMPL_TC, IMPL_GEMV, IMPL_TC2 = 0, 2, 3, 4
 IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV, "tc2": IMPL_TC2}
 
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
-SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
+SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_route_x", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
            "moe_repacked_bytes", "moe_repack_w4", "moe_expert_gemm_w4", "moe_combine", "moe_decode_workspace_size",
            "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns"]
 
@@ -55,6 +55,7 @@ _SIGS = {
     "moe_route_workspace_size": ([_i, _i, _i, _i], _sz),
     "moe_route": ([_vp, _i, _i, _i, _i] + [_vp] * 9 + [_sz, _vp], _i),
     "moe_route_noalloc": ([_vp, _i, _i, _i, _i] + [_vp] * 9, _i),
+    "moe_route_x": ([_vp, _vp, _i, _i, _i, _i, _i] + [_vp] * 10 + [_sz, _vp], _i),
     "moe_repacked_bytes": ([_i, _i, _i], _sz),
     "moe_repack_w4": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
     "moe_expert_gemm_w4": ([_i, _i, _vp, _i, _i, _i, _i, _i] + [_vp] * 5 + [_i, _vp, _vp], _i),
@@ -135,6 +136,17 @@ def moe_route(logits, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_p
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _call("moe_route", _ptr(logits), T, E, k, block_n, _ptr(topk_ids), _ptr(topk_w), _ptr(counts), _ptr(offsets),
           _ptr(perm), _ptr(inv_perm), _ptr(block_map), _ptr(num_blocks), _ptr(workspace), ws_bytes, _stream(stream))
+
+
+def moe_route_x(x, w_router, k, block_n, logits, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map,
+                num_blocks, workspace, stream=None):
+    """Router projection fused with the top-k (x bf16 [T, H], w_router bf16 [E, H] -> logits), then routing."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call("moe_route_x", _ptr(x), _ptr(w_router), T, H, E, k, block_n, _ptr(logits), _ptr(topk_ids), _ptr(topk_w),
+          _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(block_map), _ptr(num_blocks),
+          _ptr(workspace), ws_bytes, _stream(stream))
 
 
 def moe_route_noalloc(logits, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks,

@@ -47,7 +47,9 @@ int num_sms() {
 size_t route_workspace_bytes(int T, int E, int k);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32_t* ids, float* w, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm, int32_t* nb, void* ws,
-                         size_t ws_bytes, cudaStream_t s);
+                         size_t ws_bytes, cudaStream_t s, int ids_given);
+cudaError_t launch_router(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
+                          int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T,
                            int H, int k, int num_sms, cudaStream_t s);
 size_t repacked_bytes(int n_mat, int rows, int K);
@@ -116,7 +118,30 @@ int moe_route(const float* logits, int T, int E, int k, int block_n, int32_t* to
   if (!device_error_ptr()) return MOE_ERR_CUDA;
   return cuda_status(launch_route(logits, T, E, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm,
                                   block_map, num_blocks, workspace, workspace_bytes,
-                                  reinterpret_cast<cudaStream_t>(stream)));
+                                  reinterpret_cast<cudaStream_t>(stream), 0));
+}
+
+int moe_route_x(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, int block_n, float* logits,
+                int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks, void* workspace,
+                size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_route_shape(T, E, k, block_n);
+  if (rc) return rc;
+  if (H < 64 || H % 64 != 0 || E % 64 != 0 || E > 512) return MOE_ERR_SHAPE;
+  rc = check_ptrs(x, w_router, logits, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks);
+  if (rc) return rc;
+  const size_t need = route_workspace_bytes(T, E, k);
+  if (need > 0) {
+    if (workspace_bytes < need) return MOE_ERR_WORKSPACE;
+    rc = check_ptrs(workspace);
+    if (rc) return rc;
+  }
+  if (!device_error_ptr()) return MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  rc = cuda_status(launch_router(x, w_router, T, H, E, k, logits, topk_ids, topk_w, s));
+  if (rc) return rc;
+  return cuda_status(launch_route(logits, T, E, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm,
+                                  block_map, num_blocks, workspace, workspace_bytes, s, 1));
 }
 
 int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, int F, int E, int k,

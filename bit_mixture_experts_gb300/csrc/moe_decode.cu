@@ -12,30 +12,24 @@
 // launch) and hand work to each other through counters in global memory.
 //
 // Phases, in every CTA (256 threads, GV_CTAS_PER_SM per SM):
-//   -  the CTAs whose first gate/up or down item belongs to the shared expert
-//      (its tiles come first among the work items) start copying its weights
-//      at once: the shared expert needs no routing.
 //   R  routing, recomputed by every CTA in shared memory from the logits with
 //      the same device code as moe_route (top-k and weights, counts, offsets,
 //      stable permutation, block map); CTA 0 also writes moe_route's outputs.
-//      Then every CTA starts the copies of its first two gate/up items and of
-//      its first two down items, so the down weights stream during the
-//      gate/up phase (two rings of two item slots each; a slot is refilled
-//      with the item two ahead as soon as its item is computed).
-//   G  gate/up work items (tile, 16 features), exactly as the GEMV kernel.
+//   G  gate/up work items (tile, 16 features), exactly as the GEMV kernel
+//      (the first down item's weights are already streaming during the last).
 //   -  grid barrier: every h value is written.
 //   D  down work items (tile, 32 channels); h is read through L2 only.
-//   C  the gather-combine of 32-channel chunk j, by the CTA that writes the
-//      last y values of that chunk (a counter per chunk): one warp per (token,
-//      chunk), out = bf16(sum_j topk_w[t, j] * y[row(t, j)] + y[shared row]),
-//      FP32 in the same fixed order as moe_combine.  No CTA waits here.
-//   The last CTA to finish resets the barrier counter for the next call.
-// The grid barrier is a counter in global memory (one fence and one atomic
-// per CTA); it relies on every CTA being resident, which the cooperative
-// launch guarantees.  Every wait is bounded nonetheless; on expiry it records
+//   -  grid barrier: every y value is written.
+//   C  the gather-combine, one warp per (token, 32 channels):
+//      out = bf16(sum_j topk_w[t, j] * y[row(t, j)] + y[shared row]), FP32 in
+//      the same fixed order as moe_combine.
+//   The last CTA to finish resets the barrier counters for the next call.
+// The grid barriers are counters in global memory (one fence and one atomic
+// per CTA); they rely on every CTA being resident, which the cooperative
+// launch guarantees.  Each wait is bounded nonetheless; on expiry it records
 // MOE_DEV_TIMEOUT and goes on.  (A first version signalled per work item --
-// a counter per tile for h, per token and 32 channels for y, both waited on --
-// and spent most of its time in the fences those signals need.)
+// a counter per tile for h, per token and 32 channels for y -- and spent
+// most of its time in the fences those signals need.)
 #include "moe_common.cuh"
 #include "moe_gemv_dev.cuh"
 #include "moe_ptx.cuh"
@@ -50,7 +44,6 @@ namespace {
 constexpr int DEC_MAXT = 8;                         // tokens per call
 constexpr int DEC_MAXA = DEC_MAXT * 32;             // assignments (k <= 32)
 constexpr int DEC_MAXTILES = DEC_MAXA + DEC_MAXT;   // routed tiles (>= 1 row each) + shared tiles
-constexpr int DEC_MAXLAST = 128;                    // channel chunks of 32 (H <= 4096)
 
 struct DecParams {
   const uint16_t* x;
@@ -68,19 +61,12 @@ struct DecParams {
   uint16_t* h;
   uint16_t* y;
   uint16_t* out;
-  int* ws;  // counters: [0] h written, [2] CTAs done, [4 + j] writers of y chunk j
+  int* ws;  // grid barrier counters: [0] h written, [1] y written, [2] CTAs done
   int* err;
   unsigned long long wait_cycles;
   int T, H, F, E, k, bn;
-  int G0, G1;  // K groups per thread of the gate/up and of the down items
+  int G;  // K groups per thread (max over the two matrices)
 };
-
-// A tile of the block map packed into one int: expert (11 bits), first row
-// (11 bits), rows (5 bits); T <= 8 and k <= 32 keep rows below 264.
-__device__ __forceinline__ int pack_tile(int e, int r0, int n) { return e | (r0 << 11) | (n << 22); }
-__device__ __forceinline__ int tile_expert(int v) { return v & 0x7ff; }
-__device__ __forceinline__ int tile_row0(int v) { return (v >> 11) & 0x7ff; }
-__device__ __forceinline__ int tile_rows(int v) { return v >> 22; }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -96,7 +82,7 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 // the shared expert's T rows follow as one tile.  s_ok receives the number
 // of routed tiles.
 __device__ __noinline__ void route_small_batch(const int* s_ids, int* s_inv, int* s_tok, int* s_sorted,
-                                               int* s_tile, int* s_ok, int A, int T, int E, int k) {
+                                               int (*s_tile)[3], int* s_ok, int A, int T, int E, int k) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int a = 32 * warp + lane;
   if (a < A) {
@@ -124,13 +110,17 @@ __device__ __noinline__ void route_small_batch(const int* s_ids, int* s_inv, int
     if ((starts >> r) & 1ull) {
       const int ti = __popcll(starts & ((1ull << r) - 1ull));
       const unsigned long long later = r == 63 ? 0ull : starts & ~((2ull << r) - 1ull);
-      s_tile[ti] = pack_tile(s_sorted[r], r, (later ? __ffsll(static_cast<long long>(later)) - 1 : A) - r);
+      s_tile[ti][0] = s_sorted[r];
+      s_tile[ti][1] = r;
+      s_tile[ti][2] = (later ? __ffsll(static_cast<long long>(later)) - 1 : A) - r;
     }
   }
   if (lane == 0) {
     const int n = __popcll(starts);
     *s_ok = n;
-    s_tile[n] = pack_tile(E, A, T);
+    s_tile[n][0] = E;
+    s_tile[n][1] = A;
+    s_tile[n][2] = T;
   }
   if (lane < T) s_tok[A + lane] = lane;
 }
@@ -139,7 +129,7 @@ __device__ __noinline__ void route_small_batch(const int* s_ids, int* s_inv, int
 // their exclusive scan (offsets and first tiles), the stable permutation and
 // the block map, as moe_route computes them.  s_ok receives the number of
 // routed tiles.
-__device__ __noinline__ void route_general(const int* s_ids, int* s_inv, int* s_tok, int* s_tile, int* s_cnt,
+__device__ __noinline__ void route_general(const int* s_ids, int* s_inv, int* s_tok, int (*s_tile)[3], int* s_cnt,
                                            int* s_off, int* s_tile0, uint64_t* s_scan, int* s_ok, int A, int T,
                                            int E, int k, int bn) {
   const int tid = threadIdx.x;
@@ -181,11 +171,15 @@ __device__ __noinline__ void route_general(const int* s_ids, int* s_inv, int* s_
   for (int e = tid; e < E; e += GV_THREADS) {
     const int c = s_cnt[e];
     for (int i = 0, r = 0; r < c; ++i, r += bn) {
-      s_tile[s_tile0[e] + i] = pack_tile(e, s_off[e] + r, min(bn, c - r));
+      s_tile[s_tile0[e] + i][0] = e;
+      s_tile[s_tile0[e] + i][1] = s_off[e] + r;
+      s_tile[s_tile0[e] + i][2] = min(bn, c - r);
     }
   }
   for (int i = tid, r = tid * bn; r < T; i += GV_THREADS, r += GV_THREADS * bn) {
-    s_tile[ntr + i] = pack_tile(E, A + r, min(bn, T - r));
+    s_tile[ntr + i][0] = E;
+    s_tile[ntr + i][1] = A + r;
+    s_tile[ntr + i][2] = min(bn, T - r);
   }
   __syncthreads();
 }
@@ -197,81 +191,24 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
   __shared__ float s_w[DEC_MAXA];
   __shared__ int s_inv[DEC_MAXA];                // assignment -> permuted row
   __shared__ int s_tok[DEC_MAXA + DEC_MAXT];     // permuted row -> token
-  __shared__ int s_tile[DEC_MAXTILES];           // packed (expert, first row, rows), moe_route's order
+  __shared__ int s_tile[DEC_MAXTILES][3];        // (expert, first row, rows)
   __shared__ uint64_t s_scan[33];
   __shared__ int s_sorted[64];                   // small-batch path: expert of each permuted row
   __shared__ int s_ok;
-  __shared__ int s_nlast;                        // channel chunks this CTA combines
-  __shared__ int s_last[DEC_MAXLAST];
-  __shared__ __align__(8) uint64_t s_bar[2][2][GV_WARPS];  // [G, D ring][slot][warp]: copies landed
   extern __shared__ uint4 dec_smem[];
   const int T = p.T, E = p.E, k = p.k, bn = p.bn, H = p.H, F = p.F;
   const int A = T * k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // dynamic shared memory: the gate/up ring (two item slots of G0 groups per thread), the down ring
-  // (two slots of G1 groups), then the partial sums of two items, which during routing hold the
-  // per-expert tables instead
-  const int G0 = p.G0, G1 = p.G1;
-  const int gq = 2 * G0 * GV_THREADS, gsbn = G0 * GV_THREADS;  // per slot: uint4 words, (scale, bias) words
-  const int dq = 2 * G1 * GV_THREADS, dsbn = G1 * GV_THREADS;
-  uint4* g_q = dec_smem;
-  uint32_t* g_sb = reinterpret_cast<uint32_t*>(g_q + 2 * gq);
-  uint4* d_q = reinterpret_cast<uint4*>(g_sb + 2 * gsbn);
-  uint32_t* d_sb = reinterpret_cast<uint32_t*>(d_q + 2 * dq);
-  float* spart0 = reinterpret_cast<float*>(d_sb + 2 * dsbn);
-  int* s_cnt = reinterpret_cast<int*>(spart0);  // [E], routing only
-  int* s_off = s_cnt + E;                        // [E]
-  int* s_tile0 = s_off + E;                      // [E]
-  int* ws_bar = p.ws;                            // [0] h written, [2] CTAs done, [4 + j] y chunk j written
-
-  // The shared expert's tiles come first among the work items, so the CTAs
-  // whose first items are the shared expert's copy its weights before the
-  // routing is known.  Internal tile it: it < ns the shared expert's tile it,
-  // else the routed tile it - ns of the block map.
-  const int ns = ceil_div(T, bn);
-  const int IPT0 = F / 16, IPT1 = H / 32;
-  const int MT0 = (2 * F) / TC_M, MT1 = H / TC_M;
-  const int KT0 = H / KG, KT1 = F / KG;
-  if (tid == 0) {
-    for (int i = 0; i < 2 * 2 * GV_WARPS; ++i) ptx::mbar_init(ptx::smem_u32(&s_bar[0][0][0] + i), 32);
-    ptx::fence_mbar_init();
-  }
-  __syncthreads();
-
-  auto tile_of = [&](int it) -> int {  // packed tile of internal tile it
-    return it < ns ? pack_tile(E, A + it * bn, min(bn, T - it * bn)) : s_tile[it - ns];
-  };
-  // copies of work item u (gate/up when !down) into slot b of its ring: this thread's weight row,
-  // then an arrival on the warp's barrier of the slot once they have landed
-  auto issue = [&](bool down, int u, int b) {
-    const int ipt = down ? IPT1 : IPT0;
-    const int it = u / ipt, j = u - it * ipt;
-    int mt, L;
-    if (down) item_row<1>(j, lane, &mt, &L);
-    else item_row<0>(j, lane, &mt, &L);
-    const int KT = down ? KT1 : KT0, G = down ? G1 : G0;
-    const uint8_t* wrow = (down ? p.w2 : p.w13) +
-                          (static_cast<size_t>(tile_expert(tile_of(it))) * (down ? MT1 : MT0) + mt) * KT *
-                              static_cast<size_t>(W_BLOCK);
-    uint4* qd = (down ? d_q + b * dq : g_q + b * gq) + tid;
-    uint32_t* sd = (down ? d_sb + b * dsbn : g_sb + b * gsbn) + tid;
-#pragma unroll 1
-    for (int i = 0; i < G; ++i) {
-      const int kg = warp + GV_WARPS * i;
-      if (kg >= KT) break;
-      const uint8_t* blk = wrow + static_cast<size_t>(kg) * W_BLOCK;
-      ptx::cp_async_16(ptx::smem_u32(qd + (2 * i) * GV_THREADS), blk + L * 16);
-      ptx::cp_async_16(ptx::smem_u32(qd + (2 * i + 1) * GV_THREADS), blk + 2048 + L * 16);
-      ptx::cp_async_4(ptx::smem_u32(sd + i * GV_THREADS), blk + W_PACKED + L * 4);
-    }
-    ptx::cp_async_mbar_arrive(ptx::smem_u32(&s_bar[down][b][warp]));
-  };
-
-  // ---------------------------------------------------------------- the shared expert's first copies
-  const bool pre_g = static_cast<int>(blockIdx.x) < ns * IPT0;
-  const bool pre_d = static_cast<int>(blockIdx.x) < ns * IPT1;
-  if (pre_g) issue(false, blockIdx.x, 0);
-  if (pre_d) issue(true, blockIdx.x, 0);
+  // dynamic shared memory: weight slots of two items, (scale, bias) slots, partial sums, per-expert tables
+  const int G = p.G;
+  const int slot_q = 2 * G * GV_THREADS, slot_sb = G * GV_THREADS;
+  uint4* swq0 = dec_smem;
+  uint32_t* swsb0 = reinterpret_cast<uint32_t*>(dec_smem + 2 * slot_q);
+  float* spart0 = reinterpret_cast<float*>(swsb0 + 2 * slot_sb);
+  int* s_cnt = reinterpret_cast<int*>(spart0 + 2 * GV_WARPS * GV_MAXN * 32);  // [E]
+  int* s_off = s_cnt + E;                                                     // [E]
+  int* s_tile0 = s_off + E;                                                   // [E]
+  int* ws_bar = p.ws;  // [0] h written, [1] y written, [2] CTAs done
 
   // ---------------------------------------------------------------- R: routing
   if (warp < T) {
@@ -305,7 +242,7 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
     route_general(s_ids, s_inv, s_tok, s_tile, s_cnt, s_off, s_tile0, s_scan, &s_ok, A, T, E, k, bn);
   }
   const int ntr = s_ok;
-  const int nt = ntr + ns;
+  const int nt = ntr + ceil_div(T, bn);
   if (blockIdx.x == 0) {
     // the outputs of moe_route for the same logits
     for (int a = tid; a < A; a += GV_THREADS) {
@@ -319,34 +256,59 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
       p.offsets[e] = s_off[e];
     }
     for (int i = tid; i < nt; i += GV_THREADS) {
-      const int v = s_tile[i];
-      p.block_map[3 * i] = tile_expert(v);
-      p.block_map[3 * i + 1] = tile_row0(v);
-      p.block_map[3 * i + 2] = tile_rows(v);
+      p.block_map[3 * i] = s_tile[i][0];
+      p.block_map[3 * i + 1] = s_tile[i][1];
+      p.block_map[3 * i + 2] = s_tile[i][2];
     }
     if (tid == 0) {
       p.offsets[E] = A;
       p.num_blocks[0] = nt;
     }
   }
-  __syncthreads();  // the per-expert tables are dead from here on: their space holds partial sums
 
   // ---------------------------------------------------------------- G, D: work items
+  const int IPT0 = F / 16, IPT1 = H / 32;
+  const int MT0 = (2 * F) / TC_M, MT1 = H / TC_M;
+  const int KT0 = H / KG, KT1 = F / KG;
   const int nG = nt * IPT0, nD = nt * IPT1;
-  // this CTA's items: gate/up items u = blockIdx.x + q gridDim.x, then down items likewise
+  // this CTA's items: its gate/up items, then its down items
   const int myG = blockIdx.x < nG ? ceil_div(nG - blockIdx.x, gridDim.x) : 0;
   const int myD = blockIdx.x < nD ? ceil_div(nD - blockIdx.x, gridDim.x) : 0;
-  // the down ring's first two items stream while the gate/up items run
-  if (myG > 0 && !pre_g) issue(false, blockIdx.x, 0);
-  if (myD > 0 && !pre_d) issue(true, blockIdx.x, 0);
-  if (myD > 1) issue(true, blockIdx.x + gridDim.x, 1);
-  if (myG > 1) issue(false, blockIdx.x + gridDim.x, 1);
+
+  // copies of item q of this CTA (this thread's weight row) into slot buffer b; one commit group
+  auto issue = [&](int q, int b) {
+    if (q < myG + myD) {
+      const bool down = q >= myG;
+      const int u = blockIdx.x + (down ? q - myG : q) * gridDim.x;
+      const int ipt = down ? IPT1 : IPT0;
+      const int tile = u / ipt, j = u - tile * ipt;
+      int mt, L;
+      if (down) item_row<1>(j, lane, &mt, &L);
+      else item_row<0>(j, lane, &mt, &L);
+      const int KT = down ? KT1 : KT0;
+      const uint8_t* wrow = (down ? p.w2 : p.w13) +
+                            (static_cast<size_t>(s_tile[tile][0]) * (down ? MT1 : MT0) + mt) * KT *
+                                static_cast<size_t>(W_BLOCK);
+      uint4* qd = swq0 + b * slot_q + tid;
+      uint32_t* sd = swsb0 + b * slot_sb + tid;
+#pragma unroll 1
+      for (int i = 0; i < G; ++i) {
+        const int kg = warp + GV_WARPS * i;
+        if (kg >= KT) break;
+        const uint8_t* blk = wrow + static_cast<size_t>(kg) * W_BLOCK;
+        ptx::cp_async_16(ptx::smem_u32(qd + (2 * i) * GV_THREADS), blk + L * 16);
+        ptx::cp_async_16(ptx::smem_u32(qd + (2 * i + 1) * GV_THREADS), blk + 2048 + L * 16);
+        ptx::cp_async_4(ptx::smem_u32(sd + i * GV_THREADS), blk + W_PACKED + L * 4);
+      }
+    }
+    ptx::cp_async_commit();
+  };
 
   // every CTA has passed the barrier once all have arrived; bounded, records a timeout
   auto grid_barrier = [&](int* bar) {
     __syncthreads();
     if (tid == 0) {
-      __threadfence();  // this CTA's h values before its arrival
+      __threadfence();  // this CTA's h / y values before its arrival
       const int before_me = atomicAdd(bar, 1);
       if (before_me < 0 || before_me >= static_cast<int>(gridDim.x))
         set_device_error(p.err, MOE_DEV_BAD_WORKSPACE);  // the workspace was not zero at the start
@@ -361,44 +323,32 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
     }
     __syncthreads();
   };
-  // wait until this warp's copies of slot b of a ring (use number `use` of that slot) have landed
-  auto wait_slot = [&](bool down, int b, int use) -> void {
-    const uint32_t bar = ptx::smem_u32(&s_bar[down][b][warp]);
-    const uint32_t par = static_cast<uint32_t>(use & 1);
-    if (ptx::mbar_try_wait(bar, par)) return;
-    const long long t0 = clock64();
-    while (!ptx::mbar_try_wait(bar, par)) {
-      if (static_cast<unsigned long long>(clock64() - t0) > p.wait_cycles) {
-        set_device_error(p.err, MOE_DEV_TIMEOUT);
-        break;
-      }
-    }
-  };
 
+  issue(0, 0);
   for (int q = 0; q < myG + myD; ++q) {
-    const bool down = q >= myG;
-    const int qq = down ? q - myG : q;  // index among this CTA's items of the kind
+    const int buf = q & 1;
     if (q == myG) grid_barrier(ws_bar);  // all of h is written before any down item reads it
-    const int b = qq & 1;
-    const int u = blockIdx.x + qq * gridDim.x;
+    issue(q + 1, buf ^ 1);  // the next item's weights stream during this one
+    const bool down = q >= myG;
+    const int u = blockIdx.x + (down ? q - myG : q) * gridDim.x;
     const int ipt = down ? IPT1 : IPT0;
-    const int it = u / ipt, j = u - it * ipt;
-    const int tv = tile_of(it);
-    const int row0 = tile_row0(tv), nrow = tile_rows(tv);
+    const int tile = u / ipt, j = u - tile * ipt;
+    const int row0 = s_tile[tile][1], nrow = s_tile[tile][2];
     // activation row of this lane's token column (gate/up: x of the row's token; down: the row of h);
     // columns past the tile read the tile's first row
     const int r = row0 + ((lane >> 2) < nrow ? (lane >> 2) : 0);
     const uint32_t xo = down ? static_cast<uint32_t>(r) * static_cast<uint32_t>(F)
                              : static_cast<uint32_t>(s_tok[r]) * static_cast<uint32_t>(H);
     float d[2][4] = {};
-    wait_slot(down, b, qq >> 1);  // this warp's rows of item qq have landed
-    if (down) item_mma<true>(d_q + b * dq + 32 * warp, d_sb + b * dsbn + 32 * warp, p.h, xo, warp, lane, KT1, G1, d);
-    else item_mma<false>(g_q + b * gq + 32 * warp, g_sb + b * gsbn + 32 * warp, p.x, xo, warp, lane, KT0, G0, d);
-    __syncwarp();  // every lane is done with the slot's rows before they are overwritten
-    if (qq + 2 < (down ? myD : myG)) issue(down, u + 2 * gridDim.x, b);
+    ptx::cp_async_wait<1>();  // this thread's copies of item q have landed
+    __syncwarp();             // ... and those of the warp's other lanes, whose rows this lane reads
+    const uint4* sw = swq0 + buf * slot_q + 32 * warp;
+    const uint32_t* ssbw = swsb0 + buf * slot_sb + 32 * warp;
+    if (down) item_mma<true>(sw, ssbw, p.h, xo, warp, lane, KT1, G, d);
+    else item_mma<false>(sw, ssbw, p.x, xo, warp, lane, KT0, G, d);
 
     // reduce the warps' partial sums (fixed order) and write the item's outputs
-    float* spart = spart0 + (q & 1) * (GV_WARPS * GV_MAXN * 32);
+    float* spart = spart0 + buf * (GV_WARPS * GV_MAXN * 32);
     store_partials(spart, d, warp, lane, nrow);
     __syncthreads();
     if (!down) {
@@ -418,50 +368,34 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
     }
   }
   if (myD == 0) grid_barrier(ws_bar);  // CTAs without down items still take part in the first barrier
-  ptx::cp_async_wait_all();  // no copy outlives its item (after a timed-out wait, they land here)
+  ptx::cp_async_wait_all();
+  grid_barrier(ws_bar + 1);  // all of y is written
 
-  // ---------------------------------------------------------------- C: combine by the last writer of each chunk
-  // Channel chunk j (32 channels) of the output needs the y rows of every tile; the CTA whose down
-  // item completes chunk j last (a counter per chunk) combines it for all tokens, so no CTA waits for
-  // another here.
-  __syncthreads();  // this CTA's y values are written
-  if (tid == 0) {
-    __threadfence();  // ... and visible to every CTA before the counters say so
-    int nl = 0;
-    for (int qq = 0; qq < myD; ++qq) {
-      const int j = (blockIdx.x + qq * gridDim.x) % IPT1;
-      const int before = atomicAdd(ws_bar + 4 + j, 1);
-      if (before == nt - 1) s_last[nl++] = j;
-      else if (before < 0 || before >= nt) set_device_error(p.err, MOE_DEV_BAD_WORKSPACE);
-    }
-    s_nlast = nl;
-    __threadfence();  // the other CTAs' y values, before this CTA reads them
-  }
-  __syncthreads();
-  for (int c = warp; c < T * s_nlast; c += GV_WARPS) {
-    const int t = c % T, jb = s_last[c / T];
+  // ---------------------------------------------------------------- C: combine, one warp per (token, 32 channels)
+  for (int c = blockIdx.x * GV_WARPS + warp; c < T * IPT1; c += gridDim.x * GV_WARPS) {
+    const int t = c / IPT1, jb = c - t * IPT1;
     // rows loaded eight at a time before they are summed (one L2 round trip per batch)
     const uint16_t ys = __ldcg(p.y + static_cast<size_t>(A + t) * H + 32 * jb + lane);
     float o = 0.f;
     for (int j0 = 0; j0 < k; j0 += 8) {
       uint16_t yb[8];
 #pragma unroll
-      for (int b8 = 0; b8 < 8; ++b8)
-        yb[b8] = j0 + b8 < k ? __ldcg(p.y + static_cast<size_t>(s_inv[t * k + j0 + b8]) * H + 32 * jb + lane) : 0;
+      for (int b = 0; b < 8; ++b)
+        yb[b] = j0 + b < k ? __ldcg(p.y + static_cast<size_t>(s_inv[t * k + j0 + b]) * H + 32 * jb + lane) : 0;
 #pragma unroll
-      for (int b8 = 0; b8 < 8; ++b8)
-        if (j0 + b8 < k) o = fmaf(s_w[t * k + j0 + b8], bf16_bits_to_float(yb[b8]), o);
+      for (int b = 0; b < 8; ++b)
+        if (j0 + b < k) o = fmaf(s_w[t * k + j0 + b], bf16_bits_to_float(yb[b]), o);
     }
     o = fmaf(1.0f, bf16_bits_to_float(ys), o);
     p.out[static_cast<size_t>(t) * H + 32 * jb + lane] = float_to_bf16_bits(o);
   }
-  if (tid < s_nlast) ws_bar[4 + s_last[tid]] = 0;  // this call is done with the chunk's counter
 
-  // ---------------------------------------------------------------- the last CTA resets the barrier
+  // ---------------------------------------------------------------- the last CTA resets the counters
   __syncthreads();
   if (tid == 0) {
     if (atomicAdd(ws_bar + 2, 1) == static_cast<int>(gridDim.x) - 1) {
       ws_bar[0] = 0;
+      ws_bar[1] = 0;
       ws_bar[2] = 0;
     }
   }
@@ -469,13 +403,11 @@ __global__ void __launch_bounds__(GV_THREADS, GV_CTAS_PER_SM) decode_kernel(cons
 
 int decode_max_tokens() { return DEC_MAXT; }
 
-// [0] the h barrier, [1] unused, [2] CTAs done, [3] unused, [4 + j] writers of y chunk j (H / 32 chunks)
-size_t decode_workspace_bytes(int, int H) { return (4 + static_cast<size_t>(H) / 32) * sizeof(int); }
+size_t decode_workspace_bytes(int, int) { return 4 * sizeof(int); }
 
-static size_t decode_smem_bytes(int G0, int G1, int E) {
-  const size_t part = 2 * static_cast<size_t>(GV_WARPS) * GV_MAXN * 32 * sizeof(float);
-  const size_t tables = 3 * static_cast<size_t>(E) * sizeof(int);
-  return 2 * static_cast<size_t>(G0 + G1) * GV_THREADS * (2 * 16 + 4) + (part > tables ? part : tables);
+static size_t decode_smem_bytes(int G, int E) {
+  return 2 * static_cast<size_t>(G) * GV_THREADS * (2 * 16 + 4) +
+         2 * static_cast<size_t>(GV_WARPS) * GV_MAXN * 32 * sizeof(float) + 3 * static_cast<size_t>(E) * sizeof(int);
 }
 
 cudaError_t launch_decode(const uint16_t* x, const float* logits, const void* w13, const void* w2, int T, int H, int F,
@@ -509,10 +441,10 @@ cudaError_t launch_decode(const uint16_t* x, const float* logits, const void* w1
   prm.E = E;
   prm.k = k;
   prm.bn = bn;
-  prm.G0 = (H / KG + GV_WARPS - 1) / GV_WARPS;
-  prm.G1 = (F / KG + GV_WARPS - 1) / GV_WARPS;
-  if (prm.G0 > GV_GB || prm.G1 > GV_GB || H / 32 > DEC_MAXLAST) return cudaErrorInvalidValue;
-  const size_t smem = decode_smem_bytes(prm.G0, prm.G1, E);
+  const int g0 = (H / KG + GV_WARPS - 1) / GV_WARPS, g1 = (F / KG + GV_WARPS - 1) / GV_WARPS;
+  prm.G = g0 > g1 ? g0 : g1;
+  if (prm.G > GV_GB) return cudaErrorInvalidValue;
+  const size_t smem = decode_smem_bytes(prm.G, E);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

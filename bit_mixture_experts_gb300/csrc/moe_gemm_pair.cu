@@ -108,17 +108,17 @@ struct PairParams {
   int a0;       // first TMEM column of the A ring
 };
 
-// Bounded wait by a whole warp (acquire at cluster scope: the phase may be
-// completed by the other CTA).  False on timeout or when another role of this
-// CTA has already given up; the decision is warp-uniform.
+// Bounded wait by a whole warp (the phase may be completed by arrivals from the
+// other CTA).  False on timeout or when another role of this CTA has already
+// given up; the decision is warp-uniform.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
                                           unsigned long long limit, uint32_t sleep_ns) {
-  if (__all_sync(0xffffffffu, ptx::mbar_try_wait_cl(bar, parity))) return true;
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
   const long long t0 = clock64();
   for (;;) {
     // the hardware suspends the thread until the phase completes or sleep_ns pass; sleep_ns never
     // exceeds the limit, so a short limit is checked after at most that long
-    const bool done = ptx::mbar_try_wait_sleep_cl(bar, parity, sleep_ns);
+    const bool done = ptx::mbar_try_wait_sleep(bar, parity, sleep_ns);
     if (__all_sync(0xffffffffu, done)) return true;
     int give_up = *s_abort;
     if (!give_up && static_cast<unsigned long long>(clock64() - t0) > limit) give_up = 2;
@@ -137,10 +137,10 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 constexpr unsigned long long DRAIN_MIN_CYCLES = 20000000ull;
 
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
-  if (ptx::mbar_try_wait_cl(bar, parity)) return;
+  if (ptx::mbar_try_wait(bar, parity)) return;
   if (limit < DRAIN_MIN_CYCLES) limit = DRAIN_MIN_CYCLES;
   const long long t0 = clock64();
-  while (!ptx::mbar_try_wait_sleep_cl(bar, parity, 20000u)) {
+  while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (static_cast<unsigned long long>(clock64() - t0) > limit) return;
   }
 }

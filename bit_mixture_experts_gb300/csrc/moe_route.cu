@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     const float* __restrict__ logits, int T, int E, int k, int bn, int32_t* __restrict__ topk_ids,
     float* __restrict__ topk_w, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm, int32_t* __restrict__ block_map,
-    int32_t* __restrict__ num_blocks) {
+    int32_t* __restrict__ num_blocks, int ids_given) {
   extern __shared__ int smem_i[];
   int* s_cnt = smem_i;                    // [E]
   int* s_wc = smem_i + E;                 // [32][E] per-warp counts
@@ -39,6 +39,10 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
 
   for (int i = threadIdx.x; i < 33 * E; i += blockDim.x) smem_i[i] = 0;
   for (int t = warp; t < T; t += 32) {
+    if (ids_given) {  // top-k already chosen (moe_route_x): take the ids
+      if (lane < k) s_ids[t * k + lane] = min(max(__ldg(topk_ids + t * k + lane), 0), E - 1);
+      continue;
+    }
     int id;
     float w;
     warp_topk_any(logits + static_cast<size_t>(t) * E, E, k, lane, &id, &w);
@@ -121,7 +125,7 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
                                                           int32_t* cc, int* ctr, int32_t* counts, int32_t* offsets,
                                                           int32_t* perm, int32_t* inv_perm, int32_t* block_map,
                                                           int32_t* num_blocks, int cap, int* err,
-                                                          unsigned long long wait_cycles) {
+                                                          unsigned long long wait_cycles, int ids_given) {
   extern __shared__ int smem_i[];
   int* s_hist = smem_i;        // [E] chunk counts, then the chunk's next free row per expert
   int* s_wc = smem_i + E;      // [8][E] per-warp group sizes
@@ -138,6 +142,15 @@ __global__ void __launch_bounds__(256) route_fused_kernel(const float* __restric
   for (int t = t0 + warp; t < t1; t += 8) {
     int id;
     float w;
+    if (ids_given) {  // top-k already chosen (moe_route_x): take the ids
+      id = lane < k ? __ldg(topk_ids + static_cast<size_t>(t) * k + lane) : 0;
+      if (id < 0 || id >= E) {
+        set_device_error(err, MOE_DEV_BAD_INDEX);
+        id = 0;
+      }
+      if (lane < k) atomicAdd(&s_hist[id], 1);
+      continue;
+    }
     warp_topk_any(logits + static_cast<size_t>(t) * E, E, k, lane, &id, &w);
     if (lane < k) {
       topk_ids[static_cast<size_t>(t) * k + lane] = id;
@@ -298,7 +311,7 @@ unsigned long long wait_limit_ns();
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32_t* ids, float* w,
                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm,
-                         int32_t* nb, void* ws, size_t ws_bytes, cudaStream_t s) {
+                         int32_t* nb, void* ws, size_t ws_bytes, cudaStream_t s, int ids_given) {
   int* err = device_error_ptr();
   if (route_use_small(T, k)) {
     size_t sm = static_cast<size_t>(33) * E * sizeof(int);
@@ -307,7 +320,8 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
                                                   static_cast<int>(sm));
       if (e0 != cudaSuccess) return e0;
     }
-    route_small_kernel<<<1, 1024, sm, s>>>(logits, T, E, k, bn, ids, w, counts, offsets, perm, inv_perm, bm, nb);
+    route_small_kernel<<<1, 1024, sm, s>>>(logits, T, E, k, bn, ids, w, counts, offsets, perm, inv_perm, bm, nb,
+                                           ids_given);
     note_launches(1);
     return cudaGetLastError();
   }
@@ -336,7 +350,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
   cfg.numAttrs = 1;
   const int cap = moe_block_map_capacity(T, E, k, bn);
   cudaError_t e = cudaLaunchKernelEx(&cfg, route_fused_kernel, logits, T, E, k, tc, bn, ids, w, cc, ctr, counts,
-                                     offsets, perm, inv_perm, bm, nb, cap, err, wait_cycles);
+                                     offsets, perm, inv_perm, bm, nb, cap, err, wait_cycles, ids_given);
   note_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -401,7 +415,7 @@ extern "C" int moe_route_noalloc(const float* logits, int T, int E, int k, int b
   if (!moe::device_error_ptr()) return MOE_ERR_CUDA;
   const cudaError_t e = moe::launch_route(logits, T, E, k, block_n, topk_ids, topk_w, counts, offsets, perm,
                                           inv_perm, block_map, num_blocks, scratch, kRouteScratchBytes,
-                                          reinterpret_cast<cudaStream_t>(stream));
+                                          reinterpret_cast<cudaStream_t>(stream), 0);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

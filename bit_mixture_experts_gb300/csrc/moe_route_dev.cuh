@@ -32,14 +32,16 @@ __device__ __forceinline__ float key_float(uint32_t key) {
 // difference l_j - l_0 is carried exactly as hi + lo (two-sum), so the only
 // errors are expf's (<= 2 ulp), the float sum of k terms and the division:
 // well under 1e-6 relative.
-template <int EPL>
+// COHERENT reads the row through L2 only (a row written earlier by other CTAs
+// of the same kernel); otherwise through the read-only path.
+template <int EPL, bool COHERENT = false>
 __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, int k, int lane,
                                           int* id_out, float* w_out) {
   uint32_t key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     int e = i * 32 + lane;
-    key[i] = e < E ? float_key(__ldg(row + e)) : 0u;
+    key[i] = e < E ? float_key(COHERENT ? __ldcg(row + e) : __ldg(row + e)) : 0u;
   }
   uint32_t chosen = 0;
   int my_id = 0;
@@ -80,13 +82,14 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, 
   *w_out = z / s;
 }
 
+template <bool COHERENT = false>
 __device__ __forceinline__ void warp_topk_any(const float* row, int E, int k, int lane, int* id, float* w) {
-  if (E <= 32) warp_topk<1>(row, E, k, lane, id, w);
-  else if (E <= 64) warp_topk<2>(row, E, k, lane, id, w);
-  else if (E <= 128) warp_topk<4>(row, E, k, lane, id, w);
-  else if (E <= 256) warp_topk<8>(row, E, k, lane, id, w);
-  else if (E <= 512) warp_topk<16>(row, E, k, lane, id, w);
-  else warp_topk<32>(row, E, k, lane, id, w);
+  if (E <= 32) warp_topk<1, COHERENT>(row, E, k, lane, id, w);
+  else if (E <= 64) warp_topk<2, COHERENT>(row, E, k, lane, id, w);
+  else if (E <= 128) warp_topk<4, COHERENT>(row, E, k, lane, id, w);
+  else if (E <= 256) warp_topk<8, COHERENT>(row, E, k, lane, id, w);
+  else if (E <= 512) warp_topk<16, COHERENT>(row, E, k, lane, id, w);
+  else warp_topk<32, COHERENT>(row, E, k, lane, id, w);
 }
 
 // Exclusive scan of one uint64 per thread over the whole block (blockDim.x a

@@ -132,6 +132,27 @@ int moe_route(const float* logits, int T, int E, int k, int block_n,
               void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * moe_route_x -- the router projection fused with the top-k, then the routing
+ * of moe_route ("Perplexity Open Sources Lily", Technical Details, Model
+ * bullet: a router chooses 8 of 256 experts per token).
+ *
+ * x        bf16 [T, H]   the tokens' activations
+ * w_router bf16 [E, H]   the router's projection, one row per expert
+ * logits   float32 [T, E] output: x w_router^T, products of the bf16 operands
+ *                         accumulated in FP32 on the tensor cores
+ * topk_ids ... workspace: as moe_route; the top-k (same selection, ties and
+ *          weights as moe_route) is taken from these logits in the same
+ *          kernel that computes them, then the histogram, scan, scatter and
+ *          block map follow in moe_route's kernel.
+ * Needs H % 64 == 0, E % 64 == 0 and E <= 512 (one cluster of E / 64 CTAs
+ * per 128 tokens).  Two kernel launches on `stream`.
+ */
+int moe_route_x(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, int block_n,
+                float* logits, int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
+                int32_t* perm, int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks,
+                void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
  * moe_route_noalloc -- moe_route for callers that may not allocate device
  * memory: code handed only its input and output buffers by a host engine
  * whose allocator owns the whole device (a serving process that reserves

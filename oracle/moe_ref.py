@@ -76,6 +76,23 @@ def dequant(packed, scale_bits, bias_bits) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------- #
+# router projection
+# --------------------------------------------------------------------------- #
+def router_logits(x_bits, wr_bits) -> np.ndarray:
+    """Router projection: logits[t, e] = sum_h x[t, h] * Wr[e, h], rounded once to float32.
+
+    The router chooses experts from one logit per expert ("Perplexity Open
+    Sources Lily", Technical Details, Model bullet); here the logit is the dot
+    product of the token's bf16 activations with the expert's bf16 router row.
+    The products are exact in float64 and their float64 sum is within 1e-12
+    relative of the exact sum, far inside the final float32 rounding.
+    """
+    x = bf16_value(x_bits)
+    w = bf16_value(wr_bits)
+    return (x @ w.T).astype(np.float32)
+
+
+# --------------------------------------------------------------------------- #
 # routing
 # --------------------------------------------------------------------------- #
 def topk_route(logits, k: int):

@@ -315,6 +315,34 @@ def pin_closed_form_scaled_down(T=6, E=3, k=2, H=128):
     assert inexact > T * H  # most y values really are rounded
 
 
+def pin_router_logits_integer(T=5, H=192, E=7, seed=12):
+    """Router projection on small-integer operands (exact in bf16 and in float32): every logit equals
+    the integer dot product x[t] . Wr[e], computed here with Python integers."""
+    r = np.random.default_rng(seed)
+    xi = r.integers(-3, 4, size=(T, H))
+    wi = r.integers(-2, 3, size=(E, H))
+    got = moe_ref.router_logits(workloads.f32_to_bf16_bits(xi.astype(np.float32)),
+                                workloads.f32_to_bf16_bits(wi.astype(np.float32)))
+    assert got.shape == (T, E) and got.dtype == np.float32
+    for t in range(T):
+        for e in range(E):
+            assert got[t, e] == float(sum(int(a) * int(b) for a, b in zip(xi[t], wi[e]))), (t, e)
+
+
+def pin_router_logits_exact_sum(T=3, H=128, E=5, seed=13):
+    """Router projection on random bf16 operands: each logit is the exactly summed products
+    (math.fsum) rounded once to float32."""
+    r = np.random.default_rng(seed)
+    xb = workloads.f32_to_bf16_bits(r.standard_normal((T, H)).astype(np.float32))
+    wb = workloads.f32_to_bf16_bits((r.standard_normal((E, H)) / 11.0).astype(np.float32))
+    got = moe_ref.router_logits(xb, wb)
+    x = workloads.bf16_bits_to_f32(xb).astype(np.float64)
+    w = workloads.bf16_bits_to_f32(wb).astype(np.float64)
+    for t in range(T):
+        for e in range(E):
+            assert got[t, e] == np.float32(math.fsum(x[t] * w[e])), (t, e)
+
+
 def pin_bruteforce_layer(shape=None, T=None, seed=0):
     """The vectorised oracle equals the per-token brute force on the tiny workload."""
     wl = workloads.WORKLOADS["tiny"] if shape is None else workloads.custom(T, *shape)
@@ -330,4 +358,5 @@ ALL_PINS = [
     pin_round_bf16_library, pin_round_bf16_bitlevel, pin_dequant_golden, pin_dequant_exact_fraction,
     pin_unpack_order, pin_routing_golden, pin_topk_bruteforce, pin_topk_softmax_library,
     pin_routing_invariants, pin_closed_form_constant, pin_closed_form_permutation, pin_closed_form_scaled_down,
+    pin_router_logits_integer, pin_router_logits_exact_sum,
 ]

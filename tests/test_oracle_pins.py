@@ -96,7 +96,8 @@ def test_generator_statistics():
 def _mutations():
     orig = {n: getattr(moe_ref, n) for n in
             ("unpack_u4", "dequant", "expert_swiglu_exact", "topk_route", "expert_down_exact",
-             "expert_weights", "stable_permutation", "round_bf16", "block_map", "exclusive_scan")}
+             "expert_weights", "stable_permutation", "round_bf16", "block_map", "exclusive_scan",
+             "router_logits")}
 
     def msb_first(p):
         q = orig["unpack_u4"](p)
@@ -155,7 +156,15 @@ def _mutations():
         c = np.asarray(counts, np.int64)
         return np.concatenate([np.cumsum(c), [c.sum()]]).astype(np.int32)
 
+    def router_drops_last_k(x_bits, wr_bits):
+        return orig["router_logits"](np.asarray(x_bits)[:, :-1], np.asarray(wr_bits)[:, :-1])
+
+    def router_reversed_k(x_bits, wr_bits):
+        return orig["router_logits"](np.asarray(x_bits)[:, ::-1], np.asarray(wr_bits))
+
     return {
+        "router_drops_last_k": ("router_logits", router_drops_last_k),
+        "router_reversed_k": ("router_logits", router_reversed_k),
         "nibble_msb_first": ("unpack_u4", msb_first),
         "dequant_drops_bias": ("dequant", no_bias),
         "silu_on_up": ("expert_swiglu_exact", silu_on_up),

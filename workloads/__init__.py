@@ -123,6 +123,12 @@ def router_weight(shape: LayerShape, seed: int = 0) -> np.ndarray:
     return r.normal(0.0, 1.0 / math.sqrt(shape.H), size=(shape.E, shape.H)).astype(np.float32)
 
 
+def router_weight_bits(shape: LayerShape, seed: int = 0) -> np.ndarray:
+    """The router projection as bf16 bits [E, H] (the fp32 weight above, rounded): the operand of the
+    fused router projection, which multiplies bf16 activations by bf16 router rows."""
+    return f32_to_bf16_bits(router_weight(shape, seed))
+
+
 def skew_offsets(E: int, beta: float = SKEW_BETA, seed: int = 0) -> np.ndarray:
     """Per-expert logit offset beta * (-s * ln rank_e), ranks a seeded permutation of 1..E."""
     r = _rng(seed, 3, E)
