@@ -359,8 +359,11 @@ def measure_host_synced(args, wl, layer, d, dev):
     w = layer.weights
     A = T * s.k
     counts_h = torch.empty(s.E, dtype=torch.int32).pin_memory()
-    nb_dev = torch.empty(s.E + 1, dtype=torch.int32, device=dev)
-    bm_dev = torch.empty((_lib.moe_block_map_capacity(T, s.E, s.k, bn), 3), dtype=torch.int32, device=dev)
+    # per expert: its tile count 16 bytes apart and its block-map rows from a 16-byte boundary (4 rows),
+    # as the library requires of every pointer
+    nb_dev = torch.empty(4 * (s.E + 1), dtype=torch.int32, device=dev)
+    bm_dev = torch.empty((_lib.moe_block_map_capacity(T, s.E, s.k, bn) + 4 * (s.E + 1), 3), dtype=torch.int32,
+                         device=dev)
 
     def step():
         _lib.moe_route(logits, s.k, bn, b["topk_ids"], b["topk_w"], b["counts"], b["offsets"], b["perm"],
@@ -372,19 +375,20 @@ def measure_host_synced(args, wl, layer, d, dev):
         for e in range(s.E + 1):
             n = int(c[e]) if e < s.E else T
             r0 = off if e < s.E else A
+            rows += [(0, 0, 0)] * (-len(rows) % 4)
             first.append(len(rows))
             rows += [(e, r0 + i, min(bn, n - i)) for i in range(0, n, bn)]
             nbs.append(len(rows) - first[-1])
             off += n if e < s.E else 0
         bm_dev[:len(rows)].copy_(torch.tensor(rows, dtype=torch.int32))
-        nb_dev.copy_(torch.tensor(nbs, dtype=torch.int32))
+        nb_dev.copy_(torch.tensor([[v, 0, 0, 0] for v in nbs], dtype=torch.int32).view(-1))
         launches = 2
         for mode, act, wt, dst in ((_lib.GATE_UP, x, w.w13, b["h"]), (_lib.DOWN, b["h"], w.w2, b["y"])):
             for e in range(s.E + 1):
                 if nbs[e] == 0:
                     continue
                 _lib.moe_expert_gemm_w4(mode, impl, act, T, s.H, s.F, s.E, s.k, wt, b["perm"], b["topk_w"],
-                                        bm_dev.data_ptr() + 12 * first[e], nb_dev.data_ptr() + 4 * e, bn, dst)
+                                        bm_dev.data_ptr() + 12 * first[e], nb_dev.data_ptr() + 16 * e, bn, dst)
                 launches += 1
         _lib.moe_combine(b["y"], b["inv_perm"], b["topk_w"], out)
         return launches
@@ -406,6 +410,111 @@ def measure_host_synced(args, wl, layer, d, dev):
             "launches_per_step": launches,
             "note": "routing on the GPU, counts to the host (synchronised), block map built on the host, one "
                     "GEMM launch per expert and projection; wall clock per step"}
+
+
+def measure_chain(args, dev, T=1, L=4):
+    """Decode through L layers in sequence (layer.MoEDecodeChain): each layer's logits are the router
+    projection of the previous layer's output, then the fused decode kernel; 2 L launches per step,
+    replayed as one CUDA graph, L2 flushed between steps.  Reports the time per layer and, per layer,
+    the bytes of its touched experts' weights and its router matrix against the HBM roofline."""
+    import torch
+
+    from bit_mixture_experts_gb300 import _lib
+    from bit_mixture_experts_gb300.layer import MoEDecodeChain
+
+    s = workloads.FULL
+    ws = [workloads.make_weights(s, seed=100 + l) for l in range(L)]
+    wrs = [workloads.router_weight_bits(s, seed=100 + l) for l in range(L)]
+    chain = MoEDecodeChain(s.H, s.E, s.k, s.F, ws, wrs, device=dev, impl="gemv")
+    del ws
+    tok = workloads.make_tokens(s, T, seed=7)
+    x = torch.from_numpy(tok["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    for _ in range(max(3, args.warmup)):
+        chain.forward(x)
+    torch.cuda.synchronize()
+    touched = [int((layer.buffers(T)["counts"] > 0).sum().item()) for layer in chain.layers]
+    g = torch.cuda.CUDAGraph()
+    n_cap = _lib.moe_launch_count()
+    with torch.cuda.graph(g):
+        chain.forward(x)
+    launches = _lib.moe_launch_count() - n_cap
+    g.replay()
+    torch.cuda.synchronize()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda._sleep(int(min(100e-3, 0.3e-3 * args.steps + 2e-3) * 2.0e9))
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert _lib.moe_get_device_error() == 0, "device error word set"
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    w13, w2 = expert_bytes(s)
+    # per layer: the touched experts' weights, the router matrix, and x / its norm / out / logits
+    step_bytes = sum((n + 1) * (w13 + w2) for n in touched) + L * (s.E * s.H * 2 + 3 * T * s.H * 2 + T * s.E * 4)
+    peaks = load_peaks()
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    return {"layers": L, "T": T, "ms_per_step": ms, "us_per_layer": 1e3 * ms / L, "value": T * L / (ms * 1e-3),
+            "unit": "layer-tokens/s", "gpu_launches_per_step": int(launches), "touched_experts": touched,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                         "algorithmic_per_step": int(step_bytes),
+                         "note": "per layer: touched experts' W4 weights + the bf16 router matrix + x, logits, out"},
+            "note": "each layer: RMS norm of the previous layer's output (moe_rms_norm), its router logits on the "
+                    "GPU (moe_router), then the fused decode kernel; one CUDA graph per step, L2 flushed between "
+                    "steps"}
+
+
+def measure_unfused(args, wl, d, dev, fused_ms):
+    """Ablation of the fused dequantisation (the pages credit it with +77.4% prefill): the same layer
+    with the weights first expanded to a bf16 copy in HBM (moe_expand_w4), then the same tensor-core
+    kernel reading that copy (MOE_IMPL_TC_BF16).  Two timings: the expansion in every step (the
+    dequantise-then-GEMM pipeline), and a resident bf16 copy (3.6 times the weight bytes per step, and
+    1.6 GB of memory for this layer).  CUDA events on the stream, inputs larger than L2."""
+    import torch
+
+    from bit_mixture_experts_gb300 import _lib
+    from bit_mixture_experts_gb300.layer import MoELayerW4
+
+    s = wl.shape
+    T = wl.T
+    layer = MoELayerW4(s.H, s.E, s.k, s.F, d, device=dev, impl="tc_bf16", block_n=args.block_n)
+    x = torch.from_numpy(d["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.from_numpy(d["logits"]).to(dev)
+    out = torch.empty((T, s.H), dtype=torch.bfloat16, device=dev)
+    p13, p2 = d["w13_packed"].shape, d["w2_packed"].shape
+
+    def timed(expand):
+        for _ in range(max(2, args.warmup)):
+            if expand:
+                layer.expand(layer.w13_r, p13, layer.w13_x)
+                layer.expand(layer.w2_r, p2, layer.w2_x)
+            layer.forward(x, logits, out)
+        torch.cuda.synchronize()
+        n = max(3, min(args.steps, 20))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            if expand:
+                layer.expand(layer.w13_r, p13, layer.w13_x)
+                layer.expand(layer.w2_r, p2, layer.w2_x)
+            layer.forward(x, logits, out)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    ms_expand = timed(True)
+    ms_resident = timed(False)
+    assert _lib.moe_get_device_error() == 0, "device error word set"
+    bf16_bytes = layer.w13_x.numel() + layer.w2_x.numel()
+    return {"expand_every_step_ms": ms_expand, "resident_bf16_copy_ms": ms_resident, "fused_ms_per_step": fused_ms,
+            "fused_speedup_vs_expand": ms_expand / fused_ms, "fused_speedup_vs_resident": ms_resident / fused_ms,
+            "bf16_copy_bytes": int(bf16_bytes),
+            "note": "moe_expand_w4 (bf16 copy of all 257 experts' weights) then the tensor-core kernel on that "
+                    "copy; same results bit for bit"}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -433,6 +542,8 @@ def run_ours(args, rank, world, local_rank):
         if name == args.workload:
             primary_d = d
         results[name] = measure_workload(args, wl, layer, d, rank, world, dev)
+    if not args.only and rank == 0 and world == 1:
+        results["decode1_chain4"] = measure_chain(args, dev, T=1, L=4)
     ablations = {}
     if not args.no_ablations and rank == 0 and world == 1 and args.workload in ("prefill512", "prefill4k"):
         wl = workloads.WORKLOADS[args.workload]
@@ -441,6 +552,7 @@ def run_ours(args, rank, world, local_rank):
         hs["fused_ms_per_step"] = results[args.workload]["ms_per_step"]
         hs["fused_speedup"] = hs["ms_per_step"] / results[args.workload]["ms_per_step"]
         ablations["host_synced_routing"] = hs
+        ablations["unfused_dequant"] = measure_unfused(args, wl, primary_d, dev, results[args.workload]["ms_per_step"])
     if clocks:
         clocks.stop()
     p = results[args.workload]
@@ -462,7 +574,9 @@ def run_ours(args, rank, world, local_rank):
         "ablations": ablations,
         "workloads_note": ("the other workloads of the metric, each timed the same way right after the primary "
                            "one (same clocks record); prefill4k and skew16k report the gate/up kernel against the "
-                           "bf16 tensor peak, decode1/decode8 the fused decode kernel against HBM"),
+                           "bf16 tensor peak, decode1/decode8 the fused decode kernel against HBM; decode1_chain4 "
+                           "is batch-1 decode through four dependent layers (router projection + fused decode "
+                           "kernel per layer)"),
     }
     if clocks:
         res["clocks"] = clocks.summary()

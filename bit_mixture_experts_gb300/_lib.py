@@ -20,12 +20,12 @@ ERRORS = {-1: "MOE_ERR_NULL", -2: "MOE_ERR_ALIGN", -3: "MOE_ERR_SHAPE", -4: "MOE
 DEVICE_ERRORS = {0: "ok", 1: "MOE_DEV_BAD_BLOCK", 2: "MOE_DEV_BAD_INDEX", 3: "MOE_DEV_TIMEOUT", 4: "MOE_DEV_BAD_WORKSPACE"}
 
 GATE_UP, DOWN = 0, 1
-IMPL_AUTO, IMPL_TC, IMPL_GEMV, IMPL_TC2 = 0, 2, 3, 4
-IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV, "tc2": IMPL_TC2}
+IMPL_AUTO, IMPL_TC, IMPL_GEMV, IMPL_TC2, IMPL_TC_BF16 = 0, 2, 3, 4, 5
+IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV, "tc2": IMPL_TC2, "tc_bf16": IMPL_TC_BF16}
 
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
-SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_route_x", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
-           "moe_repacked_bytes", "moe_repack_w4", "moe_expert_gemm_w4", "moe_combine", "moe_decode_workspace_size",
+SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_route_x", "moe_router", "moe_rms_norm", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
+           "moe_repacked_bytes", "moe_repack_w4", "moe_expanded_bytes", "moe_expand_w4", "moe_expert_gemm_w4", "moe_combine", "moe_decode_workspace_size",
            "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns"]
 
 
@@ -56,7 +56,11 @@ _SIGS = {
     "moe_route": ([_vp, _i, _i, _i, _i] + [_vp] * 9 + [_sz, _vp], _i),
     "moe_route_noalloc": ([_vp, _i, _i, _i, _i] + [_vp] * 9, _i),
     "moe_route_x": ([_vp, _vp, _i, _i, _i, _i, _i] + [_vp] * 10 + [_sz, _vp], _i),
+    "moe_router": ([_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
+    "moe_rms_norm": ([_vp, _vp, _i, _i, ctypes.c_float, _vp], _i),
     "moe_repacked_bytes": ([_i, _i, _i], _sz),
+    "moe_expanded_bytes": ([_i, _i, _i], _sz),
+    "moe_expand_w4": ([_vp, _i, _i, _i, _vp, _vp], _i),
     "moe_repack_w4": ([_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp], _i),
     "moe_expert_gemm_w4": ([_i, _i, _vp, _i, _i, _i, _i, _i] + [_vp] * 5 + [_i, _vp, _vp], _i),
     "moe_combine": ([_vp, _vp, _vp, _vp, _i, _i, _i, _vp], _i),
@@ -149,6 +153,20 @@ def moe_route_x(x, w_router, k, block_n, logits, topk_ids, topk_w, counts, offse
           _ptr(workspace), ws_bytes, _stream(stream))
 
 
+def moe_router(x, w_router, k, logits, topk_ids, topk_w, stream=None):
+    """Router projection and top-k only (x bf16 [T, H], w_router bf16 [E, H] -> logits, ids, weights)."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    _call("moe_router", _ptr(x), _ptr(w_router), T, H, E, k, _ptr(logits), _ptr(topk_ids), _ptr(topk_w),
+          _stream(stream))
+
+
+def moe_rms_norm(x, out, eps=1e-6, stream=None):
+    """out = bf16(x / rms(x)) per token (x, out bf16 [T, H] on the device)."""
+    T, H = x.shape
+    _call("moe_rms_norm", _ptr(x), _ptr(out), T, H, float(eps), _stream(stream))
+
+
 def moe_route_noalloc(logits, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks,
                       stream=None):
     """moe_route with the library's own fixed scratch instead of a workspace (no allocation)."""
@@ -161,6 +179,15 @@ def moe_repack_w4(packed, scale, bias, gate_up, out, stream=None):
     n_mat, rows, kw = packed.shape
     _call("moe_repack_w4", _ptr(packed), _ptr(scale), _ptr(bias), n_mat, rows, kw * 8, int(gate_up), _ptr(out),
           _stream(stream))
+
+
+def moe_expanded_bytes(n_mat, rows, K) -> int:
+    return load().moe_expanded_bytes(n_mat, rows, K)
+
+
+def moe_expand_w4(w_repacked, n_mat, rows, K, out, stream=None):
+    """The unfused path's bf16 copy of repacked 4-bit weights (for IMPL_TC_BF16)."""
+    _call("moe_expand_w4", _ptr(w_repacked), n_mat, rows, K, _ptr(out), _stream(stream))
 
 
 def moe_expert_gemm_w4(mode, impl, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks, block_n, out,

@@ -48,6 +48,7 @@ size_t route_workspace_bytes(int T, int E, int k);
 cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32_t* ids, float* w, int32_t* counts,
                          int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm, int32_t* nb, void* ws,
                          size_t ws_bytes, cudaStream_t s, int ids_given);
+cudaError_t launch_rms_norm(const uint16_t* x, uint16_t* out, int T, int H, float eps, int num_sms, cudaStream_t s);
 cudaError_t launch_router(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
                           int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T,
@@ -69,7 +70,10 @@ cudaError_t launch_decode(const uint16_t* x, const float* logits, const void* w1
 unsigned long long wait_limit_ns();
 cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                            const int32_t* perm, const float* topk_w, const int32_t* block_map,
-                           const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s);
+                           const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s,
+                           bool raw);
+size_t expanded_bytes(int n_mat, int rows, int K);
+cudaError_t launch_expand(const void* w4, int n_mat, int rows, int K, void* out, cudaStream_t s);
 cudaError_t launch_gemm_pair(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                              const int32_t* perm, const int32_t* block_map, const int32_t* num_blocks, int bn, int cap,
                              void* out, cudaStream_t s);
@@ -121,6 +125,25 @@ int moe_route(const float* logits, int T, int E, int k, int block_n, int32_t* to
                                   reinterpret_cast<cudaStream_t>(stream), 0));
 }
 
+int moe_rms_norm(const uint16_t* x, uint16_t* out, int T, int H, float eps, moe_stream_t stream) {
+  if (T < 1 || T > (1 << 20) || H < 8 || H % 8 != 0 || !(eps >= 0.0f)) return MOE_ERR_SHAPE;
+  int rc = check_ptrs(x, out);
+  if (rc) return rc;
+  return cuda_status(launch_rms_norm(x, out, T, H, eps, num_sms(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_router(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
+               int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+  int rc = check_route_shape(T, E, k, 1);
+  if (rc) return rc;
+  if (H < 64 || H % 64 != 0 || E % 64 != 0 || E > 512) return MOE_ERR_SHAPE;
+  rc = check_ptrs(x, w_router, logits, topk_ids, topk_w);
+  if (rc) return rc;
+  if (!device_error_ptr()) return MOE_ERR_CUDA;
+  return cuda_status(launch_router(x, w_router, T, H, E, k, logits, topk_ids, topk_w,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_route_x(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, int block_n, float* logits,
                 int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* perm,
                 int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks, void* workspace,
@@ -153,11 +176,12 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
   rc = check_ptrs(act, w_packed, perm, topk_w, block_map, num_blocks, out);
   if (rc) return rc;
   if (impl == MOE_IMPL_AUTO) impl = block_n <= gemv_max_rows() ? MOE_IMPL_GEMV : MOE_IMPL_TC;
-  if (impl != MOE_IMPL_GEMV && impl != MOE_IMPL_TC && impl != MOE_IMPL_TC2) return MOE_ERR_MODE;
-  // the kernels step K and M by 128; the GEMV takes tiles of at most 8 rows, the tensor-core kernel
+  if (impl != MOE_IMPL_GEMV && impl != MOE_IMPL_TC && impl != MOE_IMPL_TC2 && impl != MOE_IMPL_TC_BF16)
+    return MOE_ERR_MODE;
+  // the kernels step K and M by 128; the GEMV takes tiles of at most 8 rows, the tensor-core kernels
   // 128, the CTA-pair kernel 256
   if (H % 128 != 0 || F % 128 != 0) return MOE_ERR_SHAPE;
-  if (block_n > (impl == MOE_IMPL_GEMV ? gemv_max_rows() : impl == MOE_IMPL_TC ? 128 : 256)) return MOE_ERR_SHAPE;
+  if (block_n > (impl == MOE_IMPL_GEMV ? gemv_max_rows() : impl == MOE_IMPL_TC2 ? 256 : 128)) return MOE_ERR_SHAPE;
   if (!device_error_ptr()) return MOE_ERR_CUDA;
   const int cap = moe_block_map_capacity(T, E, k, block_n);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -168,7 +192,19 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
     return cuda_status(launch_gemm_pair(mode, act, T, H, F, E, k, w_packed, perm, block_map, num_blocks, block_n,
                                         cap, out, s));
   return cuda_status(launch_gemm_tc(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
-                                    block_n, cap, out, num_sms(), s));
+                                    block_n, cap, out, num_sms(), s, impl == MOE_IMPL_TC_BF16));
+}
+
+size_t moe_expanded_bytes(int n_mat, int rows, int K) {
+  if (n_mat < 1 || rows < 128 || rows % 128 != 0 || K < 64 || K % 64 != 0) return 0;
+  return expanded_bytes(n_mat, rows, K);
+}
+
+int moe_expand_w4(const void* w_repacked, int n_mat, int rows, int K, void* out, moe_stream_t stream) {
+  if (n_mat < 1 || rows < 128 || rows % 128 != 0 || K < 64 || K % 64 != 0) return MOE_ERR_SHAPE;
+  int rc = check_ptrs(w_repacked, out);
+  if (rc) return rc;
+  return cuda_status(launch_expand(w_repacked, n_mat, rows, K, out, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T, int H,

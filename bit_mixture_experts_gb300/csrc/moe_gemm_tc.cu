@@ -82,14 +82,22 @@ constexpr int EPI_ROWS = 32;     // output rows per epilogue chunk (one tcgen05.
 constexpr int STAGE_BYTES = 2 * EPI_ROWS * TC_M * 2;  // epilogue staging: two chunks of 32 rows x 128 bf16
 constexpr int EPI_BAR = 1;       // named barrier of the four epilogue warps
 
+// Pre-expanded weights (the unfused comparison path, moe_expand_w4): per
+// (matrix, M-tile, K group) one block of 128 rows x 64 bf16; the 16-byte
+// chunk i of row L sits at chunk position i ^ (L & 7), so that the 32 rows a
+// warp reads at once fall in different banks.
+constexpr int RAW_BLOCK = TC_M * KG * 2;
+
 // Sizes that depend on MG, the M-tiles per work unit (they share each
-// activation stage), and GPS, the quant groups per pipeline stage.  The ring
-// depths are chosen at launch from the shared memory available.
-template <int MG, int GPS>
+// activation stage), GPS, the quant groups per pipeline stage, and RAW (the
+// weights arrive already expanded to bf16).  The ring depths are chosen at
+// launch from the shared memory available.
+template <int MG, int GPS, bool RAW = false>
 struct UnitCfg {
-  static constexpr int W_STAGE = MG * GPS * W_BLOCK;         // packed weights of one stage
+  static constexpr int WB = RAW ? RAW_BLOCK : W_BLOCK;       // bytes of one (M-tile, K group) block
+  static constexpr int W_STAGE = MG * GPS * WB;              // weights of one stage
   static constexpr int A_COLS = MG * GPS * 32;               // TMEM columns of one dequantised stage
-  static_assert((GPS * W_BLOCK) % 16 == 0, "bulk copies move multiples of 16 bytes");
+  static_assert((GPS * WB) % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
 
 
@@ -194,14 +202,15 @@ __device__ __forceinline__ bool unit_tile(const TcParams& p, int u, int MGT, Til
 //      gate/up: cp.async gather of token rows (warps 2-3),
 //      down: TMA tiles of contiguous h rows (warp 2)  -> MMA
 //   D  FP32 accumulators, TMEM, MMA -> epilogue (1 or 2 buffers)
-template <int MODE, int MG, int GPS>
+template <int MODE, int MG, int GPS, bool RAW = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmap_act) {
   static_assert(MODE == 1 || MG == 2, "gate/up pairs the gate and the up M-tile in one unit");
   static_assert(MG == 1 || MG == 2, "one or two M-tiles per unit");
   static_assert(GPS == 2 || (GPS == 4 && MODE == 1 && MG == 1), "2-group stages, or 4 for the one-M-tile down GEMM");
-  constexpr int W_STAGE = UnitCfg<MG, GPS>::W_STAGE;
-  constexpr int A_COLS = UnitCfg<MG, GPS>::A_COLS;
+  constexpr int W_STAGE = UnitCfg<MG, GPS, RAW>::W_STAGE;
+  constexpr int A_COLS = UnitCfg<MG, GPS, RAW>::A_COLS;
+  constexpr int WB = UnitCfg<MG, GPS, RAW>::WB;
   const int NW = p.nw;
   const int W_RING_BYTES = NW * W_STAGE;
   constexpr int KS = KG * GPS;               // K per stage
@@ -276,15 +285,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int grp;
       if (!unit_tile(p, u, MGT, &t, &grp)) continue;
       const int nm = min(MG, MT - grp * MG);
-      const uint8_t* g0 = p.w + (static_cast<size_t>(t.expert) * MT + grp * MG) * KT * static_cast<size_t>(W_BLOCK);
+      const uint8_t* g0 = p.w + (static_cast<size_t>(t.expert) * MT + grp * MG) * KT * static_cast<size_t>(WB);
       for (int ks = 0; ks < NS; ++ks, ++it) {
         const int s = it % NW, r = it / NW;
         if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim, p.sleep_ns)) goto wprod_done;
         const uint32_t dst = sbase + off_w + s * W_STAGE;
-        ptx::mbar_arrive_expect_tx_elect(bar(BAR_WFULL + s), static_cast<uint32_t>(nm * GPS * W_BLOCK));
+        ptx::mbar_arrive_expect_tx_elect(bar(BAR_WFULL + s), static_cast<uint32_t>(nm * GPS * WB));
         for (int m = 0; m < nm; ++m)
-          ptx::bulk_g2s_elect(dst + m * GPS * W_BLOCK, g0 + (static_cast<size_t>(m) * KT + ks * GPS) * W_BLOCK,
-                              GPS * W_BLOCK, bar(BAR_WFULL + s));
+          ptx::bulk_g2s_elect(dst + m * GPS * WB, g0 + (static_cast<size_t>(m) * KT + ks * GPS) * WB, GPS * WB,
+                              bar(BAR_WFULL + s));
       }
     }
   wprod_done:;
@@ -444,13 +453,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int sa = it % NA, sw = it % NW;
         if (!wait_warp(bar(BAR_WFULL + sw), (it / NW) & 1, s_abort, p.err, lim, p.sleep_ns)) goto dequant_done;
         const uint8_t* ws = smem + off_w + sw * W_STAGE;
+        if (RAW) {
+          // weights already expanded: this thread's row of every block goes to TMEM as it is
+          if (it >= NA && !wait_warp(bar(BAR_AEMPTY + sa), ((it / NA) - 1) & 1, s_abort, p.err, lim, p.sleep_ns))
+            goto dequant_done;
+          const uint32_t ta = trow + sa * A_COLS;
+#pragma unroll
+          for (int m = 0; m < MG; ++m) {
+            if (m >= nm) break;
+#pragma unroll
+            for (int g = 0; g < GPS; ++g) {
+              const uint4* row = reinterpret_cast<const uint4*>(ws + (m * GPS + g) * WB + L * 128);
+              uint32_t v[32];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint4 c = row[i ^ (L & 7)];
+                v[4 * i] = c.x;
+                v[4 * i + 1] = c.y;
+                v[4 * i + 2] = c.z;
+                v[4 * i + 3] = c.w;
+              }
+              ptx::tmem_st_32x32b_x32(ta + m * GPS * 32 + g * 32, v);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(BAR_WEMPTY + sw));  // the rows are in registers (and stored)
+        } else {
         uint4 pk[MG][GPS][2];
         uint32_t sbw[MG][GPS];
 #pragma unroll
         for (int m = 0; m < MG; ++m)
 #pragma unroll
           for (int g = 0; g < GPS; ++g) {
-            const uint8_t* blk = ws + (m * GPS + g) * W_BLOCK;
+            const uint8_t* blk = ws + (m * GPS + g) * WB;
             if (m < nm) {
               pk[m][g][0] = *reinterpret_cast<const uint4*>(blk + L * 16);
               pk[m][g][1] = *reinterpret_cast<const uint4*>(blk + 2048 + L * 16);
@@ -477,6 +512,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             expand_group(pk[m][g][0], pk[m][g][1], sbw[m][g], v);
             ptx::tmem_st_32x32b_x32(ta + m * GPS * 32 + g * 32, v);
           }
+        }
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -621,6 +657,43 @@ __global__ void repack_kernel(const uint32_t* __restrict__ packed, const uint16_
   }
 }
 
+// --------------------------------------------------------------------------
+// expansion of repacked 4-bit weights into a bf16 copy in the same tile order
+// (the unfused path: what the fused kernels never write), blocks of 128 rows
+// x 64 bf16 with row L's 16-byte chunk i at position i ^ (L & 7).
+// --------------------------------------------------------------------------
+__global__ void expand_kernel(const uint8_t* __restrict__ w4, size_t blocks, uint8_t* __restrict__ out) {
+  const size_t total = blocks * TC_M;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int L = static_cast<int>(idx % TC_M);
+    const size_t b = idx / TC_M;
+    const uint8_t* blk = w4 + b * W_BLOCK;
+    const uint4 p0 = *reinterpret_cast<const uint4*>(blk + L * 16);
+    const uint4 p1 = *reinterpret_cast<const uint4*>(blk + 2048 + L * 16);
+    const uint32_t sb = *reinterpret_cast<const uint32_t*>(blk + W_PACKED + L * 4);
+    uint32_t v[32];
+    expand_group(p0, p1, sb, v);
+    uint4* row = reinterpret_cast<uint4*>(out + b * RAW_BLOCK + L * 128);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) row[i ^ (L & 7)] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+size_t expanded_bytes(int n_mat, int rows, int K) {
+  return static_cast<size_t>(n_mat) * (rows / TC_M) * (K / KG) * RAW_BLOCK;
+}
+
+cudaError_t launch_expand(const void* w4, int n_mat, int rows, int K, void* out, cudaStream_t s) {
+  const size_t blocks = static_cast<size_t>(n_mat) * (rows / TC_M) * (K / KG);
+  size_t grid = (blocks * TC_M + 255) / 256;
+  if (grid > 65535) grid = 65535;
+  expand_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<const uint8_t*>(w4), blocks,
+                                                            static_cast<uint8_t*>(out));
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 size_t repacked_bytes(int n_mat, int rows, int K) {
   return static_cast<size_t>(n_mat) * (rows / TC_M) * (K / KG) * W_BLOCK;
 }
@@ -678,7 +751,8 @@ int max_dyn_smem() {
 
 cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                            const int32_t* perm, const float* topk_w, const int32_t* block_map,
-                           const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s) {
+                           const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s,
+                           bool raw) {
   TcParams prm;
   prm.act = act;
   prm.w = static_cast<const uint8_t*>(w);
@@ -704,20 +778,22 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   // M-tiles per unit: gate/up pairs gate and up; the down GEMM keeps two accumulator buffers
   const int MG = (mode == MOE_GATE_UP_SWIGLU || boxr <= 64) ? 2 : 1;
   // quant groups per stage: the one-M-tile down GEMM takes 4 (16 MMAs per stage, as the two-M-tile units)
-  const int GPS = (MG == 1 && F % (4 * KG) == 0) ? 4 : 2;
+  // (two for pre-expanded weights, whose four-group stages would not fit twice beside the activations)
+  const int GPS = (MG == 1 && F % (4 * KG) == 0 && !raw) ? 4 : 2;
   prm.sb = GPS * boxr * 128;
-  const int w_stage = MG == 2 ? UnitCfg<2, 2>::W_STAGE : GPS == 4 ? UnitCfg<1, 4>::W_STAGE : UnitCfg<1, 2>::W_STAGE;
+  const int w_stage = (raw ? RAW_BLOCK : W_BLOCK) * MG * GPS;
   const int a_cols = MG == 2 ? UnitCfg<2, 2>::A_COLS : GPS == 4 ? UnitCfg<1, 4>::A_COLS : UnitCfg<1, 2>::A_COLS;
   const int fixed = BAR_BYTES + MISC_BYTES + STAGE_BYTES;
   const int total = max_dyn_smem() - 1024 - fixed;
   // shared memory: three activation stages when that leaves four weight slots (else two), the
   // weight ring up to NWMAX slots, then more activation stages with what is left
+  const int min_w = raw ? 2 : 4;  // pre-expanded stages are 3.6 times larger
   int nbs = 0, nws = 0;
-  for (int want = 3; want >= 2 && nws < 4; --want) {
+  for (int want = 3; want >= 2 && nws < min_w; --want) {
     nbs = want;
     nws = (total - nbs * prm.sb) / w_stage;
   }
-  if (nws < 4 || nbs < 2) return cudaErrorInvalidValue;
+  if (nws < min_w || nbs < 2) return cudaErrorInvalidValue;
   if (nws > NWMAX) nws = NWMAX;
   nbs = (total - nws * w_stage) / prm.sb;
   if (nbs > NBMAX) nbs = NBMAX;
@@ -749,10 +825,15 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  void (*kern)(const TcParams, const CUtensorMap) = mode == MOE_GATE_UP_SWIGLU ? gemm_tc_kernel<0, 2, 2>
-                                                    : MG == 2                    ? gemm_tc_kernel<1, 2, 2>
-                                                    : GPS == 4                   ? gemm_tc_kernel<1, 1, 4>
-                                                                                 : gemm_tc_kernel<1, 1, 2>;
+  void (*kern)(const TcParams, const CUtensorMap) =
+      raw ? (mode == MOE_GATE_UP_SWIGLU ? gemm_tc_kernel<0, 2, 2, true>
+             : MG == 2                  ? gemm_tc_kernel<1, 2, 2, true>
+             : GPS == 4                 ? gemm_tc_kernel<1, 1, 4, true>
+                                        : gemm_tc_kernel<1, 1, 2, true>)
+          : (mode == MOE_GATE_UP_SWIGLU ? gemm_tc_kernel<0, 2, 2>
+             : MG == 2                  ? gemm_tc_kernel<1, 2, 2>
+             : GPS == 4                 ? gemm_tc_kernel<1, 1, 4>
+                                        : gemm_tc_kernel<1, 1, 2>);
   const cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (ea != cudaSuccess) return ea;
   kern<<<num_sms, NTHREADS, smem, s>>>(prm, tmap);

@@ -9,7 +9,7 @@ import numpy as np
 
 from . import _lib
 
-DEFAULT_BLOCK_N = {_lib.IMPL_TC: 128, _lib.IMPL_GEMV: 8, _lib.IMPL_TC2: 128}
+DEFAULT_BLOCK_N = {_lib.IMPL_TC: 128, _lib.IMPL_GEMV: 8, _lib.IMPL_TC2: 128, _lib.IMPL_TC_BF16: 128}
 DECODE_MAX_T = 16  # token counts up to this take the GEMV kernel under impl="auto"
 
 
@@ -23,7 +23,7 @@ def default_block_n(impl: int, T: int, E: int, k: int) -> int:
     give the grid more tiles; from there on 128-row tiles halve the
     dequantisation per token.  The GEMV kernel takes tiles of up to 8 rows.
     """
-    if impl in (_lib.IMPL_TC, _lib.IMPL_TC2) and T * k < 64 * E:
+    if impl in (_lib.IMPL_TC, _lib.IMPL_TC2, _lib.IMPL_TC_BF16) and T * k < 64 * E:
         return 64
     return DEFAULT_BLOCK_N[impl]
 
@@ -62,7 +62,13 @@ class MoELayerW4:
         self.w13_r = self._repack(w["w13_packed"], w["w13_scale"], w["w13_bias"],
                                   gate_up=2 if self.impl == _lib.IMPL_TC2 else 1)
         self.w2_r = self._repack(w["w2_packed"], w["w2_scale"], w["w2_bias"], gate_up=False)
-        self.weights = _lib.Weights(self.w13_r.data_ptr(), self.w2_r.data_ptr())
+        if self.impl == _lib.IMPL_TC_BF16:
+            # the unfused comparison path: a resident bf16 copy of the expanded weights
+            self.w13_x = self.expand(self.w13_r, w["w13_packed"].shape)
+            self.w2_x = self.expand(self.w2_r, w["w2_packed"].shape)
+            self.weights = _lib.Weights(self.w13_x.data_ptr(), self.w2_x.data_ptr())
+        else:
+            self.weights = _lib.Weights(self.w13_r.data_ptr(), self.w2_r.data_ptr())
         self._bufs = {}
 
     def _repack(self, packed, scale, bias, gate_up):
@@ -71,6 +77,15 @@ class MoELayerW4:
         nbytes = _lib.moe_repacked_bytes(n_mat, rows, kw * 8)
         out = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         _lib.moe_repack_w4(packed, scale, bias, gate_up, out)
+        return out
+
+    def expand(self, repacked, packed_shape, out=None):
+        """bf16 copy of repacked weights (moe_expand_w4) for packed canonical shape [n_mat, rows, K/8]."""
+        import torch
+        n_mat, rows, kw = packed_shape
+        if out is None:
+            out = torch.empty(_lib.moe_expanded_bytes(n_mat, rows, kw * 8), dtype=torch.uint8, device=self.device)
+        _lib.moe_expand_w4(repacked, n_mat, rows, kw * 8, out)
         return out
 
     def impl_for(self, T):
@@ -136,3 +151,53 @@ class MoELayerW4:
         _lib.moe_layer_forward_host(x_host, logits_host, out_host, stage["x"], stage["logits"], stage["out"], T,
                                     self.H, self.F, self.E, self.k, self.block_n_for(T), self.impl_for(T), self.weights,
                                     b["struct"], stream)
+
+
+class MoEDecodeChain:
+    """Several MoE layers in sequence for small-batch decode (T <= 8 with the GEMV kernel): layer l's
+    input is the RMS norm of layer l-1's output (of x for layer 0), and its router logits are its own
+    router projection of that input (moe_router, tensor cores), so the layers depend on each other as
+    in a model's decode step.  Three launches per layer: moe_rms_norm, moe_router, then
+    moe_layer_forward (the fused decode kernel), all on one stream and capturable as one CUDA graph.
+
+    `layer_weights` holds one canonical weight dict per layer (as MoELayerW4 takes), `router_bits` one
+    bf16 router matrix [E, H] (uint16 bits) per layer.
+    """
+
+    def __init__(self, H, E, k, F, layer_weights, router_bits, device="cuda", impl="auto", block_n=None):
+        import torch
+        assert len(layer_weights) == len(router_bits) >= 1
+        self.H, self.E, self.k, self.F = H, E, k, F
+        self.device = torch.device(device)
+        self.layers = [MoELayerW4(H, E, k, F, w, device=self.device, impl=impl, block_n=block_n)
+                       for w in layer_weights]
+        self.wr = [_dev(np.asarray(b, dtype=np.uint16), self.device) for b in router_bits]
+        self._bufs = {}
+
+    def buffers(self, T):
+        """Per-layer outputs (bf16 [T, H]), logits (fp32 [T, E]) and the router's top-k scratch."""
+        import torch
+        if T not in self._bufs:
+            dev, L = self.device, len(self.layers)
+            self._bufs[T] = {
+                "xn": [torch.empty((T, self.H), dtype=torch.bfloat16, device=dev) for _ in range(L)],
+                "out": [torch.empty((T, self.H), dtype=torch.bfloat16, device=dev) for _ in range(L)],
+                "logits": [torch.empty((T, self.E), dtype=torch.float32, device=dev) for _ in range(L)],
+                "ids": [torch.empty((T, self.k), dtype=torch.int32, device=dev) for _ in range(L)],
+                "w": [torch.empty((T, self.k), dtype=torch.float32, device=dev) for _ in range(L)],
+            }
+            for layer in self.layers:
+                layer.buffers(T)
+        return self._bufs[T]
+
+    def forward(self, x, stream=None):
+        """x bf16 [T, H] on the device -> the last layer's output (a buffer of the chain)."""
+        T = x.shape[0]
+        b = self.buffers(T)
+        cur = x
+        for l, layer in enumerate(self.layers):
+            _lib.moe_rms_norm(cur, b["xn"][l], stream=stream)
+            _lib.moe_router(b["xn"][l], self.wr[l], self.k, b["logits"][l], b["ids"][l], b["w"][l], stream)
+            layer.forward(b["xn"][l], b["logits"][l], b["out"][l], stream)
+            cur = b["out"][l]
+        return cur

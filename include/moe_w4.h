@@ -80,8 +80,11 @@ enum {
   MOE_IMPL_AUTO = 0,      /* GEMV when block_n <= 8, else the tensor-core kernel */
   MOE_IMPL_TC = 2,        /* tcgen05 kernel, one CTA per work unit */
   MOE_IMPL_GEMV = 3,      /* decode GEMV kernel, mma.sync */
-  MOE_IMPL_TC2 = 4        /* tcgen05 kernel on CTA pairs (.cta_group::2): gate/up weights repacked
+  MOE_IMPL_TC2 = 4,       /* tcgen05 kernel on CTA pairs (.cta_group::2): gate/up weights repacked
                              with gate_up = 2 (interleaved tiles); tiles of up to 256 rows */
+  MOE_IMPL_TC_BF16 = 5    /* the unfused comparison path: the tcgen05 kernel over weights already
+                             expanded to bf16 by moe_expand_w4 (3.6 times the bytes of the 4-bit
+                             weights); same results as MOE_IMPL_TC */
 };
 
 /* ------------------------------------------------------------------------ */
@@ -153,6 +156,17 @@ int moe_route_x(const uint16_t* x, const uint16_t* w_router, int T, int H, int E
                 void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * moe_router -- the first kernel of moe_route_x alone: logits = x w_router^T
+ * and the top-k ids and weights, one launch.  For callers that route
+ * elsewhere, such as moe_layer_forward's fused decode kernel (which takes the
+ * logits and recomputes the same top-k with the rest of the routing): a
+ * batch-1 decode step through several layers is then two launches per layer,
+ * each layer's output the next layer's x.  Same limits as moe_route_x.
+ */
+int moe_router(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
+               int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/*
  * moe_route_noalloc -- moe_route for callers that may not allocate device
  * memory: code handed only its input and output buffers by a host engine
  * whose allocator owns the whole device (a serving process that reserves
@@ -180,6 +194,14 @@ int moe_route_noalloc(const float* logits, int T, int E, int k, int block_n,
                       int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
                       int32_t* perm, int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks,
                       moe_stream_t stream);
+
+/*
+ * moe_rms_norm -- out[t] = bf16(x[t] / sqrt(mean_c x[t, c]^2 + eps)), unit
+ * gain, FP32 sum of squares, each output rounded once: the glue that
+ * normalises a layer's input when several layers run in sequence (the
+ * decode chain).  x, out bf16 [T, H], H % 8 == 0; out may not overlap x.
+ */
+int moe_rms_norm(const uint16_t* x, uint16_t* out, int T, int H, float eps, moe_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Weights                                                                  */
@@ -214,6 +236,22 @@ size_t moe_repacked_bytes(int n_mat, int rows, int K);
 int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t* bias,
                   int n_mat, int rows, int K, int gate_up, void* out, moe_stream_t stream);
 
+/*
+ * moe_expand_w4 -- the unfused path's first step: expand repacked 4-bit
+ * weights (moe_repack_w4's output for n_mat matrices of rows x K) into a bf16
+ * copy in HBM, in the same tile order (per matrix, 128-row tile, 64-wide K
+ * group: 128 rows x 64 bf16, the 16-byte chunk i of row L stored at position
+ * i ^ (L & 7)), each weight bf16(q * scale + bias) as the fused kernels
+ * compute it.  moe_expert_gemm_w4 with MOE_IMPL_TC_BF16 reads this copy.
+ * The pages credit fusing the dequantisation into the grouped GEMM, with no
+ * full bf16 copy ever written, with +77.4% prefill throughput ("Perplexity
+ * Open Sources Lily", TL;DR; the itinai.com post on the same engine,
+ * paragraph 2); this pair of calls is the path that claim is measured against.
+ * out: moe_expanded_bytes(n_mat, rows, K) bytes.
+ */
+size_t moe_expanded_bytes(int n_mat, int rows, int K);
+int moe_expand_w4(const void* w_repacked, int n_mat, int rows, int K, void* out, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Grouped expert GEMM                                                      */
 /* ------------------------------------------------------------------------ */
@@ -238,9 +276,10 @@ int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t*
  *        nibbles with each 64-group's bf16 scale and bias in the same block).
  * block_map / num_blocks: moe_route's outputs for the same block_n.
  * impl: MOE_IMPL_*.  AUTO takes GEMV for block_n <= 8 and TC otherwise.  TC
- * needs block_n <= 128, TC2 block_n <= 256 (and gate/up weights repacked with
- * gate_up = 2); GEMV (decode: tiles of at most 8 token rows) needs block_n <=
- * 8; all need H % 128 == 0 and F % 128 == 0.  Returns
+ * and TC_BF16 need block_n <= 128, TC2 block_n <= 256 (and gate/up weights
+ * repacked with gate_up = 2); GEMV (decode: tiles of at most 8 token rows)
+ * needs block_n <= 8; all need H % 128 == 0 and F % 128 == 0.  TC_BF16 reads
+ * the bf16 copy of moe_expand_w4 instead of the 4-bit weights.  Returns
  * MOE_ERR_SHAPE when the chosen kernel cannot take the shape and
  * MOE_ERR_MODE for an unknown mode or impl.
  */

@@ -19,17 +19,36 @@ def bf16_of_bits(b: int) -> float:
 
 
 def rne_bf16(v: float) -> float:
-    """Round a float64 to bf16 (8 significant bits), ties to even, on its bit pattern."""
-    if v == 0.0:
+    """Round a float64 to bf16 (8 significant bits, float32's exponent range), ties to even, on
+    its bit pattern: drop the float64 fraction bits bf16 does not keep -- 45 of 52 for normal
+    results, more below 2**-126 where bf16's spacing stays 2**-133 -- and round on the rest."""
+    if v == 0.0 or v != v or abs(v) == float("inf"):
         return v
     u = struct.unpack("<Q", struct.pack("<d", v))[0]
-    drop = 52 - 7                      # fraction bits float64 keeps beyond bf16's 7
-    keep = u >> drop
-    rem = u & ((1 << drop) - 1)
+    sign = u >> 63
+    exp = (u >> 52) & 0x7FF                  # biased float64 exponent of |v|
+    drop = 52 - 7                             # fraction bits float64 keeps beyond bf16's 7
+    mag = u & ((1 << 63) - 1)
+    if exp - 1023 < -126:
+        # bf16 subnormal: spacing 2**-133; a float64 |v| = mant * 2**(exp-1075) with the implicit
+        # bit in mant, so the bits below 2**-133 are the lowest (-133) - (exp - 1075) of mant
+        mant = (mag & ((1 << 52) - 1)) | (1 << 52)
+        shift = (1075 - 133) - exp + 0        # bits of mant below the 2**-133 place
+        if shift > 60:
+            return -0.0 if sign else 0.0
+        keep, rem, half = mant >> shift, mant & ((1 << shift) - 1), 1 << (shift - 1)
+        if rem > half or (rem == half and (keep & 1)):
+            keep += 1
+        return (-1.0 if sign else 1.0) * keep * 2.0 ** -133
+    keep = mag >> drop
+    rem = mag & ((1 << drop) - 1)
     half = 1 << (drop - 1)
     if rem > half or (rem == half and (keep & 1)):
         keep += 1
-    return struct.unpack("<d", struct.pack("<Q", keep << drop))[0]
+    r = struct.unpack("<d", struct.pack("<Q", (keep << drop) | (sign << 63)))[0]
+    if abs(r) > (2.0 - 2.0 ** -7) * 2.0 ** 127:
+        return -float("inf") if sign else float("inf")
+    return r
 
 
 def nibble(word: int, i: int) -> int:

@@ -44,14 +44,21 @@ def bf16_value(bits) -> np.ndarray:
 def round_bf16(a) -> np.ndarray:
     """Round float64 values to the nearest bf16 value, ties to even.
 
-    bf16 keeps 8 significant bits.  With a = m * 2**e, 0.5 <= |m| < 1, the
-    rounded value is rint(m * 2**8) * 2**(e-8); numpy's rint rounds half to
-    even.  Only the normal range occurs in this layer (no subnormal or
-    overflowing values are produced by the synthetic inputs).
+    bf16 keeps 8 significant bits and float32's exponent range.  With
+    a = m * 2**e, 0.5 <= |m| < 1, a normal result (|a| >= 2**-126) is
+    rint(m * 2**8) * 2**(e-8); below 2**-126 the spacing stays 2**-133 (the
+    subnormals), so tiny values round to a multiple of it (possibly to a signed
+    zero).  Values past the largest finite bf16 round to infinity.  numpy's rint
+    rounds half to even.
     """
     a = np.asarray(a, dtype=np.float64)
-    m, e = np.frexp(a)
-    return np.ldexp(np.rint(m * 256.0), e - 8)
+    _, e = np.frexp(a)
+    q = np.where(e >= -125, e - 8, -133)         # exponent of the spacing at a
+    r = np.ldexp(np.rint(np.ldexp(a, -q)), q)
+    return np.where(np.abs(r) > BF16_MAX, np.copysign(np.inf, a), r)
+
+
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
 
 
 def unpack_u4(packed) -> np.ndarray:
@@ -73,6 +80,21 @@ def dequant(packed, scale_bits, bias_bits) -> np.ndarray:
     s = np.repeat(bf16_value(scale_bits), GROUP, axis=-1)
     b = np.repeat(bf16_value(bias_bits), GROUP, axis=-1)
     return round_bf16(q * s + b)
+
+
+# --------------------------------------------------------------------------- #
+# between layers
+# --------------------------------------------------------------------------- #
+RMS_EPS = 1e-6
+
+
+def rms_norm(x_bits, eps: float = RMS_EPS) -> np.ndarray:
+    """Unit-gain RMS norm of each token, the input of a layer in a stack of layers:
+    bf16(x / sqrt(mean(x^2) + eps)), computed in float64 and rounded once.  The pages do
+    not describe the model's normalisation; this is the plainest one."""
+    x = bf16_value(x_bits)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return round_bf16(x * r)
 
 
 # --------------------------------------------------------------------------- #
@@ -195,10 +217,11 @@ def expert_swiglu(xrows, w13) -> np.ndarray:
 
 
 def bf16_floor_ceil(a):
-    """The two bf16 values enclosing a (equal when a is a bf16 value)."""
+    """The two bf16 values enclosing a (equal when a is a bf16 value), subnormals included."""
     a = np.asarray(a, dtype=np.float64)
-    m, e = np.frexp(a)
-    return np.ldexp(np.floor(m * 256.0), e - 8), np.ldexp(np.ceil(m * 256.0), e - 8)
+    _, e = np.frexp(a)
+    q = np.where(e >= -125, e - 8, -133)
+    return np.ldexp(np.floor(np.ldexp(a, -q)), q), np.ldexp(np.ceil(np.ldexp(a, -q)), q)
 
 
 def expert_down_exact(h, w2) -> np.ndarray:

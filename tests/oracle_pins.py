@@ -70,7 +70,11 @@ def pin_round_bf16_library():
     r = np.random.default_rng(1)
     v = np.concatenate([r.standard_normal(20000) * 10.0 ** r.integers(-6, 6, 20000),
                         # exact ties: 9 significant bits with the last one set
-                        (r.integers(256, 512, 4000) * 2 + 1) * 2.0 ** r.integers(-20, 20, 4000)]
+                        (r.integers(256, 512, 4000) * 2 + 1) * 2.0 ** r.integers(-20, 20, 4000),
+                        # the subnormal range (|v| < 2^-126, spacing 2^-133), ties there, and near the top
+                        r.standard_normal(4000) * 2.0 ** r.integers(-149, -120, 4000),
+                        (r.integers(0, 256, 1000) * 2 + 1) * 2.0 ** -134,
+                        r.uniform(3.0e38, 3.4e38, 1000) * r.choice([-1, 1], 1000)]
                        ).astype(np.float32)
     ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
     got = moe_ref.round_bf16(v.astype(np.float64))
@@ -78,9 +82,10 @@ def pin_round_bf16_library():
 
 
 def pin_round_bf16_bitlevel():
-    """round_bf16 on arbitrary float64 values equals the bit-level brute force."""
+    """round_bf16 on arbitrary float64 values equals the bit-level brute force (subnormals included)."""
     r = np.random.default_rng(2)
-    v = r.standard_normal(3000) * 10.0 ** r.integers(-5, 5, 3000)
+    v = np.concatenate([r.standard_normal(3000) * 10.0 ** r.integers(-5, 5, 3000),
+                        r.standard_normal(1000) * 2.0 ** r.integers(-150, -118, 1000)])
     for a in v:
         assert moe_ref.round_bf16(np.array([a]))[0] == brute.rne_bf16(float(a)), a
 
@@ -343,6 +348,22 @@ def pin_router_logits_exact_sum(T=3, H=128, E=5, seed=13):
             assert got[t, e] == np.float32(math.fsum(x[t] * w[e])), (t, e)
 
 
+def pin_rms_norm(T=4, H=64, seed=14):
+    """RMS norm: a constant row becomes all +-1 (up to eps, which bf16 cannot see), and every output is
+    the brute-force x / sqrt(mean x^2 + eps) rounded once to bf16."""
+    const = np.array([[2.5] * H, [-0.375] * H], dtype=np.float32)
+    got = moe_ref.rms_norm(workloads.f32_to_bf16_bits(const))
+    assert np.array_equal(got, np.sign(const.astype(np.float64)))
+    r = np.random.default_rng(seed)
+    xb = workloads.f32_to_bf16_bits((r.standard_normal((T, H)) * 3).astype(np.float32))
+    got = moe_ref.rms_norm(xb)
+    for t in range(T):
+        row = [brute.bf16_of_bits(b) for b in xb[t]]
+        scale = 1.0 / math.sqrt(math.fsum(v * v for v in row) / H + moe_ref.RMS_EPS)
+        for c in range(H):
+            assert got[t, c] == brute.rne_bf16(row[c] * scale), (t, c)
+
+
 def pin_bruteforce_layer(shape=None, T=None, seed=0):
     """The vectorised oracle equals the per-token brute force on the tiny workload."""
     wl = workloads.WORKLOADS["tiny"] if shape is None else workloads.custom(T, *shape)
@@ -358,5 +379,5 @@ ALL_PINS = [
     pin_round_bf16_library, pin_round_bf16_bitlevel, pin_dequant_golden, pin_dequant_exact_fraction,
     pin_unpack_order, pin_routing_golden, pin_topk_bruteforce, pin_topk_softmax_library,
     pin_routing_invariants, pin_closed_form_constant, pin_closed_form_permutation, pin_closed_form_scaled_down,
-    pin_router_logits_integer, pin_router_logits_exact_sum,
+    pin_router_logits_integer, pin_router_logits_exact_sum, pin_rms_norm,
 ]

@@ -120,6 +120,18 @@ def test_layer_prefill512_all_outputs(impl):
     G.check_layer(d, layer, got, what=f"prefill512 {impl}, all tokens")
 
 
+@pytest.mark.parametrize("name", [(300, 512, 32, 4, 256, False), (600, 256, 8, 2, 256, False), "prefill512"],
+                         ids=["T300", "T600", "prefill512"])
+def test_unfused_path_equals_fused(name):
+    """The unfused comparison path (weights expanded to a bf16 copy by moe_expand_w4, then the tensor-core
+    kernel reading that copy) gives bit for bit the outputs of the fused kernel, and passes the oracle check."""
+    d = G.workload(name)
+    (fused,), _ = run_layer(d, "tc")
+    (unfused,), layer = run_layer(d, "tc_bf16")
+    assert np.array_equal(fused, unfused)
+    G.check_layer(d, layer, unfused, what=f"unfused {name}")
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_gate_up_intermediate(impl):
     """The gate/up GEMM alone: h = bf16(silu(g) u) per permuted row against the oracle's h."""

@@ -97,7 +97,7 @@ def _mutations():
     orig = {n: getattr(moe_ref, n) for n in
             ("unpack_u4", "dequant", "expert_swiglu_exact", "topk_route", "expert_down_exact",
              "expert_weights", "stable_permutation", "round_bf16", "block_map", "exclusive_scan",
-             "router_logits")}
+             "router_logits", "rms_norm")}
 
     def msb_first(p):
         q = orig["unpack_u4"](p)
@@ -162,7 +162,12 @@ def _mutations():
     def router_reversed_k(x_bits, wr_bits):
         return orig["router_logits"](np.asarray(x_bits)[:, ::-1], np.asarray(wr_bits))
 
+    def rms_sum_not_mean(x_bits, eps=moe_ref.RMS_EPS):
+        x = moe_ref.bf16_value(x_bits)
+        return moe_ref.round_bf16(x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps))
+
     return {
+        "rms_norm_sum_not_mean": ("rms_norm", rms_sum_not_mean),
         "router_drops_last_k": ("router_logits", router_drops_last_k),
         "router_reversed_k": ("router_logits", router_reversed_k),
         "nibble_msb_first": ("unpack_u4", msb_first),
