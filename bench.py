@@ -173,6 +173,8 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
     stream = torch.cuda.current_stream()
     impl, bn = layer.impl_for(T), layer.block_n_for(T)
     w = layer.weights
+    fused_combine = impl == _lib.IMPL_TC and b.get("combine_ws") is not None
+    nseg = 3 if fused_combine else 4
 
     def step(ev=None):
         if ev is not None:
@@ -185,6 +187,13 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
                                 b["block_map"], b["num_blocks"], bn, b["h"])
         if ev is not None:
             ev[2].record(stream)
+        if fused_combine:
+            # the layer's own path with the tensor-core kernel: the combine in the down GEMM's epilogue
+            _lib.moe_down_combine(b["h"], T, s.H, s.F, s.E, s.k, w.w2, b["perm"], b["inv_perm"], b["topk_w"],
+                                  b["block_map"], b["num_blocks"], bn, b["y"], out, b["combine_ws"])
+            if ev is not None:
+                ev[3].record(stream)
+            return
         _lib.moe_expert_gemm_w4(_lib.DOWN, impl, b["h"], T, s.H, s.F, s.E, s.k, w.w2, b["perm"], b["topk_w"],
                                 b["block_map"], b["num_blocks"], bn, b["y"])
         if ev is not None:
@@ -216,7 +225,7 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
             flush.zero_()
         step(events[i])
     torch.cuda.synchronize()
-    seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(4)] for i in range(args.steps)])
+    seg = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(nseg)] for i in range(args.steps)])
     assert _lib.moe_get_device_error() == 0, "device error word set"
 
     # the step captured once as a CUDA graph (the library launches only on the given stream and never
@@ -328,9 +337,13 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
                f"inputs larger than L2 ({work['step_bytes'] / 1e6:.0f} MB streamed per step)"),
         "stages_note": ("eager launches of the four entry points (moe_route, gate/up and down moe_expert_gemm_w4, "
                         "moe_combine); the timed step is the fused decode kernel") if fused_decode else
+                       ("eager launches of the three entry points (moe_route, gate/up moe_expert_gemm_w4, "
+                        "moe_down_combine); the timed step replays the same launches") if fused_combine else
                        "eager launches of the four entry points; the timed step replays the same launches",
-        "stages_ms": {"route": float(seg[:, 0].mean()), "gate_up": gu_ms, "down": float(seg[:, 2].mean()),
-                      "combine": float(seg[:, 3].mean())},
+        "stages_ms": ({"route": float(seg[:, 0].mean()), "gate_up": gu_ms, "down_combine": float(seg[:, 2].mean())}
+                      if fused_combine else
+                      {"route": float(seg[:, 0].mean()), "gate_up": gu_ms, "down": float(seg[:, 2].mean()),
+                       "combine": float(seg[:, 3].mean())}),
         "roofline": roof,
         "layer_roofline": {"tflops": layer_tflops, "frac_bf16": layer_tflops / peaks["bf16_tflops"],
                            "hbm_gbs": layer_gbs, "frac_hbm": layer_gbs / peaks["hbm_gbs"],
@@ -463,9 +476,8 @@ def measure_chain(args, dev, T=1, L=4):
                          "frac": gbs / peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "algorithmic_per_step": int(step_bytes),
                          "note": "per layer: touched experts' W4 weights + the bf16 router matrix + x, logits, out"},
-            "note": "each layer: RMS norm of the previous layer's output (moe_rms_norm), its router logits on the "
-                    "GPU (moe_router), then the fused decode kernel; one CUDA graph per step, L2 flushed between "
-                    "steps"}
+            "note": "each layer: RMS norm of the previous layer's output and its router logits (moe_norm_router, "
+                    "one launch), then the fused decode kernel; one CUDA graph per step, L2 flushed between steps"}
 
 
 def measure_unfused(args, wl, d, dev, fused_ms):
@@ -517,6 +529,65 @@ def measure_unfused(args, wl, d, dev, fused_ms):
                     "copy; same results bit for bit"}
 
 
+def measure_fused_combine(args, wl, layer, d, dev):
+    """Ablation of the combine's own launch: the step with the combine in the down GEMM's epilogue
+    (moe_down_combine; same bits) against the step as the layer runs it (down GEMM, then moe_combine).
+    CUDA events on the stream around each eager step, L2 flushed between steps."""
+    import torch
+
+    from bit_mixture_experts_gb300 import _lib
+
+    s = wl.shape
+    T = wl.T
+    x = torch.from_numpy(d["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.from_numpy(d["logits"]).to(dev)
+    out = torch.empty((T, s.H), dtype=torch.bfloat16, device=dev)
+    ref = torch.empty_like(out)
+    b = layer.buffers(T)
+    impl, bn = layer.impl_for(T), layer.block_n_for(T)
+    if impl != _lib.IMPL_TC:
+        return None
+    w = layer.weights
+    ws = torch.zeros(_lib.moe_down_combine_workspace_size(T, s.H) // 4, dtype=torch.int32, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(fused, o):
+        _lib.moe_route(logits, s.k, bn, b["topk_ids"], b["topk_w"], b["counts"], b["offsets"], b["perm"],
+                       b["inv_perm"], b["block_map"], b["num_blocks"], b["workspace"])
+        _lib.moe_expert_gemm_w4(_lib.GATE_UP, impl, x, T, s.H, s.F, s.E, s.k, w.w13, b["perm"], b["topk_w"],
+                                b["block_map"], b["num_blocks"], bn, b["h"])
+        if fused:
+            _lib.moe_down_combine(b["h"], T, s.H, s.F, s.E, s.k, w.w2, b["perm"], b["inv_perm"], b["topk_w"],
+                                  b["block_map"], b["num_blocks"], bn, b["y"], o, ws)
+        else:
+            _lib.moe_expert_gemm_w4(_lib.DOWN, impl, b["h"], T, s.H, s.F, s.E, s.k, w.w2, b["perm"], b["topk_w"],
+                                    b["block_map"], b["num_blocks"], bn, b["y"])
+            _lib.moe_combine(b["y"], b["inv_perm"], b["topk_w"], o)
+
+    def timed(fused, o):
+        for _ in range(max(3, args.warmup)):
+            step(fused, o)
+        n = max(3, min(args.steps, 30))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record()
+            step(fused, o)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b_) for a, b_ in ev]))
+
+    ms_sep = timed(False, ref)
+    ms_fused = timed(True, out)
+    assert _lib.moe_get_device_error() == 0, "device error word set"
+    return {"fused_combine_ms_per_step": ms_fused, "separate_combine_ms_per_step": ms_sep,
+            "same_output": bool(torch.equal(out.view(torch.int16), ref.view(torch.int16))),
+            "workspace_left_zero": int(ws.count_nonzero().item()) == 0,
+            "note": "eager steps (route, gate/up, then moe_down_combine or down GEMM + moe_combine); the layer "
+                    "keeps the separate combine, which measures faster"}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -552,6 +623,7 @@ def run_ours(args, rank, world, local_rank):
         hs["fused_ms_per_step"] = results[args.workload]["ms_per_step"]
         hs["fused_speedup"] = hs["ms_per_step"] / results[args.workload]["ms_per_step"]
         ablations["host_synced_routing"] = hs
+        ablations["fused_combine"] = measure_fused_combine(args, wl, layer, primary_d, dev)
         ablations["unfused_dequant"] = measure_unfused(args, wl, primary_d, dev, results[args.workload]["ms_per_step"])
     if clocks:
         clocks.stop()

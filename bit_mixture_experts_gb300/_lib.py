@@ -24,7 +24,8 @@ IMPL_AUTO, IMPL_TC, IMPL_GEMV, IMPL_TC2, IMPL_TC_BF16 = 0, 2, 3, 4, 5
 IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV, "tc2": IMPL_TC2, "tc_bf16": IMPL_TC_BF16}
 
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
-SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_route_x", "moe_router", "moe_rms_norm", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
+SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_route_x", "moe_router", "moe_rms_norm", "moe_norm_router",
+           "moe_down_combine", "moe_down_combine_workspace_size", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
            "moe_repacked_bytes", "moe_repack_w4", "moe_expanded_bytes", "moe_expand_w4", "moe_expert_gemm_w4", "moe_combine", "moe_decode_workspace_size",
            "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns"]
 
@@ -45,7 +46,8 @@ class Weights(ctypes.Structure):
 class Buffers(ctypes.Structure):
     _fields_ = [("topk_ids", _vp), ("topk_w", _vp), ("counts", _vp), ("offsets", _vp), ("perm", _vp),
                 ("inv_perm", _vp), ("block_map", _vp), ("num_blocks", _vp), ("h", _vp), ("y", _vp),
-                ("workspace", _vp), ("workspace_bytes", _sz), ("decode_ws", _vp), ("decode_ws_bytes", _sz)]
+                ("workspace", _vp), ("workspace_bytes", _sz), ("decode_ws", _vp), ("decode_ws_bytes", _sz),
+                ("combine_ws", _vp), ("combine_ws_bytes", _sz)]
 
 
 _SIGS = {
@@ -58,6 +60,9 @@ _SIGS = {
     "moe_route_x": ([_vp, _vp, _i, _i, _i, _i, _i] + [_vp] * 10 + [_sz, _vp], _i),
     "moe_router": ([_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
     "moe_rms_norm": ([_vp, _vp, _i, _i, ctypes.c_float, _vp], _i),
+    "moe_norm_router": ([_vp, _vp, _i, _i, _i, ctypes.c_float, _vp, _vp, _vp], _i),
+    "moe_down_combine_workspace_size": ([_i, _i], _sz),
+    "moe_down_combine": ([_vp, _i, _i, _i, _i, _i] + [_vp] * 6 + [_i, _vp, _vp, _vp, _sz, _vp], _i),
     "moe_repacked_bytes": ([_i, _i, _i], _sz),
     "moe_expanded_bytes": ([_i, _i, _i], _sz),
     "moe_expand_w4": ([_vp, _i, _i, _i, _vp, _vp], _i),
@@ -167,6 +172,14 @@ def moe_rms_norm(x, out, eps=1e-6, stream=None):
     _call("moe_rms_norm", _ptr(x), _ptr(out), T, H, float(eps), _stream(stream))
 
 
+def moe_norm_router(x, w_router, x_norm, logits, eps=1e-6, stream=None):
+    """Decode step (T <= 8): x_norm = rms_norm(x) and logits = x_norm w_router^T in one launch."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    _call("moe_norm_router", _ptr(x), _ptr(w_router), T, H, E, float(eps), _ptr(x_norm), _ptr(logits),
+          _stream(stream))
+
+
 def moe_route_noalloc(logits, k, block_n, topk_ids, topk_w, counts, offsets, perm, inv_perm, block_map, num_blocks,
                       stream=None):
     """moe_route with the library's own fixed scratch instead of a workspace (no allocation)."""
@@ -201,6 +214,19 @@ def moe_combine(y, inv_perm, topk_w, out, stream=None):
     T, k = topk_w.shape
     H = out.shape[1]
     _call("moe_combine", _ptr(y), _ptr(inv_perm), _ptr(topk_w), _ptr(out), T, H, k, _stream(stream))
+
+
+def moe_down_combine_workspace_size(T, H) -> int:
+    return int(load().moe_down_combine_workspace_size(T, H))
+
+
+def moe_down_combine(h, T, H, F, E, k, w_packed, perm, inv_perm, topk_w, block_map, num_blocks, block_n, y, out,
+                     workspace, stream=None):
+    """The down GEMM with the combine in its epilogue (y and out written; workspace zero-filled once)."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _call("moe_down_combine", _ptr(h), T, H, F, E, k, _ptr(w_packed), _ptr(perm), _ptr(inv_perm), _ptr(topk_w),
+          _ptr(block_map), _ptr(num_blocks), block_n, _ptr(y), _ptr(out), _ptr(workspace), ws_bytes,
+          _stream(stream))
 
 
 def moe_decode_workspace_size(T, H) -> int:

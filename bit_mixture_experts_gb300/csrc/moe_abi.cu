@@ -49,6 +49,9 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
                          int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* bm, int32_t* nb, void* ws,
                          size_t ws_bytes, cudaStream_t s, int ids_given);
 cudaError_t launch_rms_norm(const uint16_t* x, uint16_t* out, int T, int H, float eps, int num_sms, cudaStream_t s);
+int norm_router_max_tokens();
+cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* wr, uint16_t* xn, float* logits, int T, int H,
+                               int E, float eps, cudaStream_t s);
 cudaError_t launch_router(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
                           int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T,
@@ -71,7 +74,7 @@ unsigned long long wait_limit_ns();
 cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                            const int32_t* perm, const float* topk_w, const int32_t* block_map,
                            const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s,
-                           bool raw);
+                           bool raw, uint16_t* cmb_out, const int32_t* inv_perm, int* cmb_cnt);
 size_t expanded_bytes(int n_mat, int rows, int K);
 cudaError_t launch_expand(const void* w4, int n_mat, int rows, int K, void* out, cudaStream_t s);
 cudaError_t launch_gemm_pair(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
@@ -130,6 +133,16 @@ int moe_rms_norm(const uint16_t* x, uint16_t* out, int T, int H, float eps, moe_
   int rc = check_ptrs(x, out);
   if (rc) return rc;
   return cuda_status(launch_rms_norm(x, out, T, H, eps, num_sms(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_norm_router(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, float eps, uint16_t* x_norm,
+                    float* logits, moe_stream_t stream) {
+  if (T < 1 || T > norm_router_max_tokens() || H < 8 || H % 8 != 0 || E < 1 || E > 1024 || !(eps >= 0.0f))
+    return MOE_ERR_SHAPE;
+  int rc = check_ptrs(x, w_router, x_norm, logits);
+  if (rc) return rc;
+  return cuda_status(
+      launch_norm_router(x, w_router, x_norm, logits, T, H, E, eps, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_router(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, int k, float* logits,
@@ -192,7 +205,30 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
     return cuda_status(launch_gemm_pair(mode, act, T, H, F, E, k, w_packed, perm, block_map, num_blocks, block_n,
                                         cap, out, s));
   return cuda_status(launch_gemm_tc(mode, act, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
-                                    block_n, cap, out, num_sms(), s, impl == MOE_IMPL_TC_BF16));
+                                    block_n, cap, out, num_sms(), s, impl == MOE_IMPL_TC_BF16, nullptr, nullptr,
+                                    nullptr));
+}
+
+size_t moe_down_combine_workspace_size(int T, int H) {
+  if (T < 1 || T > (1 << 20) || H < 128 || H % 128 != 0) return 0;
+  return static_cast<size_t>(T) * (H / 128) * sizeof(int32_t);
+}
+
+int moe_down_combine(const uint16_t* h, int T, int H, int F, int E, int k, const void* w_packed, const int32_t* perm,
+                     const int32_t* inv_perm, const float* topk_w, const int32_t* block_map,
+                     const int32_t* num_blocks, int block_n, uint16_t* y, uint16_t* out, void* workspace,
+                     size_t workspace_bytes, moe_stream_t stream) {
+  int rc = check_shape(T, H, F, E, k, block_n);
+  if (rc) return rc;
+  if (H % 128 != 0 || F % 128 != 0 || block_n > 128) return MOE_ERR_SHAPE;
+  rc = check_ptrs(h, w_packed, perm, inv_perm, topk_w, block_map, num_blocks, y, out, workspace);
+  if (rc) return rc;
+  if (workspace_bytes < moe_down_combine_workspace_size(T, H)) return MOE_ERR_WORKSPACE;
+  if (!device_error_ptr()) return MOE_ERR_CUDA;
+  const int cap = moe_block_map_capacity(T, E, k, block_n);
+  return cuda_status(launch_gemm_tc(MOE_DOWN, h, T, H, F, E, k, w_packed, perm, topk_w, block_map, num_blocks,
+                                    block_n, cap, y, num_sms(), reinterpret_cast<cudaStream_t>(stream), false, out,
+                                    inv_perm, static_cast<int*>(workspace)));
 }
 
 size_t moe_expanded_bytes(int n_mat, int rows, int K) {
@@ -247,6 +283,12 @@ int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out, int
   rc = moe_expert_gemm_w4(MOE_GATE_UP_SWIGLU, impl, x, T, H, F, E, k, w->w13, b->perm, b->topk_w, b->block_map,
                           b->num_blocks, block_n, b->h, stream);
   if (rc) return rc;
+  const int resolved = impl == MOE_IMPL_AUTO ? (block_n <= gemv_max_rows() ? MOE_IMPL_GEMV : MOE_IMPL_TC) : impl;
+  if (resolved == MOE_IMPL_TC && b->combine_ws) {
+    // the down GEMM with the combine in its epilogue (one launch fewer, y read back from L2 at once)
+    return moe_down_combine(b->h, T, H, F, E, k, w->w2, b->perm, b->inv_perm, b->topk_w, b->block_map,
+                            b->num_blocks, block_n, b->y, out, b->combine_ws, b->combine_ws_bytes, stream);
+  }
   rc = moe_expert_gemm_w4(MOE_DOWN, impl, b->h, T, H, F, E, k, w->w2, b->perm, b->topk_w, b->block_map,
                           b->num_blocks, block_n, b->y, stream);
   if (rc) return rc;

@@ -242,20 +242,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *s_tmem;
   const unsigned long long lim = p.wait_cycles;
   int prod_b = 0;  // activation TMA stages issued (down), for the drain after a timeout
-  int prod_w = 0;  // weight stages issued, for the drain after a timeout
+  // Weight ring: the two dequant warpgroups take alternate stages (warpgroup it & 1), and each
+  // owns every other slot -- warpgroup w's c-th stage goes to slot 2 (c % (NW / 2)) + w, fill
+  // c / (NW / 2) -- so a slot's fills are always consumed by one warpgroup in order.  (With shared
+  // slots a warpgroup could wait for a slot's next fill while the other's fill before it is still
+  // landing, and a parity wait cannot tell those two phases apart.)
+  int prod_wc[2] = {0, 0};  // weight stages issued per consuming warpgroup (also for the drain)
 
   if (warp == 0) {
     // ------------------------------------------------ weight producer: this SM's M-tile
-    int& it = prod_w;
+    const int HW = NW / 2;
+    int it = 0;  // stages of every unit, as the dequant warpgroups count them
     for (int u = cid; u < units; u += ncl) {
       Tile t;
       int grp;
       if (!unit_tile(p, u, MGT, &t, &grp)) continue;
       const int m = 2 * grp + static_cast<int>(rank);
-      if (m >= MT) continue;  // odd M-tile count: the odd CTA has no rows in the last pair
+      if (m >= MT) {  // odd M-tile count: the odd CTA has no rows in the last pair
+        it += NS;
+        continue;
+      }
       const uint8_t* g0 = p.w + (static_cast<size_t>(t.expert) * MT + m) * KT * static_cast<size_t>(W_BLOCK);
       for (int ks = 0; ks < NS; ++ks, ++it) {
-        const int s = it % NW, r = it / NW;
+        const int wg = it & 1, c = prod_wc[wg]++;
+        const int s = 2 * (c % HW) + wg, r = c / HW;
         if (r > 0 && !wait_warp(bar(BAR_WEMPTY + s), (r - 1) & 1, s_abort, p.err, lim, p.sleep_ns)) goto wprod_done;
         ptx::mbar_arrive_expect_tx_elect(bar(BAR_WFULL + s), static_cast<uint32_t>(W_STAGE));
         ptx::bulk_g2s_elect(sbase + off_w + s * W_STAGE, g0 + static_cast<size_t>(ks) * GPS * W_BLOCK, W_STAGE,
@@ -411,20 +421,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int L = 32 * q + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16) + A0;
     int it = 0;   // stages of every unit (A ring, warpgroup turn)
-    int wt = 0;   // stages of the units with rows in this CTA (W ring)
+    int wc = 0;   // this warpgroup's stages with rows in this CTA (its half of the W ring)
+    const int HW = NW / 2;
     for (int u = cid; u < units; u += ncl) {
       Tile t;
       int grp;
       if (!unit_tile(p, u, MGT, &t, &grp)) continue;
       const bool has = 2 * grp + static_cast<int>(rank) < MT;
       for (int ks = 0; ks < NS; ++ks, ++it) {
-        const int wt_here = wt;
-        if (has) ++wt;
         if ((it & 1) != wg) continue;
         const int sa = it % NA;
         if (has) {
-          const int sw = wt_here % NW;
-          if (!wait_warp(bar(BAR_WFULL + sw), (wt_here / NW) & 1, s_abort, p.err, lim, p.sleep_ns)) goto dequant_done;
+          const int c = wc++;
+          const int sw = 2 * (c % HW) + wg;
+          if (!wait_warp(bar(BAR_WFULL + sw), (c / HW) & 1, s_abort, p.err, lim, p.sleep_ns)) goto dequant_done;
           const uint8_t* ws = smem + off_w + sw * W_STAGE;
           uint4 pk[GPS][2];
           uint32_t sbw[GPS];
@@ -548,8 +558,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       wait_drain(bar(BAR_BFULL + t % NB), (t / NB) & 1, lim);
   }
   if (*s_abort && warp == 0 && lane == 0) {
-    for (int t = prod_w - NW < 0 ? 0 : prod_w - NW; t < prod_w; ++t)
-      wait_drain(bar(BAR_WFULL + t % NW), (t / NW) & 1, lim);
+    for (int w = 0; w < 2; ++w)
+      for (int c = prod_wc[w] - NW / 2 < 0 ? 0 : prod_wc[w] - NW / 2; c < prod_wc[w]; ++c)
+        wait_drain(bar(BAR_WFULL + 2 * (c % (NW / 2)) + w), (c / (NW / 2)) & 1, lim);
   }
   // neither CTA leaves (or releases the pair's TMEM) while the other may still use its shared or
   // tensor memory
@@ -637,6 +648,7 @@ cudaError_t launch_gemm_pair(int mode, const uint16_t* act, int T, int H, int F,
   }
   if (nws < 4 || nbs < 2) return cudaErrorInvalidValue;
   if (nws > NWMAX) nws = NWMAX;
+  nws &= ~1;  // an even depth: half of the slots for each dequant warpgroup
   nbs = (total - nws * w_stage) / prm.sb;
   if (nbs > NBMAX) nbs = NBMAX;
   prm.nb = nbs;

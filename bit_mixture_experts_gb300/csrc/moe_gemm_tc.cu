@@ -80,6 +80,8 @@ constexpr int BAR_BYTES = (NBAR * 8 + 15) & ~15;
 constexpr int MISC_BYTES = 16;  // abort flag, TMEM base
 constexpr int EPI_ROWS = 32;     // output rows per epilogue chunk (one tcgen05.ld x32)
 constexpr int STAGE_BYTES = 2 * EPI_ROWS * TC_M * 2;  // epilogue staging: two chunks of 32 rows x 128 bf16
+constexpr int COMB_MAX = 2 * TC_M;      // (token, channel block) pairs one down unit can complete
+constexpr int COMB_BYTES = 16 + 4 * COMB_MAX;  // their count and list (down GEMM with the combine)
 constexpr int EPI_BAR = 1;       // named barrier of the four epilogue warps
 
 // Pre-expanded weights (the unfused comparison path, moe_expand_w4): per
@@ -109,6 +111,11 @@ struct TcParams {
   const int32_t* block_map;
   const int32_t* num_blocks;
   void* out;
+  // down GEMM with the combine (null otherwise): the token order output, the routing's inverse
+  // permutation, and one counter per (token, 128-channel block), zero when the call begins
+  uint16_t* cmb_out;
+  const int32_t* inv_perm;
+  int* cmb_cnt;
   int* err;
   unsigned long long wait_cycles;
   uint32_t sleep_ns;  // suspend hint of the waits: min(20 us, the wait limit)
@@ -226,6 +233,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + off_w + W_RING_BYTES + BAR_BYTES);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + off_w + W_RING_BYTES + BAR_BYTES + 4);
   uint16_t* s_stage = reinterpret_cast<uint16_t*>(smem + off_w + W_RING_BYTES + BAR_BYTES + MISC_BYTES);
+  int* s_ncomb = reinterpret_cast<int*>(smem + off_w + W_RING_BYTES + BAR_BYTES + MISC_BYTES + STAGE_BYTES);
+  int* s_comb = s_ncomb + 4;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = MODE == 0 ? p.H : p.F;
@@ -581,7 +590,87 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(BAR_DEMPTY + d));
+      if (lane == 0) ptx::mbar_arrive(bar(BAR_DEMPTY + d));  // the accumulator is free for the next unit
+      if (MODE == 1 && p.cmb_out) {
+        // The combine, fused: every (token, 128-channel block) counts its written y rows; the thread
+        // whose row completes the k + 1 of a pair lists it, and the four warps combine the listed
+        // pairs -- out = bf16(sum_j topk_w[t, j] y[row(t, j)] + y[shared row]), FP32 in moe_combine's
+        // order -- while the MMAs of the next unit already run.  No thread waits for another CTA.
+        const int NCB = p.H / TC_M;
+        if (e == 0) *s_ncomb = 0;
+        ptx::named_bar_sync(EPI_BAR, 128);
+        __threadfence();  // the unit's y stores (all four warps', by the barrier) before this thread's counts
+        for (int i = e; i < t.rows * nm; i += 128) {
+          const int r = i % t.rows, m = i / t.rows;
+          const int row = t.row0 + r;
+          int tok = row - A;
+          if (row < A) {
+            const int a = __ldg(p.perm + row);
+            tok = (a >= 0 && a < A) ? a / p.k : -1;
+          }
+          if (tok < 0) {
+            set_device_error(p.err, MOE_DEV_BAD_INDEX);
+            continue;
+          }
+          int* c = p.cmb_cnt + static_cast<size_t>(tok) * NCB + grp * MG + m;
+          const int before = atomicAdd(c, 1);
+          if (before == p.k) {
+            __threadfence();  // the other CTAs' rows of this pair, before they are read
+            *c = 0;           // left zero for the next call
+            s_comb[atomicAdd(s_ncomb, 1)] = tok * NCB + grp * MG + m;
+          } else if (before < 0 || before > p.k) {
+            set_device_error(p.err, MOE_DEV_BAD_WORKSPACE);
+          }
+        }
+        ptx::named_bar_sync(EPI_BAR, 128);
+        const int ncomb = *s_ncomb;
+        const uint16_t* yb = static_cast<const uint16_t*>(p.out);
+        // half a warp per pair, eight channels per lane; a warp sums two pairs at a time, all of their
+        // row loads issued before the sums
+        const int half = lane >> 4, ch = 8 * (lane & 15);
+        for (int i0 = 2 * q; i0 < ncomb; i0 += 8) {
+          const int it2 = i0 + half;
+          const bool live = it2 < ncomb;
+          const int v = live ? s_comb[it2] : 0, tok = v / NCB, cb = v - tok * NCB;
+          const size_t c0 = static_cast<size_t>(cb) * TC_M + ch;
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int j0 = 0; j0 <= p.k; j0 += 9) {
+            uint4 yv[9];
+            float wv[9];
+#pragma unroll
+            for (int b = 0; b < 9; ++b) {
+              const int j = j0 + b;
+              int row = -1;
+              float w = 0.f;
+              if (live && j < p.k) {
+                row = __ldg(p.inv_perm + static_cast<size_t>(tok) * p.k + j);
+                w = __ldg(p.topk_w + static_cast<size_t>(tok) * p.k + j);
+              } else if (live && j == p.k) {
+                row = A + tok;
+                w = 1.0f;
+              }
+              const bool okr = live && j <= p.k && row >= 0 && row < A + p.T && (j == p.k || row < A);
+              if (live && j <= p.k && !okr) set_device_error(p.err, MOE_DEV_BAD_INDEX);
+              yv[b] = okr ? __ldcg(reinterpret_cast<const uint4*>(yb + static_cast<size_t>(row) * p.H + c0))
+                          : make_uint4(0u, 0u, 0u, 0u);
+              wv[b] = okr ? w : 0.f;
+            }
+#pragma unroll
+            for (int b = 0; b < 9; ++b) {
+              const uint32_t u4[4] = {yv[b].x, yv[b].y, yv[b].z, yv[b].w};
+#pragma unroll
+              for (int h2 = 0; h2 < 4; ++h2) {
+                acc[2 * h2] = fmaf(wv[b], __uint_as_float(u4[h2] << 16), acc[2 * h2]);
+                acc[2 * h2 + 1] = fmaf(wv[b], __uint_as_float(u4[h2] & 0xffff0000u), acc[2 * h2 + 1]);
+              }
+            }
+          }
+          if (live)
+            *reinterpret_cast<uint4*>(p.cmb_out + static_cast<size_t>(tok) * p.H + c0) =
+                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                           pack_bf16x2(acc[6], acc[7]));
+        }
+      }
       ++ui;
     }
   }
@@ -752,8 +841,11 @@ int max_dyn_smem() {
 cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, int E, int k, const void* w,
                            const int32_t* perm, const float* topk_w, const int32_t* block_map,
                            const int32_t* num_blocks, int bn, int cap, void* out, int num_sms, cudaStream_t s,
-                           bool raw) {
+                           bool raw, uint16_t* cmb_out, const int32_t* inv_perm, int* cmb_cnt) {
   TcParams prm;
+  prm.cmb_out = cmb_out;
+  prm.inv_perm = inv_perm;
+  prm.cmb_cnt = cmb_cnt;
   prm.act = act;
   prm.w = static_cast<const uint8_t*>(w);
   prm.perm = perm;
@@ -783,7 +875,7 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   prm.sb = GPS * boxr * 128;
   const int w_stage = (raw ? RAW_BLOCK : W_BLOCK) * MG * GPS;
   const int a_cols = MG == 2 ? UnitCfg<2, 2>::A_COLS : GPS == 4 ? UnitCfg<1, 4>::A_COLS : UnitCfg<1, 2>::A_COLS;
-  const int fixed = BAR_BYTES + MISC_BYTES + STAGE_BYTES;
+  const int fixed = BAR_BYTES + MISC_BYTES + STAGE_BYTES + COMB_BYTES;
   const int total = max_dyn_smem() - 1024 - fixed;
   // shared memory: three activation stages when that leaves four weight slots (else two), the
   // weight ring up to NWMAX slots, then more activation stages with what is left
@@ -795,6 +887,11 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
   }
   if (nws < min_w || nbs < 2) return cudaErrorInvalidValue;
   if (nws > NWMAX) nws = NWMAX;
+  // an even depth: stage it goes to slot it % NW and to dequant warpgroup it % 2, so every slot
+  // keeps one warpgroup.  With an odd depth consecutive fills of a slot alternate between the
+  // warpgroups, and one could wait for a slot's next fill while the other's fill before it is
+  // still landing -- a parity wait cannot tell those two phases apart.
+  nws &= ~1;
   nbs = (total - nws * w_stage) / prm.sb;
   if (nbs > NBMAX) nbs = NBMAX;
   prm.nb = nbs;

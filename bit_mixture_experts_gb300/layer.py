@@ -47,7 +47,7 @@ class MoELayerW4:
     tensors already on the device.
     """
 
-    def __init__(self, H, E, k, F, weights: dict, device="cuda", impl="auto", block_n=None):
+    def __init__(self, H, E, k, F, weights: dict, device="cuda", impl="auto", block_n=None, fuse_combine=False):
         import torch
         self.H, self.E, self.k, self.F = H, E, k, F
         self.device = torch.device(device)
@@ -55,6 +55,10 @@ class MoELayerW4:
         if H % 128 or F % 128:
             raise ValueError(f"H={H} and F={F} must be multiples of 128 (the kernels' K and M steps)")
         self.block_n = block_n  # None: chosen per token count by default_block_n
+        # tensor-core path: the combine in the down GEMM's epilogue (moe_down_combine) instead of its own
+        # launch; off by default, as it measures slower: the epilogue's counts, fences and gathers lengthen
+        # every unit's epilogue beyond the next unit's main loop
+        self.fuse_combine = fuse_combine
         _lib.load()
         w = {n: (v if isinstance(v, torch.Tensor) else _dev(v, self.device)) for n, v in weights.items()
              if n.startswith(("w13_", "w2_"))}
@@ -124,10 +128,14 @@ class MoELayerW4:
         # counters of the fused decode kernel (used for T <= 8 with the GEMV kernel): zero once, left zero
         dws = _lib.moe_decode_workspace_size(T, H)
         t["decode_ws"] = torch.zeros(max(dws, 16), dtype=torch.uint8, device=dev) if dws else None
+        # counters of the down GEMM's fused combine (tensor-core path): zero once, left zero
+        cws = _lib.moe_down_combine_workspace_size(T, H) if self.fuse_combine else 0
+        t["combine_ws"] = torch.zeros(max(cws, 16), dtype=torch.uint8, device=dev) if cws else None
         t["struct"] = _lib.Buffers(*(t[n].data_ptr() for n in ("topk_ids", "topk_w", "counts", "offsets", "perm",
                                                                  "inv_perm", "block_map", "num_blocks", "h", "y",
                                                                  "workspace")), wsb,
-                                   t["decode_ws"].data_ptr() if dws else None, dws)
+                                   t["decode_ws"].data_ptr() if dws else None, dws,
+                                   t["combine_ws"].data_ptr() if cws else None, cws)
         self._bufs[T] = t
         return t
 
@@ -156,9 +164,9 @@ class MoELayerW4:
 class MoEDecodeChain:
     """Several MoE layers in sequence for small-batch decode (T <= 8 with the GEMV kernel): layer l's
     input is the RMS norm of layer l-1's output (of x for layer 0), and its router logits are its own
-    router projection of that input (moe_router, tensor cores), so the layers depend on each other as
-    in a model's decode step.  Three launches per layer: moe_rms_norm, moe_router, then
-    moe_layer_forward (the fused decode kernel), all on one stream and capturable as one CUDA graph.
+    router projection of that input, so the layers depend on each other as in a model's decode step.
+    Two launches per layer: moe_norm_router (the norm and the logits), then moe_layer_forward (the
+    fused decode kernel, which takes the top-k), all on one stream and capturable as one CUDA graph.
 
     `layer_weights` holds one canonical weight dict per layer (as MoELayerW4 takes), `router_bits` one
     bf16 router matrix [E, H] (uint16 bits) per layer.
@@ -196,8 +204,7 @@ class MoEDecodeChain:
         b = self.buffers(T)
         cur = x
         for l, layer in enumerate(self.layers):
-            _lib.moe_rms_norm(cur, b["xn"][l], stream=stream)
-            _lib.moe_router(b["xn"][l], self.wr[l], self.k, b["logits"][l], b["ids"][l], b["w"][l], stream)
+            _lib.moe_norm_router(cur, self.wr[l], b["xn"][l], b["logits"][l], stream=stream)
             layer.forward(b["xn"][l], b["logits"][l], b["out"][l], stream)
             cur = b["out"][l]
         return cur

@@ -203,6 +203,17 @@ int moe_route_noalloc(const float* logits, int T, int E, int k, int block_n,
  */
 int moe_rms_norm(const uint16_t* x, uint16_t* out, int T, int H, float eps, moe_stream_t stream);
 
+/*
+ * moe_norm_router -- a decode step's layer input and router logits in one
+ * launch (at most 8 tokens): x_norm = moe_rms_norm(x) (the same bits) and
+ * logits = x_norm w_router^T (bf16 products, FP32 sums), one warp per expert.
+ * x, x_norm bf16 [T, H]; w_router bf16 [E, H]; logits float32 [T, E].  The
+ * decode chain feeds these to moe_layer_forward, whose fused decode kernel
+ * takes the top-k from the logits.  Returns MOE_ERR_SHAPE for T > 8.
+ */
+int moe_norm_router(const uint16_t* x, const uint16_t* w_router, int T, int H, int E, float eps, uint16_t* x_norm,
+                    float* logits, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Weights                                                                  */
 /* ------------------------------------------------------------------------ */
@@ -303,6 +314,29 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
 int moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, uint16_t* out, int T, int H,
                 int k, moe_stream_t stream);
 
+/*
+ * moe_down_combine -- MOE_DOWN and moe_combine in one launch of the
+ * tensor-core kernel: the down projection writes its bf16 rows y as
+ * moe_expert_gemm_w4 does, and every (token, 128-channel block) counts its
+ * written rows in `workspace`; the epilogue that writes the last of a token's
+ * k + 1 rows of a block combines them there, with moe_combine's arithmetic and
+ * order (so out is bit for bit moe_combine's).  No thread waits for another.
+ * ("Perplexity Open Sources Lily", Technical Details, Model bullet: 8 routed
+ * experts plus one shared expert per token.)
+ * h, perm, inv_perm, topk_w, block_map, num_blocks: as for MOE_DOWN and
+ * moe_combine; y bf16 [A+T, H] (written); out bf16 [T, H].
+ * workspace: moe_down_combine_workspace_size(T, H) bytes (an int32 per token
+ * and 128 channels), zero-filled by the caller before the first call; every
+ * call leaves it zero (a counter found above k is reported as
+ * MOE_DEV_BAD_WORKSPACE).  Needs block_n <= 128, H % 128 == 0, F % 128 == 0.
+ */
+size_t moe_down_combine_workspace_size(int T, int H);
+int moe_down_combine(const uint16_t* h, int T, int H, int F, int E, int k, const void* w_packed,
+                     const int32_t* perm, const int32_t* inv_perm, const float* topk_w,
+                     const int32_t* block_map, const int32_t* num_blocks, int block_n,
+                     uint16_t* y, uint16_t* out, void* workspace, size_t workspace_bytes,
+                     moe_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Whole layer                                                              */
 /* ------------------------------------------------------------------------ */
@@ -324,6 +358,10 @@ typedef struct {
   void* decode_ws;      /* fused decode path: moe_decode_workspace_size bytes, zero before the
                            first call (every call leaves it zero); NULL: never fuse */
   size_t decode_ws_bytes;
+  void* combine_ws;     /* moe_down_combine_workspace_size bytes, zero before the first call;
+                           with the tensor-core kernel the layer then runs moe_down_combine
+                           instead of MOE_DOWN + moe_combine; NULL: the two calls */
+  size_t combine_ws_bytes;
 } moe_buffers_t;
 
 /*

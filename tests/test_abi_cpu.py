@@ -94,6 +94,22 @@ def test_combine_argument_errors(lib):
     assert lib.moe_combine(p, p, ctypes.c_void_p(20), p, 4, 128, 2, None) == -2
 
 
+def test_down_combine_argument_errors(lib):
+    p = ctypes.c_void_p(256)
+    ws = lib.moe_down_combine_workspace_size(16, 256)
+    assert ws == 16 * 2 * 4
+    assert lib.moe_down_combine_workspace_size(16, 192) == 0
+    assert lib.moe_down_combine_workspace_size(0, 256) == 0
+    args = lambda H, F, bn, ptr=p, wsb=ws: lib.moe_down_combine(
+        ptr, 16, H, F, 8, 2, ptr, ptr, ptr, ptr, ptr, ptr, bn, ptr, ptr, ptr, wsb, None)
+    assert args(192, 128, 128) == -3            # H % 128
+    assert args(256, 192, 128) == -3            # F % 128
+    assert args(256, 128, 129) == -3            # tile height above 128
+    assert args(256, 128, 128, ptr=None) == -1
+    assert args(256, 128, 128, ptr=ctypes.c_void_p(260)) == -2
+    assert args(256, 128, 128, wsb=ws - 4) == -4
+
+
 def test_repacked_bytes(lib):
     # one 4608-byte block (2 halves x 128 rows x 16 B of nibbles, then 128 x (scale, bias)) per
     # 128-row tile and 64-wide K group: exactly the bytes of the canonical layout of the matrix

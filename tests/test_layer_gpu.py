@@ -132,6 +132,21 @@ def test_unfused_path_equals_fused(name):
     G.check_layer(d, layer, unfused, what=f"unfused {name}")
 
 
+@pytest.mark.parametrize("name", ["prefill4k"])
+def test_unfused_path_full_size(name):
+    """The unfused comparison path at 4096 tokens (128-row tiles, many work units per CTA, a weight ring
+    of 32 KB stages): bit for bit the fused kernel's outputs, one token per tile against the oracle."""
+    import parity
+    d = G.workload(name)
+    wl = d["workload"]
+    (fused,), _ = run_layer(d, "tc")
+    (unfused,), layer = run_layer(d, "tc_bf16")
+    assert np.array_equal(fused, unfused)
+    a = G.gpu_arrays(layer, wl.T, unfused)
+    toks = parity.tile_tokens(a["block_map"], a["num_blocks"], a["perm"], wl.T, wl.shape.k)
+    G.check_layer(d, layer, unfused, tokens=toks, what=f"unfused {name}, {toks.size} tokens (one per tile)")
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_gate_up_intermediate(impl):
     """The gate/up GEMM alone: h = bf16(silu(g) u) per permuted row against the oracle's h."""
