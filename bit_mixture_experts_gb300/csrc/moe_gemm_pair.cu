@@ -52,6 +52,7 @@
 #include "moe_common.cuh"
 #include "moe_ptx.cuh"
 #include "moe_tc_dev.cuh"
+#include "moe_tmap.cuh"
 
 namespace moe {
 
@@ -575,25 +576,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // --------------------------------------------------------------------------
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn_pair() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 int max_dyn_smem_pair() {
   static int v = 0;
   if (!v) {
@@ -664,7 +646,7 @@ cudaError_t launch_gemm_pair(int mode, const uint16_t* act, int T, int H, int F,
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
   if (mode == MOE_DOWN) {
-    EncodeTiledFn enc = encode_fn_pair();
+    EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     const int A = T * k;
     cuuint64_t gdim[2] = {static_cast<cuuint64_t>(F), static_cast<cuuint64_t>(A + T)};

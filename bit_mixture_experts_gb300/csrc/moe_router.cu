@@ -26,6 +26,7 @@
 #include "moe_common.cuh"
 #include "moe_ptx.cuh"
 #include "moe_route_dev.cuh"
+#include "moe_tmap.cuh"
 
 namespace moe {
 
@@ -186,28 +187,9 @@ __global__ void __launch_bounds__(RT_THREADS) router_kernel(const RouterParams p
 
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn_router() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 // A 2D bf16 tensor [rows, cols] (row-major) as 128-byte swizzled boxes of box_rows x 64.
 bool encode_bf16_2d(CUtensorMap* map, const uint16_t* base, int rows, int cols, int box_rows) {
-  EncodeTiledFn enc = encode_fn_router();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
