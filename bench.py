@@ -656,7 +656,7 @@ def run_ours(args, rank, world, local_rank):
 
 
 KERNEL_SOURCES = {
-    "gemm_tc_kernel": ("moe_gemm_tc.cu", "moe_ptx.cuh", "moe_common.cuh"),
+    "gemm_tc_kernel": ("moe_gemm_tc.cu", "moe_tc_dev.cuh", "moe_tmap.cuh", "moe_ptx.cuh", "moe_common.cuh"),
     "decode_kernel": ("moe_decode.cu", "moe_gemv_dev.cuh", "moe_route_dev.cuh", "moe_ptx.cuh", "moe_common.cuh"),
 }
 
