@@ -139,13 +139,16 @@ struct TcParams {
 // is warp-uniform (lane 0's clock).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
                                           unsigned long long limit, uint32_t sleep_ns) {
-  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+  // the first probe does not block: a try_wait without a time hint may wait for a while inside the
+  // instruction, past a short limit, without the limit being checked
+  if (__all_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity))) return true;
   const long long t0 = clock64();
   for (;;) {
-    // sleep until the phase completes (or 20 us pass) rather than polling
-    // the hardware suspends the thread until the phase completes or sleep_ns pass; sleep_ns never
-    // exceeds the limit, so a short limit is checked after at most that long
-    const bool done = ptx::mbar_try_wait_sleep(bar, parity, sleep_ns);
+    // sleep in hardware until the phase completes (or about 20 us pass) rather than polling; a limit
+    // shorter than 20 us is polled without sleeping instead: the sleep time is only a hint, which
+    // the hardware may exceed, and a short limit must be checked on time
+    const bool done = sleep_ns >= 20000u ? ptx::mbar_try_wait_sleep(bar, parity, sleep_ns)
+                                         : ptx::mbar_test_wait(bar, parity);
     if (__all_sync(0xffffffffu, done)) return true;
     int give_up = *s_abort;
     if (!give_up && static_cast<unsigned long long>(clock64() - t0) > limit) give_up = 2;

@@ -55,10 +55,15 @@ struct RouterParams {
 
 // Bounded wait of a whole warp on phase `parity` of `bar`; false on timeout (recorded).
 __device__ __forceinline__ bool rt_wait(uint32_t bar, uint32_t parity, const RouterParams& p) {
-  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+  // the first probe does not block: a try_wait without a time hint may wait for a while inside the
+  // instruction, past a short limit, without the limit being checked
+  if (__all_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity))) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (__all_sync(0xffffffffu, ptx::mbar_try_wait_sleep(bar, parity, p.sleep_ns))) return true;
+    // a limit shorter than 20 us is polled without sleeping (the sleep is only a hint)
+    const bool done = p.sleep_ns >= 20000u ? ptx::mbar_try_wait_sleep(bar, parity, p.sleep_ns)
+                                           : ptx::mbar_test_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
     if (static_cast<unsigned long long>(clock64() - t0) > p.wait_cycles) {
       if ((threadIdx.x & 31) == 0) set_device_error(p.err, MOE_DEV_TIMEOUT);
       return false;

@@ -32,10 +32,11 @@ def test_wait_timeout_reported_and_recovered(impl):
     good = layer.forward(x, logits).clone()
     torch.cuda.synchronize()
     assert _lib.moe_get_device_error() == 0
-    # 0.2 us: a wait on memory or another CTA that is still open after its first check runs out.
-    # Whether one is depends on timing: the tensor-core kernel's waits sleep in hardware until their
-    # phase completes, and the CTAs of a grid barrier can arrive within the limit, so the call is
-    # repeated (the device error word is read and cleared after each) until a timeout is reported.
+    # 0.2 us: a wait on memory or another CTA that is still open after its first check runs out
+    # (limits this short are polled, not slept on, so they are checked on time).  Whether a wait
+    # stays open that long depends on timing (the CTAs of a grid barrier can arrive within the
+    # limit), so the call is repeated (the device error word is read and cleared after each) until
+    # a timeout is reported.
     _lib.moe_set_wait_limit_ns(200)
     code = 0
     try:
