@@ -74,3 +74,32 @@ def test_chain_small(T):
 
 def test_chain_full_width_batch1():
     _chain_check(1, workloads.FULL, 2, "chain full width T=1")
+
+
+@pytest.mark.parametrize("T,H,E", [(1, 2048, 256), (8, 256, 64), (5, 128, 8), (3, 136, 17)])
+def test_norm_router_equals_rms_norm(T, H, E):
+    """moe_norm_router's normalised input is bit for bit moe_rms_norm's, and its logits are within the
+    FP32 accumulation bound of the exact projection of that input (H = 136 and E = 17: sizes that
+    are no multiple of a warp's 32 lanes of 8-element chunks, or of the kernel's experts per CTA)."""
+    import torch
+
+    from bit_mixture_experts_gb300 import _lib
+    dev = G.torch_dev()
+    shape = workloads.LayerShape(H=H, E=E, k=min(4, E), F=128)
+    tok = workloads.make_tokens(shape, T, seed=21)
+    wr = workloads.router_weight_bits(shape, seed=22)
+    x = torch.from_numpy(tok["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    w = torch.from_numpy(wr.view(np.int16)).to(dev).view(torch.bfloat16)
+    xn1 = torch.empty_like(x)
+    xn2 = torch.empty_like(x)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    _lib.moe_rms_norm(x, xn1)
+    _lib.moe_norm_router(x, w, xn2, logits)
+    torch.cuda.synchronize()
+    assert _lib.moe_get_device_error() == 0
+    assert torch.equal(xn1.view(torch.int16), xn2.view(torch.int16))
+    x_bits = xn2.view(torch.int16).cpu().numpy().view(np.uint16)
+    exact = moe_ref.router_logits(x_bits, wr).astype(np.float64)
+    xv, wv = moe_ref.bf16_value(x_bits), moe_ref.bf16_value(wr)
+    bound = 2.0 ** -20 * math.sqrt(H / 16 + 8) * (np.abs(xv) @ np.abs(wv).T) + np.abs(exact) * 2.0 ** -24
+    assert np.all(np.abs(logits.cpu().numpy() - exact) <= bound)
