@@ -273,9 +273,9 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
     ms = max_over_ranks(ms, world, dev)
     assert _lib.moe_get_device_error() == 0, "device error word set"
 
-    # end to end through the C ABI with host buffers (pinned): H2D of x and logits, the layer, D2H of
-    # out and a stream synchronisation in each step's wall-clock window; the L2 flush between steps
-    # runs (and is waited for) outside the window
+    # end to end through the C ABI with host buffers (pinned): x to the device, logits and out across
+    # the host link inside the kernels, and a stream synchronisation in each step's wall-clock window;
+    # the L2 flush between steps runs (and is waited for) outside the window
     e2e = None
     if not args.no_e2e:
         xh = torch.from_numpy(tok["x_bits"].view(np.int16)).pin_memory()
@@ -300,7 +300,9 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
         e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": int(xh.numel() * 2 + lh.numel() * 4),
                "d2h_bytes_per_step": int(oh.numel() * 2), "ms_per_step": e2e_ms,
-               "note": "wall clock per step: pinned H2D of x + logits, the layer, D2H of out, stream sync"}
+               "note": "wall clock per step through moe_layer_forward_host with pinned host buffers: x copied to "
+                       "the device, logits read by the routing kernel and out written by the combine (or the fused "
+                       "decode kernel) over the host link, stream sync"}
 
     # roofline of the dominant kernel: the gate/up GEMM (the fused decode kernel at decode sizes)
     gu_ms = float(seg[:, 1].mean())

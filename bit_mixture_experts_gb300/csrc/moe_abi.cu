@@ -295,6 +295,17 @@ int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out, int
   return moe_combine(b->y, b->inv_perm, b->topk_w, out, T, H, k, stream);
 }
 
+// The device's address of host memory it can read and write directly (pinned or registered, and
+// mapped), or nullptr (pageable memory, or an address the runtime does not know).
+static void* host_device_view(const void* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();  // an unknown pointer is not an error of this call
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 int moe_layer_forward_host(const uint16_t* x_host, const float* logits_host, uint16_t* out_host, uint16_t* x_dev,
                            float* logits_dev, uint16_t* out_dev, int T, int H, int F, int E, int k, int block_n,
                            int impl, const moe_weights_t* w, const moe_buffers_t* b, moe_stream_t stream) {
@@ -306,11 +317,24 @@ int moe_layer_forward_host(const uint16_t* x_host, const float* logits_host, uin
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t xb = static_cast<size_t>(T) * H * sizeof(uint16_t);
   const size_t lb = static_cast<size_t>(T) * E * sizeof(float);
+  // Pinned host buffers are read and written by the kernels over the host link where each byte
+  // crosses it once anyway: the routing (or fused decode) kernel reads every logit once, and the
+  // combine writes out straight to out_host, which saves two copy-engine operations and their
+  // latency per call.  x, which the grouped GEMM gathers k + 1 times, is copied to x_dev first.
+  // Pageable buffers go through logits_dev / out_dev with copies.
+  const float* logits_view = static_cast<const float*>(host_device_view(logits_host));
+  uint16_t* out_view = static_cast<uint16_t*>(host_device_view(out_host));
+  if (logits_view && !aligned16(logits_view)) logits_view = nullptr;
+  if (out_view && !aligned16(out_view)) out_view = nullptr;
   if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemcpyAsync(logits_dev, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-  rc = moe_layer_forward(x_dev, logits_dev, out_dev, T, H, F, E, k, block_n, impl, w, b, stream);
+  if (!logits_view &&
+      cudaMemcpyAsync(logits_dev, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  rc = moe_layer_forward(x_dev, logits_view ? logits_view : logits_dev, out_view ? out_view : out_dev, T, H, F, E, k,
+                         block_n, impl, w, b, stream);
   if (rc) return rc;
-  if (cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!out_view && cudaMemcpyAsync(out_host, out_dev, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

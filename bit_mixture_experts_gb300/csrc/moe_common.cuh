@@ -4,6 +4,10 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "moe_w4.h"
 
 namespace moe {
@@ -76,5 +80,42 @@ struct Tile {
   int row0;
   int rows;
 };
+
+// Host side: raise a kernel's dynamic shared memory limit (cudaFuncSetAttribute) only when a launch
+// needs more than the current device was given before -- the attribute persists, and the driver
+// call costs microseconds of host time on every launch that repeats it.
+inline cudaError_t ensure_dyn_smem(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> given;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = given[std::make_pair(dev, func)];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
+// Host side: resident CTAs per SM of a kernel at a block size and dynamic shared memory size,
+// computed once per device and configuration.
+inline cudaError_t cached_occupancy(const void* func, int threads, size_t smem, int* per_sm) {
+  static std::mutex mu;
+  static std::map<std::pair<std::pair<int, const void*>, std::pair<int, size_t>>, int> seen;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(std::make_pair(dev, func), std::make_pair(threads, smem));
+  auto it = seen.find(key);
+  if (it != seen.end()) {
+    *per_sm = it->second;
+    return cudaSuccess;
+  }
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, func, threads, smem);
+  if (e == cudaSuccess) seen[key] = *per_sm;
+  return e;
+}
 
 }  // namespace moe

@@ -445,11 +445,10 @@ cudaError_t launch_decode(const uint16_t* x, const float* logits, const void* w1
   prm.G = g0 > g1 ? g0 : g1;
   if (prm.G > GV_GB) return cudaErrorInvalidValue;
   const size_t smem = decode_smem_bytes(prm.G, E);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(decode_kernel), smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, GV_THREADS, smem);
+  e = cached_occupancy(reinterpret_cast<const void*>(decode_kernel), GV_THREADS, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidValue;
   if (per_sm > GV_CTAS_PER_SM) per_sm = GV_CTAS_PER_SM;

@@ -223,16 +223,21 @@ cudaError_t launch_gemm_gemv(int mode, const uint16_t* act, int T, int H, int F,
   prm.G = gemv_groups(mode == MOE_GATE_UP_SWIGLU ? H : F);
   if (prm.G > GV_GB) return cudaErrorInvalidValue;
   const size_t smem = gemv_smem_bytes(mode, H, F);
-  int dev = 0, max_smem = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  static int max_smem = 0;
+  if (!max_smem) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  }
   if (smem > static_cast<size_t>(max_smem)) return cudaErrorInvalidValue;
   const int grid = num_sms * GV_CTAS_PER_SM;
   if (mode == MOE_GATE_UP_SWIGLU) {
-    cudaFuncSetAttribute(gemv_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(gemv_kernel<0>), smem);
+    if (e != cudaSuccess) return e;
     gemv_kernel<0><<<grid, GV_THREADS, smem, s>>>(prm);
   } else {
-    cudaFuncSetAttribute(gemv_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(gemv_kernel<1>), smem);
+    if (e != cudaSuccess) return e;
     gemv_kernel<1><<<grid, GV_THREADS, smem, s>>>(prm);
   }
   note_launches(1);

@@ -665,7 +665,7 @@ cudaError_t launch_gemm_pair(int mode, const uint16_t* act, int T, int H, int F,
   void (*kern)(const PairParams, const CUtensorMap) =
       mode == MOE_GATE_UP_SWIGLU ? (GPS == 4 ? gemm_pair_kernel<0, 4> : gemm_pair_kernel<0, 2>)
                                  : (GPS == 4 ? gemm_pair_kernel<1, 4> : gemm_pair_kernel<1, 2>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<size_t>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NTHREADS);

@@ -916,7 +916,7 @@ cudaError_t launch_gemm_tc(int mode, const uint16_t* act, int T, int H, int F, i
              : MG == 2                  ? gemm_tc_kernel<1, 2, 2>
              : GPS == 4                 ? gemm_tc_kernel<1, 1, 4>
                                         : gemm_tc_kernel<1, 1, 2>);
-  const cudaError_t ea = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const cudaError_t ea = ensure_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<size_t>(smem));
   if (ea != cudaSuccess) return ea;
   kern<<<num_sms, NTHREADS, smem, s>>>(prm, tmap);
   note_launches(1);

@@ -150,8 +150,7 @@ cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* wr, uint16_t* 
   if (T > NR_MAXT || H % 8 != 0) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(T) * H * sizeof(uint16_t);
   if (smem > 48 * 1024) {
-    const cudaError_t e0 =
-        cudaFuncSetAttribute(norm_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    const cudaError_t e0 = ensure_dyn_smem(reinterpret_cast<const void*>(norm_router_kernel), smem);
     if (e0 != cudaSuccess) return e0;
   }
   norm_router_kernel<<<(E + NR_WARPS - 1) / NR_WARPS, NR_WARPS * 32, smem, s>>>(x, wr, xn, logits, T, H, E, eps);

@@ -316,8 +316,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
   if (route_use_small(T, k)) {
     size_t sm = static_cast<size_t>(33) * E * sizeof(int);
     if (sm > 48 * 1024) {
-      const cudaError_t e0 = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(sm));
+      const cudaError_t e0 = ensure_dyn_smem(reinterpret_cast<const void*>(route_small_kernel), sm);
       if (e0 != cudaSuccess) return e0;
     }
     route_small_kernel<<<1, 1024, sm, s>>>(logits, T, E, k, bn, ids, w, counts, offsets, perm, inv_perm, bm, nb,
@@ -331,8 +330,7 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int bn, int32
   int* ctr = reinterpret_cast<int*>(static_cast<char*>(ws) + ((ws_bytes - 16) & ~static_cast<size_t>(3)));
   const size_t sm = static_cast<size_t>(10) * E * sizeof(int);
   if (sm > 48 * 1024) {
-    cudaError_t e0 = cudaFuncSetAttribute(route_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(sm));
+    cudaError_t e0 = ensure_dyn_smem(reinterpret_cast<const void*>(route_fused_kernel), sm);
     if (e0 != cudaSuccess) return e0;
   }
   const unsigned long long ns = wait_limit_ns();

@@ -229,7 +229,7 @@ cudaError_t launch_router(const uint16_t* x, const uint16_t* w_router, int T, in
   memset(&tw, 0, sizeof(tw));
   if (!encode_bf16_2d(&tx, x, T, H, RT_M) || !encode_bf16_2d(&tw, w_router, E, H, RT_N))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(router_kernel), RT_SMEM);
   if (e != cudaSuccess) return e;
   const int csize = E / RT_N;
   cudaLaunchConfig_t cfg = {};

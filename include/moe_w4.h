@@ -399,10 +399,13 @@ int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out,
 
 /*
  * moe_layer_forward_host -- the same with x_host, logits_host and out_host in
- * host memory (pinned for asynchronous copies): copies the inputs to the
- * device staging buffers x_dev / logits_dev, runs the layer into out_dev and
- * copies the result back, all on `stream`.  Returns after enqueueing; the
- * caller synchronises the stream before reading out_host.
+ * host memory, all on `stream`: x is copied to the device staging buffer x_dev
+ * first (the grouped GEMM reads each row k + 1 times).  When logits_host and
+ * out_host are pinned (or registered) host memory, the kernels read the
+ * logits and write the output there directly over the host link (each byte
+ * crosses it once either way); otherwise they are copied through logits_dev
+ * and out_dev.  Returns after enqueueing; the caller synchronises the stream
+ * before reading out_host.
  */
 int moe_layer_forward_host(const uint16_t* x_host, const float* logits_host, uint16_t* out_host,
                            uint16_t* x_dev, float* logits_dev, uint16_t* out_dev,
