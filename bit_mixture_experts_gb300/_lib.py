@@ -102,18 +102,17 @@ def _call(name, *args):
 
 
 def _ptr(t):
-    """A tensor's data pointer, or a raw address given as an int."""
-    if t is None:
-        return None
-    if isinstance(t, int):
-        return ctypes.c_void_p(t)
-    return ctypes.c_void_p(t.data_ptr())
+    """A tensor's data pointer, or a raw address given as an int (every entry point declares its
+    pointer arguments as void*, so ctypes takes the integer as it is)."""
+    if t is None or isinstance(t, int):
+        return t
+    return t.data_ptr()
 
 
 def _stream(stream=None):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream
 
 
 # --------------------------------------------------------------------------- #
