@@ -327,8 +327,13 @@ int moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
  * moe_combine; y bf16 [A+T, H] (written); out bf16 [T, H].
  * workspace: moe_down_combine_workspace_size(T, H) bytes (an int32 per token
  * and 128 channels), zero-filled by the caller before the first call; every
- * call leaves it zero (a counter found above k is reported as
- * MOE_DEV_BAD_WORKSPACE).  Needs block_n <= 128, H % 128 == 0, F % 128 == 0.
+ * call that completes leaves it zero (a counter found above k is reported as
+ * MOE_DEV_BAD_WORKSPACE; after a call that reported a device error, zero it
+ * again).  Needs block_n <= 128, H % 128 == 0, F % 128 == 0; argument errors
+ * (MOE_ERR_SHAPE, _NULL, _ALIGN, _WORKSPACE) are returned before anything is
+ * enqueued.  Measured slower than MOE_DOWN + moe_combine on this GPU (the
+ * epilogue's counting and gathers lengthen every unit), so the layer uses it
+ * only when buffers->combine_ws is set.
  */
 size_t moe_down_combine_workspace_size(int T, int H);
 int moe_down_combine(const uint16_t* h, int T, int H, int F, int E, int k, const void* w_packed,
