@@ -61,10 +61,12 @@ def algorithmic(shape, T, n_touched):
     n = n_touched + 1
     gate_up_bytes = n * w13 + T * H * 2 + rows * F * 2            # weights + x + h
     down_bytes = n * w2 + rows * F * 2 + rows * H * 2              # weights + h + y
+    ffn_bytes = n * (w13 + w2) + T * H * 2 + rows * H * 2          # both projections, h on chip: weights + x + y
     flops_gate_up = 2.0 * rows * 2 * F * H
     flops_down = 2.0 * rows * H * F
     step_bytes = n * (w13 + w2) + T * H * 2 + T * E * 4 + T * H * 2
-    return {"gate_up_bytes": gate_up_bytes, "down_bytes": down_bytes, "flops_gate_up": flops_gate_up,
+    return {"gate_up_bytes": gate_up_bytes, "down_bytes": down_bytes, "ffn_bytes": ffn_bytes,
+            "flops_gate_up": flops_gate_up,
             "flops_down": flops_down, "step_bytes": step_bytes, "step_flops": flops_gate_up + flops_down}
 
 
@@ -174,7 +176,8 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
     impl, bn = layer.impl_for(T), layer.block_n_for(T)
     w = layer.weights
     fused_combine = impl == _lib.IMPL_TC and b.get("combine_ws") is not None
-    nseg = 3 if fused_combine else 4
+    fused_ffn = layer.h_on_chip(T)  # the layer runs both projections in one launch (moe_expert_ffn_w4)
+    nseg = 3 if (fused_combine or fused_ffn) else 4
 
     def step(ev=None):
         if ev is not None:
@@ -183,6 +186,16 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
                        b["inv_perm"], b["block_map"], b["num_blocks"], b["workspace"])
         if ev is not None:
             ev[1].record(stream)
+        if fused_ffn:
+            # the layer's own path at these tile heights: both projections in one launch, h on chip
+            _lib.moe_expert_ffn_w4(x, T, s.H, s.F, s.E, s.k, w.w13, w.w2, b["perm"], b["block_map"],
+                                   b["num_blocks"], bn, b["y"])
+            if ev is not None:
+                ev[2].record(stream)
+            _lib.moe_combine(b["y"], b["inv_perm"], b["topk_w"], out)
+            if ev is not None:
+                ev[3].record(stream)
+            return
         _lib.moe_expert_gemm_w4(_lib.GATE_UP, impl, x, T, s.H, s.F, s.E, s.k, w.w13, b["perm"], b["topk_w"],
                                 b["block_map"], b["num_blocks"], bn, b["h"])
         if ev is not None:
@@ -304,7 +317,8 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
                        "the device, logits read by the routing kernel and out written by the combine (or the fused "
                        "decode kernel) over the host link, stream sync"}
 
-    # roofline of the dominant kernel: the gate/up GEMM (the fused decode kernel at decode sizes)
+    # roofline of the dominant kernel: the gate/up GEMM (the fused FFN kernel where the layer keeps h on
+    # chip, the fused decode kernel at decode sizes)
     gu_ms = float(seg[:, 1].mean())
     peaks = load_peaks()
     fused_decode = impl == _lib.IMPL_GEMV and T <= 8
@@ -313,6 +327,12 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
         # over the step time
         achieved = work["step_bytes"] / (ms * 1e-3) / 1e9
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
+    elif fused_ffn and not tensor_bound(T):
+        achieved = work["ffn_bytes"] / (gu_ms * 1e-3) / 1e9
+        peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
+    elif fused_ffn:
+        achieved = work["step_flops"] / (gu_ms * 1e-3) / 1e12
+        peak, unit, bound = peaks["bf16_tflops"], "TFLOP/s", "tensor"
     elif tensor_bound(T):
         achieved = work["flops_gate_up"] / (gu_ms * 1e-3) / 1e12
         peak, unit, bound = peaks["bf16_tflops"], "TFLOP/s", "tensor"
@@ -321,14 +341,17 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
         peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
     kname = {_lib.IMPL_TC: "gemm_tc_kernel<0>", _lib.IMPL_TC2: "gemm_pair_kernel<0>",
              _lib.IMPL_GEMV: "gemv_kernel<0>"}.get(impl, str(impl))
-    traffic = (profiled_traffic(wl.name, 0) if impl == _lib.IMPL_TC else
+    traffic = (profiled_traffic(wl.name, 0, kernel="ffn_tc_kernel") if fused_ffn else
+               profiled_traffic(wl.name, 0) if impl == _lib.IMPL_TC else
                profiled_traffic(wl.name, 0, kernel="decode_kernel") if fused_decode else None)
     kdesc = ("decode_kernel: the fused layer (routing, gate/up, down and combine in one launch)" if fused_decode
-             else f"gate/up grouped GEMM {kname} (moe_expert_gemm_w4, MOE_GATE_UP_SWIGLU)")
+             else "ffn_tc_kernel: both projections of every expert tile, h kept on chip (moe_expert_ffn_w4)"
+             if fused_ffn else f"gate/up grouped GEMM {kname} (moe_expert_gemm_w4, MOE_GATE_UP_SWIGLU)")
     roof = {"kernel": kdesc, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "peak_source": peaks["source"], "traffic": traffic,
             "algorithmic_per_launch": (work["step_bytes"] if fused_decode else
-                                       work["flops_gate_up"] if tensor_bound(T) else work["gate_up_bytes"]),
+                                       (work["step_flops"] if tensor_bound(T) else work["ffn_bytes"]) if fused_ffn
+                                       else work["flops_gate_up"] if tensor_bound(T) else work["gate_up_bytes"]),
             "launch_ms": ms if fused_decode else gu_ms}
     layer_tflops = work["step_flops"] / (ms * 1e-3) / 1e12
     layer_gbs = work["step_bytes"] / (ms * 1e-3) / 1e9
@@ -341,9 +364,13 @@ def measure_workload(args, wl, layer, d, rank, world, dev):
                         "moe_combine); the timed step is the fused decode kernel") if fused_decode else
                        ("eager launches of the three entry points (moe_route, gate/up moe_expert_gemm_w4, "
                         "moe_down_combine); the timed step replays the same launches") if fused_combine else
+                       ("eager launches of the three entry points the layer uses at these tile heights (moe_route, "
+                        "moe_expert_ffn_w4, moe_combine); the timed step replays the same launches") if fused_ffn else
                        "eager launches of the four entry points; the timed step replays the same launches",
         "stages_ms": ({"route": float(seg[:, 0].mean()), "gate_up": gu_ms, "down_combine": float(seg[:, 2].mean())}
                       if fused_combine else
+                      {"route": float(seg[:, 0].mean()), "ffn": gu_ms, "combine": float(seg[:, 2].mean())}
+                      if fused_ffn else
                       {"route": float(seg[:, 0].mean()), "gate_up": gu_ms, "down": float(seg[:, 2].mean()),
                        "combine": float(seg[:, 3].mean())}),
         "roofline": roof,
@@ -590,6 +617,63 @@ def measure_fused_combine(args, wl, layer, d, dev):
                     "keeps the separate combine, which measures faster"}
 
 
+def measure_fused_ffn(args, wl, layer, d, dev):
+    """Ablation of h kept on chip: the layer's step with both projections of each expert tile in one
+    launch (moe_expert_ffn_w4) against the same step with the two grouped GEMMs and h through HBM (same
+    bits).  CUDA events on the stream around each eager step, L2 flushed between steps.  Only where the
+    layer keeps h on chip (tiles of at most 64 rows)."""
+    import torch
+
+    from bit_mixture_experts_gb300 import _lib
+
+    s = wl.shape
+    T = wl.T
+    if not layer.h_on_chip(T):
+        return None
+    x = torch.from_numpy(d["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.from_numpy(d["logits"]).to(dev)
+    outs = {n: torch.empty((T, s.H), dtype=torch.bfloat16, device=dev) for n in ("fused", "two")}
+    b = layer.buffers(T)
+    bn = layer.block_n_for(T)
+    w = layer.weights
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step(fused, o):
+        _lib.moe_route(logits, s.k, bn, b["topk_ids"], b["topk_w"], b["counts"], b["offsets"], b["perm"],
+                       b["inv_perm"], b["block_map"], b["num_blocks"], b["workspace"])
+        if fused:
+            _lib.moe_expert_ffn_w4(x, T, s.H, s.F, s.E, s.k, w.w13, w.w2, b["perm"], b["block_map"],
+                                   b["num_blocks"], bn, b["y"])
+        else:
+            _lib.moe_expert_gemm_w4(_lib.GATE_UP, _lib.IMPL_TC, x, T, s.H, s.F, s.E, s.k, w.w13, b["perm"],
+                                    b["topk_w"], b["block_map"], b["num_blocks"], bn, b["h"])
+            _lib.moe_expert_gemm_w4(_lib.DOWN, _lib.IMPL_TC, b["h"], T, s.H, s.F, s.E, s.k, w.w2, b["perm"],
+                                    b["topk_w"], b["block_map"], b["num_blocks"], bn, b["y"])
+        _lib.moe_combine(b["y"], b["inv_perm"], b["topk_w"], o)
+
+    def timed(fused, o):
+        for _ in range(max(3, args.warmup)):
+            step(fused, o)
+        n = max(3, min(args.steps, 30))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record()
+            step(fused, o)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b_) for a, b_ in ev]))
+
+    ms_two = timed(False, outs["two"])
+    ms_fused = timed(True, outs["fused"])
+    assert _lib.moe_get_device_error() == 0, "device error word set"
+    return {"fused_ffn_ms_per_step": ms_fused, "two_gemms_ms_per_step": ms_two,
+            "same_output": bool(torch.equal(outs["fused"].view(torch.int16), outs["two"].view(torch.int16))),
+            "note": "eager steps: route, then moe_expert_ffn_w4 (the layer's path here) or the gate/up and down "
+                    "grouped GEMMs with h through HBM, then moe_combine"}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -626,6 +710,7 @@ def run_ours(args, rank, world, local_rank):
         hs["fused_speedup"] = hs["ms_per_step"] / results[args.workload]["ms_per_step"]
         ablations["host_synced_routing"] = hs
         ablations["fused_combine"] = measure_fused_combine(args, wl, layer, primary_d, dev)
+        ablations["fused_ffn"] = measure_fused_ffn(args, wl, layer, primary_d, dev)
         ablations["unfused_dequant"] = measure_unfused(args, wl, primary_d, dev, results[args.workload]["ms_per_step"])
     if clocks:
         clocks.stop()
@@ -660,6 +745,7 @@ def run_ours(args, rank, world, local_rank):
 KERNEL_SOURCES = {
     "gemm_tc_kernel": ("moe_gemm_tc.cu", "moe_tc_dev.cuh", "moe_tmap.cuh", "moe_ptx.cuh", "moe_common.cuh"),
     "decode_kernel": ("moe_decode.cu", "moe_gemv_dev.cuh", "moe_route_dev.cuh", "moe_ptx.cuh", "moe_common.cuh"),
+    "ffn_tc_kernel": ("moe_ffn_tc.cu", "moe_tc_dev.cuh", "moe_ptx.cuh", "moe_common.cuh"),
 }
 
 

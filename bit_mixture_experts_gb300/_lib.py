@@ -25,7 +25,7 @@ IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV, "tc2": IMPL_TC2, "
 
 # Exported symbols of include/moe_w4.h (checked by the CPU tests).
 SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_route_x", "moe_router", "moe_rms_norm", "moe_norm_router",
-           "moe_down_combine", "moe_down_combine_workspace_size", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
+           "moe_down_combine", "moe_down_combine_workspace_size", "moe_expert_ffn_w4", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
            "moe_repacked_bytes", "moe_repack_w4", "moe_expanded_bytes", "moe_expand_w4", "moe_expert_gemm_w4", "moe_combine", "moe_decode_workspace_size",
            "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns"]
 
@@ -62,6 +62,7 @@ _SIGS = {
     "moe_rms_norm": ([_vp, _vp, _i, _i, ctypes.c_float, _vp], _i),
     "moe_norm_router": ([_vp, _vp, _i, _i, _i, ctypes.c_float, _vp, _vp, _vp], _i),
     "moe_down_combine_workspace_size": ([_i, _i], _sz),
+    "moe_expert_ffn_w4": ([_vp, _i, _i, _i, _i, _i] + [_vp] * 5 + [_i, _vp, _vp], _i),
     "moe_down_combine": ([_vp, _i, _i, _i, _i, _i] + [_vp] * 6 + [_i, _vp, _vp, _vp, _sz, _vp], _i),
     "moe_repacked_bytes": ([_i, _i, _i], _sz),
     "moe_expanded_bytes": ([_i, _i, _i], _sz),
@@ -213,6 +214,12 @@ def moe_combine(y, inv_perm, topk_w, out, stream=None):
     T, k = topk_w.shape
     H = out.shape[1]
     _call("moe_combine", _ptr(y), _ptr(inv_perm), _ptr(topk_w), _ptr(out), T, H, k, _stream(stream))
+
+
+def moe_expert_ffn_w4(x, T, H, F, E, k, w13, w2, perm, block_map, num_blocks, block_n, y, stream=None):
+    """Both projections per expert tile in one launch, h kept on chip (y written, no h)."""
+    _call("moe_expert_ffn_w4", _ptr(x), T, H, F, E, k, _ptr(w13), _ptr(w2), _ptr(perm), _ptr(block_map),
+          _ptr(num_blocks), block_n, _ptr(y), _stream(stream))
 
 
 def moe_down_combine_workspace_size(T, H) -> int:

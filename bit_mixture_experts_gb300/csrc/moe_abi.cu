@@ -65,6 +65,9 @@ cudaError_t launch_gemm_gemv(int mode, const uint16_t* act, int T, int H, int F,
 int gemv_max_rows();
 int decode_max_tokens();
 size_t decode_workspace_bytes(int T, int H);
+cudaError_t launch_ffn_tc(const uint16_t* x, int T, int H, int F, int E, int k, const void* w13, const void* w2,
+                          const int32_t* perm, const int32_t* block_map, const int32_t* num_blocks, int bn, int cap,
+                          uint16_t* y, int num_sms, cudaStream_t s);
 cudaError_t launch_decode(const uint16_t* x, const float* logits, const void* w13, const void* w2, int T, int H, int F,
                           int E, int k, int bn, int32_t* topk_ids, float* topk_w, int32_t* counts, int32_t* offsets,
                           int32_t* perm, int32_t* inv_perm, int32_t* block_map, int32_t* num_blocks, uint16_t* h,
@@ -209,6 +212,20 @@ int moe_expert_gemm_w4(int mode, int impl, const uint16_t* act, int T, int H, in
                                     nullptr));
 }
 
+int moe_expert_ffn_w4(const uint16_t* x, int T, int H, int F, int E, int k, const void* w13, const void* w2,
+                      const int32_t* perm, const int32_t* block_map, const int32_t* num_blocks, int block_n,
+                      uint16_t* y, moe_stream_t stream) {
+  int rc = check_shape(T, H, F, E, k, block_n);
+  if (rc) return rc;
+  if (H % 128 != 0 || F % 256 != 0 || block_n > 64) return MOE_ERR_SHAPE;
+  rc = check_ptrs(x, w13, w2, perm, block_map, num_blocks, y);
+  if (rc) return rc;
+  if (!device_error_ptr()) return MOE_ERR_CUDA;
+  const int cap = moe_block_map_capacity(T, E, k, block_n);
+  return cuda_status(launch_ffn_tc(x, T, H, F, E, k, w13, w2, perm, block_map, num_blocks, block_n, cap, y, num_sms(),
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_down_combine_workspace_size(int T, int H) {
   if (T < 1 || T > (1 << 20) || H < 128 || H % 128 != 0) return 0;
   return static_cast<size_t>(T) * (H / 128) * sizeof(int32_t);
@@ -280,10 +297,18 @@ int moe_layer_forward(const uint16_t* x, const float* logits, uint16_t* out, int
   int rc = moe_route(logits, T, E, k, block_n, b->topk_ids, b->topk_w, b->counts, b->offsets, b->perm, b->inv_perm,
                      b->block_map, b->num_blocks, b->workspace, b->workspace_bytes, stream);
   if (rc) return rc;
+  const int resolved = impl == MOE_IMPL_AUTO ? (block_n <= gemv_max_rows() ? MOE_IMPL_GEMV : MOE_IMPL_TC) : impl;
+  if (resolved == MOE_IMPL_TC && !b->combine_ws && block_n <= 64 && H % 128 == 0 && F % 256 == 0) {
+    // tiles of at most 64 rows: both projections of a tile in one launch, h kept in shared memory
+    // (the same bits of y; measured faster than the two GEMMs at these tile heights)
+    rc = moe_expert_ffn_w4(x, T, H, F, E, k, w->w13, w->w2, b->perm, b->block_map, b->num_blocks, block_n, b->y,
+                           stream);
+    if (rc) return rc;
+    return moe_combine(b->y, b->inv_perm, b->topk_w, out, T, H, k, stream);
+  }
   rc = moe_expert_gemm_w4(MOE_GATE_UP_SWIGLU, impl, x, T, H, F, E, k, w->w13, b->perm, b->topk_w, b->block_map,
                           b->num_blocks, block_n, b->h, stream);
   if (rc) return rc;
-  const int resolved = impl == MOE_IMPL_AUTO ? (block_n <= gemv_max_rows() ? MOE_IMPL_GEMV : MOE_IMPL_TC) : impl;
   if (resolved == MOE_IMPL_TC && b->combine_ws) {
     // the down GEMM with the combine in its epilogue (one launch fewer, y read back from L2 at once)
     return moe_down_combine(b->h, T, H, F, E, k, w->w2, b->perm, b->inv_perm, b->topk_w, b->block_map,

@@ -109,46 +109,8 @@ struct PairParams {
   int a0;       // first TMEM column of the A ring
 };
 
-// Bounded wait by a whole warp (the phase may be completed by arrivals from the
-// other CTA).  False on timeout or when another role of this CTA has already
-// given up; the decision is warp-uniform.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
-                                          unsigned long long limit, uint32_t sleep_ns) {
-  // the first probe does not block: a try_wait without a time hint may wait for a while inside the
-  // instruction, past a short limit, without the limit being checked
-  if (__all_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity))) return true;
-  const long long t0 = clock64();
-  for (;;) {
-    // sleep in hardware until the phase completes (or about 20 us pass) rather than polling; a limit
-    // shorter than 20 us is polled without sleeping instead: the sleep time is only a hint, which
-    // the hardware may exceed, and a short limit must be checked on time
-    const bool done = sleep_ns >= 20000u ? ptx::mbar_try_wait_sleep(bar, parity, sleep_ns)
-                                         : ptx::mbar_test_wait(bar, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    int give_up = *s_abort;
-    if (!give_up && static_cast<unsigned long long>(clock64() - t0) > limit) give_up = 2;
-    give_up = __shfl_sync(0xffffffffu, give_up, 0);
-    if (give_up) {
-      if (give_up == 2 && (threadIdx.x & 31) == 0) {
-        set_device_error(err, MOE_DEV_TIMEOUT);
-        *s_abort = 1;
-      }
-      return false;
-    }
-  }
-}
-
-// Drain wait: ignores the abort flag and waits at least about 10 ms.
-constexpr unsigned long long DRAIN_MIN_CYCLES = 20000000ull;
-
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
-  if (ptx::mbar_try_wait(bar, parity)) return;
-  if (limit < DRAIN_MIN_CYCLES) limit = DRAIN_MIN_CYCLES;
-  const long long t0 = clock64();
-  while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
-    if (static_cast<unsigned long long>(clock64() - t0) > limit) return;
-  }
-}
+// The bounded waits (wait_warp, wait_drain) are moe_tc_dev.cuh's: a phase completed by arrivals
+// from the other CTA of the pair is waited for the same way.
 
 // Unit u = (block-map tile u / MGT, M-tile pair u % MGT).  False for a
 // malformed entry (the same decision in every role of both CTAs).

@@ -35,6 +35,54 @@ __device__ __forceinline__ void expand_group(const uint4 p0, const uint4 p1, uin
   }
 }
 
+// Bounded waits.  The time limit is counted in SM clock cycles (clock64, cheap
+// to read) from the first unsuccessful try; `limit` is in cycles.
+//
+// Bounded wait on phase `parity` of `bar` by a whole warp.  Returns false on
+// timeout or when another role has already given up (s_abort); the decision
+// is warp-uniform (lane 0's clock).
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
+                                          unsigned long long limit, uint32_t sleep_ns) {
+  // the first probe does not block: a try_wait without a time hint may wait for a while inside the
+  // instruction, past a short limit, without the limit being checked
+  if (__all_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    // sleep in hardware until the phase completes (or about 20 us pass) rather than polling; a limit
+    // shorter than 20 us is polled without sleeping instead: the sleep time is only a hint, which
+    // the hardware may exceed, and a short limit must be checked on time
+    const bool done = sleep_ns >= 20000u ? ptx::mbar_try_wait_sleep(bar, parity, sleep_ns)
+                                         : ptx::mbar_test_wait(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    int give_up = *s_abort;
+    if (!give_up && static_cast<unsigned long long>(clock64() - t0) > limit) give_up = 2;
+    give_up = __shfl_sync(0xffffffffu, give_up, 0);
+    if (give_up) {
+      if (give_up == 2 && (threadIdx.x & 31) == 0) {
+        set_device_error(err, MOE_DEV_TIMEOUT);
+        *s_abort = 1;
+      }
+      return false;
+    }
+  }
+}
+
+// Wait that ignores s_abort (used to drain copies and MMAs already in flight
+// before the CTA exits).  Whatever the configured limit, it waits at least
+// DRAIN_MIN_CYCLES (about 10 ms): a copy still landing in shared memory or an
+// MMA still using TMEM must not outlive the CTA, even when a very short wait
+// limit made the kernel give up early.
+constexpr unsigned long long DRAIN_MIN_CYCLES = 20000000ull;
+
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
+  if (ptx::mbar_try_wait(bar, parity)) return;
+  if (limit < DRAIN_MIN_CYCLES) limit = DRAIN_MIN_CYCLES;
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
+    if (static_cast<unsigned long long>(clock64() - t0) > limit) return;
+  }
+}
+
 // silu(g) = g / (1 + e^-g) with the fast exponential and division; the
 // product with u is rounded to bf16 afterwards, which hides their few-ulp
 // error except within a few FP32 ulps of a bf16 rounding boundary.

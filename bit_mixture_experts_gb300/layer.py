@@ -92,6 +92,13 @@ class MoELayerW4:
         _lib.moe_expand_w4(repacked, n_mat, rows, kw * 8, out)
         return out
 
+    def h_on_chip(self, T):
+        """Whether the layer call for T tokens runs both projections as moe_expert_ffn_w4 (h kept in shared
+        memory, the h buffer not written): the tensor-core kernel with tiles of at most 64 rows and
+        F % 256 == 0, as moe_layer_forward decides."""
+        return (self.impl_for(T) == _lib.IMPL_TC and self.block_n_for(T) <= 64 and self.F % 256 == 0
+                and self.H % 128 == 0 and not self.fuse_combine)
+
     def impl_for(self, T):
         """GEMM kernel used for T tokens: under "auto", GEMV for decode-sized T, else tensor cores."""
         if self.impl != _lib.IMPL_AUTO:
@@ -148,8 +155,8 @@ class MoELayerW4:
         b = self.buffers(T)
         if out is None:
             out = torch.empty((T, self.H), dtype=torch.bfloat16, device=self.device)
-        _lib.moe_layer_forward(x, logits, out, T, self.H, self.F, self.E, self.k, self.block_n_for(T), self.impl_for(T),
-                               self.weights, b["struct"], stream)
+        _lib.moe_layer_forward(x, logits, out, T, self.H, self.F, self.E, self.k, self.block_n_for(T),
+                               self.impl_for(T), self.weights, b["struct"], stream)
         return out
 
     def forward_host(self, x_host, logits_host, out_host, stage, stream=None):

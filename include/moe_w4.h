@@ -315,6 +315,25 @@ int moe_combine(const uint16_t* y, const int32_t* inv_perm, const float* topk_w,
                 int k, moe_stream_t stream);
 
 /*
+ * moe_expert_ffn_w4 -- both projections of every expert tile in one launch,
+ * h kept on chip: for each block-map tile, the gate/up GEMM with SwiGLU writes
+ * the tile's h into shared memory and the down GEMM of the same tile reads it
+ * from there ("Perplexity Open Sources Lily", Technical Details, Prefill
+ * optimizations bullet: the weights are expanded inside the GEMM; here h, too,
+ * never leaves the chip).  x bf16 [T, H]; w13, w2 repacked as for
+ * moe_expert_gemm_w4 (gate_up = 1 for w13); perm, block_map, num_blocks from
+ * moe_route; y bf16 [A+T, H] (written; combine it with moe_combine).  The
+ * same bits of y as MOE_GATE_UP_SWIGLU followed by MOE_DOWN; no h is written.
+ * Needs block_n <= 64 (the tile's h must fit in shared memory),
+ * H % 128 == 0 and F % 256 == 0, else MOE_ERR_SHAPE; argument errors are
+ * returned before anything is enqueued.  moe_layer_forward uses it for the
+ * tensor-core path whenever these hold (faster than the two GEMMs there).
+ */
+int moe_expert_ffn_w4(const uint16_t* x, int T, int H, int F, int E, int k, const void* w13, const void* w2,
+                      const int32_t* perm, const int32_t* block_map, const int32_t* num_blocks, int block_n,
+                      uint16_t* y, moe_stream_t stream);
+
+/*
  * moe_down_combine -- MOE_DOWN and moe_combine in one launch of the
  * tensor-core kernel: the down projection writes its bf16 rows y as
  * moe_expert_gemm_w4 does, and every (token, 128-channel block) counts its
@@ -387,7 +406,10 @@ typedef struct {
 /*
  * moe_layer_forward -- the whole hot path on one stream with no host sync:
  * moe_route, gate/up GEMM, down GEMM, moe_combine.  x bf16 [T,H], logits
- * float32 [T,E], out bf16 [T,H] are device pointers.
+ * float32 [T,E], out bf16 [T,H] are device pointers.  With the tensor-core
+ * kernel, tiles of at most 64 rows and F % 256 == 0 the two GEMMs run as
+ * moe_expert_ffn_w4 (h kept on chip, the same y); buffers->h is then not
+ * written.
  *
  * Decode: when the GEMV kernel is chosen (impl MOE_IMPL_GEMV, or AUTO with
  * block_n <= 8), T <= 8, k <= 32 and buffers->decode_ws is set, the four steps

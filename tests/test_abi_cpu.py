@@ -110,6 +110,16 @@ def test_down_combine_argument_errors(lib):
     assert args(256, 128, 128, wsb=ws - 4) == -4
 
 
+def test_expert_ffn_argument_errors(lib):
+    p = ctypes.c_void_p(256)
+    args = lambda H, F, bn, ptr=p: lib.moe_expert_ffn_w4(ptr, 16, H, F, 8, 2, ptr, ptr, ptr, ptr, ptr, bn, ptr, None)
+    assert args(192, 256, 64) == -3             # H % 128
+    assert args(256, 384, 64) == -3             # F % 256
+    assert args(256, 256, 65) == -3             # tiles above 64 rows (h must fit in shared memory)
+    assert args(256, 256, 64, ptr=None) == -1
+    assert args(256, 256, 64, ptr=ctypes.c_void_p(260)) == -2
+
+
 def test_repacked_bytes(lib):
     # one 4608-byte block (2 halves x 128 rows x 16 B of nibbles, then 128 x (scale, bias)) per
     # 128-row tile and 64-wide K group: exactly the bytes of the canonical layout of the matrix

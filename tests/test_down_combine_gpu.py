@@ -78,6 +78,9 @@ def test_fused_combine_direct_call_and_bad_workspace():
     want = plain.forward(x, logits).clone()
     b = plain.buffers(T)
     bn = plain.block_n_for(T)
+    # the layer call may have kept h on chip (moe_expert_ffn_w4): h from the gate/up GEMM on the same routing
+    _lib.moe_expert_gemm_w4(_lib.GATE_UP, _lib.IMPL_TC, x, T, H, F, E, k, plain.weights.w13, b["perm"], b["topk_w"],
+                            b["block_map"], b["num_blocks"], bn, b["h"])
     ws_bytes = _lib.moe_down_combine_workspace_size(T, H)
     assert ws_bytes == T * (H // 128) * 4
     ws = torch.zeros(ws_bytes // 4, dtype=torch.int32, device=x.device)
