@@ -16,7 +16,7 @@ MOE_DEV_TIMEOUT = 3
 DEFAULT_LIMIT_NS = 1_000_000_000
 
 
-@pytest.mark.parametrize("impl", ["tc", "gemv"])
+@pytest.mark.parametrize("impl", ["tc", "gemv", "ffn"])
 def test_wait_timeout_reported_and_recovered(impl):
     import torch
     from bit_mixture_experts_gb300 import _lib
@@ -24,10 +24,13 @@ def test_wait_timeout_reported_and_recovered(impl):
     G.ensure_built()
     # tc: 300 tokens (multi-CTA routing with its grid barrier, pipeline waits of the GEMM);
     # gemv: 8 tokens (the fused decode kernel and its grid barriers)
-    spec = (300, 256, 16, 4, 128, False) if impl == "tc" else (8, 256, 16, 4, 128, False)
+    # ffn: 200 tokens with F = 256 (64-row tiles: both projections in one launch, h kept on chip)
+    spec = {"tc": (300, 256, 16, 4, 128, False), "gemv": (8, 256, 16, 4, 128, False),
+            "ffn": (200, 256, 16, 4, 256, False)}[impl]
     d = G.workload(spec)
     T, H, E, k, F, _ = spec
-    layer = MoELayerW4(H, E, k, F, d, impl=impl)
+    layer = MoELayerW4(H, E, k, F, d, impl="tc" if impl == "ffn" else impl)
+    assert layer.h_on_chip(T) == (impl == "ffn")
     x, logits = G.to_dev_inputs(d)
     good = layer.forward(x, logits).clone()
     torch.cuda.synchronize()
