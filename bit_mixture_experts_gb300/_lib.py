@@ -27,7 +27,8 @@ IMPLS = {"auto": IMPL_AUTO, "tc": IMPL_TC, "gemv": IMPL_GEMV, "tc2": IMPL_TC2, "
 SYMBOLS = ["moe_version", "moe_launch_count", "moe_route_noalloc", "moe_route_x", "moe_router", "moe_rms_norm", "moe_norm_router",
            "moe_down_combine", "moe_down_combine_workspace_size", "moe_expert_ffn_w4", "moe_block_map_capacity", "moe_route_workspace_size", "moe_route",
            "moe_repacked_bytes", "moe_repack_w4", "moe_expanded_bytes", "moe_expand_w4", "moe_expert_gemm_w4", "moe_combine", "moe_decode_workspace_size",
-           "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns"]
+           "moe_layer_forward", "moe_layer_forward_host", "moe_get_device_error", "moe_set_wait_limit_ns",
+           "moe_trace_words", "moe_trace_reset", "moe_trace_read"]
 
 
 class MoeError(RuntimeError):
@@ -75,6 +76,9 @@ _SIGS = {
     "moe_layer_forward_host": ([_vp] * 6 + [_i] * 7 + [ctypes.POINTER(Weights), ctypes.POINTER(Buffers), _vp], _i),
     "moe_get_device_error": ([ctypes.POINTER(ctypes.c_int32)], _i),
     "moe_set_wait_limit_ns": ([ctypes.c_uint64], None),
+    "moe_trace_words": ([], ctypes.c_size_t),
+    "moe_trace_reset": ([_vp], _i),
+    "moe_trace_read": ([_vp, ctypes.c_size_t], _i),
 }
 
 _lib = None
@@ -254,6 +258,20 @@ def moe_layer_forward_host(x_host, logits_host, out_host, x_dev, logits_dev, out
 
 def moe_set_wait_limit_ns(ns: int) -> None:
     load().moe_set_wait_limit_ns(int(ns))
+
+
+def moe_trace_words() -> int:
+    """Words of wait statistics the loaded library keeps (0 unless it is the trace build)."""
+    return int(load().moe_trace_words())
+
+
+def moe_trace_reset(stream=None) -> None:
+    _call("moe_trace_reset", _stream(stream))
+
+
+def moe_trace_read(out) -> None:
+    """Copies the wait statistics into `out`, a contiguous uint64 numpy array of moe_trace_words() words."""
+    _call("moe_trace_read", out.ctypes.data, out.size)
 
 
 def moe_get_device_error() -> int:

@@ -3,8 +3,12 @@
 Each .cu under csrc/ is compiled to an object in parallel, then linked into
 bit_mixture_experts_gb300/libmoe_w4.so (CUDA runtime linked statically).
 Objects go to bit_mixture_experts_gb300/_build/.  Rebuilds only what changed.
+With --trace the same sources are built with -DMOE_TRACE into
+libmoe_w4_trace.so (objects in _build_trace/): the tensor-core kernels then
+record their wait statistics (moe_trace_read; `python -m
+bit_mixture_experts_gb300.trace` reports them).
 
-    python -m bit_mixture_experts_gb300.build [--force] [--verbose]
+    python -m bit_mixture_experts_gb300.build [--force] [--verbose] [--trace]
 """
 from __future__ import annotations
 
@@ -21,6 +25,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_w4.so")
+BUILD_TRACE = os.path.join(PKG, "_build_trace")
+LIB_TRACE = os.path.join(PKG, "libmoe_w4_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -51,8 +57,8 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str, force: bool, verbose: bool, extra=()) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, force: bool, verbose: bool, extra=(), build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
     if force or _stale(obj, [src, *_headers(), __file__]):
         cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
@@ -65,22 +71,23 @@ def _compile(src: str, force: bool, verbose: bool, extra=()) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, trace: bool = False) -> str:
+    build_dir, lib = (BUILD_TRACE, LIB_TRACE) if trace else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DMOE_TRACE"] if trace else [])
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, force or ptxas_info, verbose or ptxas_info, extra), srcs))
-    if force or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, force or ptxas_info, verbose or ptxas_info, extra, build_dir), srcs))
+    if force or _stale(lib, objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None):
@@ -88,8 +95,9 @@ def main(argv=None):
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--ptxas-info", action="store_true", help="print -Xptxas -v register/smem usage")
+    ap.add_argument("--trace", action="store_true", help="build libmoe_w4_trace.so (-DMOE_TRACE) instead")
     a = ap.parse_args(argv)
-    print(build(a.force, a.verbose, a.ptxas_info))
+    print(build(a.force, a.verbose, a.ptxas_info, a.trace))
 
 
 if __name__ == "__main__":

@@ -9,9 +9,23 @@
 
 namespace moe {
 
+#ifdef MOE_TRACE
+// The trace build keeps the wait statistics of the tensor-core kernels right after the error word
+// (TRACE_ERR_INTS ints, then TRACE_CTAS x 32 warps x 4 words; see trace_wait).
+constexpr int TRACE_ERR_INTS = 64;
+constexpr size_t TRACE_WORDS = 1024 * 32 * 4;
+struct TraceBlock {
+  int err[TRACE_ERR_INTS];
+  unsigned long long words[TRACE_WORDS];
+};
+__device__ TraceBlock g_trace_block;
+#define MOE_ERROR_SYMBOL g_trace_block  // the error word is its first int
+#else
 __device__ int g_device_error = 0;
+#define MOE_ERROR_SYMBOL g_device_error
+#endif
 
-// Per-device address of g_device_error, looked up once per device.
+// Per-device address of the device error word, looked up once per device.
 int* device_error_ptr() {
   static std::mutex mu;
   static int* ptrs[64] = {nullptr};
@@ -20,7 +34,7 @@ int* device_error_ptr() {
   std::lock_guard<std::mutex> lock(mu);
   if (!ptrs[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, MOE_ERROR_SYMBOL) != cudaSuccess) return nullptr;
     ptrs[dev] = static_cast<int*>(p);
   }
   return ptrs[dev];
@@ -367,9 +381,9 @@ int moe_get_device_error(int32_t* code) {
   if (!code) return MOE_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, MOE_ERROR_SYMBOL, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   const int zero = 0;
-  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyToSymbol(MOE_ERROR_SYMBOL, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   *code = v;
   return MOE_OK;
 }
@@ -392,5 +406,42 @@ int moe_repack_w4(const uint32_t* packed, const uint16_t* scale, const uint16_t*
 }
 
 void moe_set_wait_limit_ns(uint64_t ns) { set_wait_limit_ns(ns); }
+
+size_t moe_trace_words(void) {
+#ifdef MOE_TRACE
+  return moe::TRACE_WORDS;
+#else
+  return 0;
+#endif
+}
+
+int moe_trace_reset(moe_stream_t stream) {
+#ifdef MOE_TRACE
+  int* err = moe::device_error_ptr();
+  if (!err) return MOE_ERR_CUDA;
+  return moe::cuda_status(cudaMemsetAsync(err + moe::TRACE_ERR_INTS, 0,
+                                          moe::TRACE_WORDS * sizeof(unsigned long long),
+                                          reinterpret_cast<cudaStream_t>(stream)));
+#else
+  (void)stream;
+  return MOE_ERR_MODE;
+#endif
+}
+
+int moe_trace_read(uint64_t* host, size_t words) {
+#ifdef MOE_TRACE
+  if (!host) return MOE_ERR_NULL;
+  int* err = moe::device_error_ptr();
+  if (!err) return MOE_ERR_CUDA;
+  const size_t n = words < moe::TRACE_WORDS ? words : moe::TRACE_WORDS;
+  return cudaMemcpy(host, err + moe::TRACE_ERR_INTS, n * sizeof(uint64_t), cudaMemcpyDeviceToHost) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+#else
+  (void)host;
+  (void)words;
+  return MOE_ERR_MODE;
+#endif
+}
 
 }  // extern "C"

@@ -41,8 +41,8 @@ __device__ __forceinline__ void expand_group(const uint4 p0, const uint4 p1, uin
 // Bounded wait on phase `parity` of `bar` by a whole warp.  Returns false on
 // timeout or when another role has already given up (s_abort); the decision
 // is warp-uniform (lane 0's clock).
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
-                                          unsigned long long limit, uint32_t sleep_ns) {
+__device__ __forceinline__ bool wait_warp_untraced(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
+                                                   unsigned long long limit, uint32_t sleep_ns) {
   // the first probe does not block: a try_wait without a time hint may wait for a while inside the
   // instruction, past a short limit, without the limit being checked
   if (__all_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity))) return true;
@@ -65,6 +65,37 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
       return false;
     }
   }
+}
+
+#ifdef MOE_TRACE
+// Trace build only (libmoe_w4_trace.so, moe_trace_read): per (CTA, warp) statistics of the waits
+// above, in the words that follow the device error word there: cycles waited, waits, the complement
+// (2^64 - 1 - t) of clock64 at the start of the first wait, and clock64 at the end of the last.  Lane
+// 0 adds them with reductions whose result is not read, so a traced wait costs a few issued
+// instructions and no round trip to memory.
+constexpr int TRACE_CTAS = 1024;
+constexpr int TRACE_ERR_INTS = 64;  // the error word's block before the trace words
+__device__ __forceinline__ void trace_wait(int* err, long long t0, long long t1) {
+  if ((threadIdx.x & 31) != 0) return;
+  unsigned long long* w = reinterpret_cast<unsigned long long*>(err + TRACE_ERR_INTS) +
+                          4 * ((blockIdx.x % TRACE_CTAS) * 32 + (threadIdx.x >> 5));
+  atomicAdd(w, static_cast<unsigned long long>(t1 - t0));
+  atomicAdd(w + 1, 1ull);
+  atomicMax(w + 2, ~static_cast<unsigned long long>(t0));
+  atomicMax(w + 3, static_cast<unsigned long long>(t1));
+}
+#endif
+
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* s_abort, int* err,
+                                          unsigned long long limit, uint32_t sleep_ns) {
+#ifdef MOE_TRACE
+  const long long t0 = clock64();
+  const bool r = wait_warp_untraced(bar, parity, s_abort, err, limit, sleep_ns);
+  trace_wait(err, t0, clock64());
+  return r;
+#else
+  return wait_warp_untraced(bar, parity, s_abort, err, limit, sleep_ns);
+#endif
 }
 
 // Wait that ignores s_abort (used to drain copies and MMAs already in flight

@@ -458,6 +458,28 @@ int moe_get_device_error(int32_t* code);
  * result left incomplete by a timeout is reported, not followed.  Test hook. */
 void moe_set_wait_limit_ns(uint64_t ns);
 
+/* Wait statistics of the tensor-core kernels (moe_gemm_tc.cu, moe_ffn_tc.cu,
+ * moe_gemm_pair.cu) in a trace build: libmoe_w4_trace.so, built by
+ * `python -m bit_mixture_experts_gb300.build --trace` (-DMOE_TRACE), which
+ * `python -m bit_mixture_experts_gb300.trace` loads and reports.  The product
+ * library libmoe_w4.so records nothing.
+ *
+ * For each CTA (blockIdx.x mod 1024) and warp (32 slots), four uint64 words:
+ * SM cycles spent in the kernel's bounded mbarrier waits, the number of such
+ * waits, 2^64 - 1 - clock64 at the start of the warp's first wait (zero: no
+ * wait), and clock64 at the end of its last -- word 4 (32 cta + warp) + i.
+ * The words accumulate over launches until the next reset.
+ *
+ * moe_trace_words: the number of words (1024 x 32 x 4), or 0 in the product
+ * library.
+ * moe_trace_reset: zeroes them, ordered on `stream`.
+ * moe_trace_read: synchronous copy of the first `words` words to `host`.
+ * Both return MOE_ERR_MODE in the product library, MOE_ERR_NULL for a null
+ * `host`, MOE_ERR_CUDA on a failed CUDA call. */
+size_t moe_trace_words(void);
+int moe_trace_reset(moe_stream_t stream);
+int moe_trace_read(uint64_t* host, size_t words);
+
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int moe_version(void);
 

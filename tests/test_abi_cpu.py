@@ -178,3 +178,25 @@ def test_layer_forward_argument_errors(lib):
     assert fwd(1, 2048, small_ws, weights=None) == -1
     assert fwd(1, 100, small_ws) == -3                          # H % 64 on the fused decode path
     assert fwd(1, 2048, small_ws) == -4                         # decode workspace below its size
+
+
+def test_product_library_records_no_trace(lib):
+    """Wait statistics exist only in the trace build; the product library says so and records nothing."""
+    import numpy as np
+    assert lib.moe_trace_words() == 0
+    assert lib.moe_trace_reset(None) == -7
+    buf = np.zeros(4, np.uint64)
+    assert lib.moe_trace_read(buf.ctypes.data, buf.size) == -7
+
+
+def test_trace_build_exports_its_words():
+    """The -DMOE_TRACE build of the same sources (libmoe_w4_trace.so) compiles, loads beside the product
+    library, and keeps 1024 CTAs x 32 warps x 4 words."""
+    from bit_mixture_experts_gb300 import build
+    path = build.build(trace=True)
+    assert os.path.basename(path) == "libmoe_w4_trace.so"
+    tl = ctypes.CDLL(path)
+    tl.moe_trace_words.restype = ctypes.c_size_t
+    assert tl.moe_trace_words() == 1024 * 32 * 4
+    tl.moe_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    assert tl.moe_trace_read(None, 4) == -1  # MOE_ERR_NULL before any CUDA call
