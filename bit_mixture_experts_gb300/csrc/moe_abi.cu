@@ -6,14 +6,17 @@
 #include <mutex>
 
 #include "moe_common.cuh"
+#ifdef MOE_TRACE
+#include "moe_tc_dev.cuh"  // the trace words' layout (TRACE_ERR_INTS, TRACE_CTAS, trace_wait)
+#endif
 
 namespace moe {
 
 #ifdef MOE_TRACE
 // The trace build keeps the wait statistics of the tensor-core kernels right after the error word
 // (TRACE_ERR_INTS ints, then TRACE_CTAS x 32 warps x 4 words; see trace_wait).
-constexpr int TRACE_ERR_INTS = 64;
-constexpr size_t TRACE_WORDS = 1024 * 32 * 4;
+using tc_dev::TRACE_ERR_INTS;
+constexpr size_t TRACE_WORDS = static_cast<size_t>(tc_dev::TRACE_CTAS) * 32 * 4;
 struct TraceBlock {
   int err[TRACE_ERR_INTS];
   unsigned long long words[TRACE_WORDS];
