@@ -349,11 +349,19 @@ def pin_router_logits_exact_sum(T=3, H=128, E=5, seed=13):
 
 
 def pin_rms_norm(T=4, H=64, seed=14):
-    """RMS norm: a constant row becomes all +-1 (up to eps, which bf16 cannot see), and every output is
-    the brute-force x / sqrt(mean x^2 + eps) rounded once to bf16."""
+    """RMS norm: a constant row becomes all +-1 (up to eps, which bf16 cannot see); a constant row c
+    whose square is comparable to eps (or below it) becomes c / sqrt(c^2 + 1e-6), the closed form that
+    fixes where eps sits and its value (the reading of the layer's normalisation: eps = 1e-6 under
+    the square root); and every output is the brute-force x / sqrt(mean x^2 + eps) rounded once to
+    bf16."""
     const = np.array([[2.5] * H, [-0.375] * H], dtype=np.float32)
     got = moe_ref.rms_norm(workloads.f32_to_bf16_bits(const))
     assert np.array_equal(got, np.sign(const.astype(np.float64)))
+    for c in (2.0 ** -10, -(2.0 ** -12)):
+        got = moe_ref.rms_norm(workloads.f32_to_bf16_bits(np.full((1, H), c, dtype=np.float32)))
+        want = brute.rne_bf16(c / math.sqrt(c * c + 1e-6))
+        assert abs(want) < 0.75  # far from the +-1 of large rows: eps decides it
+        assert np.all(got == want), (c, got[0, 0], want)
     r = np.random.default_rng(seed)
     xb = workloads.f32_to_bf16_bits((r.standard_normal((T, H)) * 3).astype(np.float32))
     got = moe_ref.rms_norm(xb)

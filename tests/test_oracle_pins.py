@@ -166,7 +166,43 @@ def _mutations():
         x = moe_ref.bf16_value(x_bits)
         return moe_ref.round_bf16(x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps))
 
+    def scale_bias_swapped(packed, scale_bits, bias_bits):
+        return orig["dequant"](packed, bias_bits, scale_bits)
+
+    def sigmoid_for_silu(g):
+        return 1.0 / (1.0 + np.exp(-g))
+
+    def rms_eps_outside(x_bits, eps=moe_ref.RMS_EPS):
+        x = moe_ref.bf16_value(x_bits)
+        return moe_ref.round_bf16(x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps))
+
+    def logits_rounded(x_bits, wr_bits):
+        return moe_ref.round_bf16(orig["router_logits"](x_bits, wr_bits)).astype(np.float32)
+
+    def tiles_too_tall(counts, offsets, T, block_n):
+        return orig["block_map"](counts, offsets, T, block_n + 1)
+
+    def nibble_pairs_swapped(p):
+        q = orig["unpack_u4"](p)
+        return q.reshape(*q.shape[:-1], -1, 2)[..., ::-1].reshape(q.shape)
+
+    def groups_of_32(packed, scale_bits, bias_bits):
+        q = orig["unpack_u4"](packed).astype(np.float64)
+        K = q.shape[-1]
+        s = np.repeat(moe_ref.bf16_value(scale_bits), 32, axis=-1)
+        b = np.repeat(moe_ref.bf16_value(bias_bits), 32, axis=-1)
+        s = np.concatenate([s, s], axis=-1)[..., :K]
+        b = np.concatenate([b, b], axis=-1)[..., :K]
+        return moe_ref.round_bf16(q * s + b)
+
     return {
+        "dequant_scale_bias_swapped": ("dequant", scale_bias_swapped),
+        "silu_is_sigmoid": ("silu", sigmoid_for_silu),
+        "rms_norm_eps_outside_sqrt": ("rms_norm", rms_eps_outside),
+        "router_logits_rounded_to_bf16": ("router_logits", logits_rounded),
+        "block_map_tiles_one_too_tall": ("block_map", tiles_too_tall),
+        "nibble_pairs_swapped": ("unpack_u4", nibble_pairs_swapped),
+        "dequant_groups_of_32": ("dequant", groups_of_32),
         "rms_norm_sum_not_mean": ("rms_norm", rms_sum_not_mean),
         "router_drops_last_k": ("router_logits", router_drops_last_k),
         "router_reversed_k": ("router_logits", router_reversed_k),
