@@ -195,7 +195,22 @@ def _mutations():
         b = np.concatenate([b, b], axis=-1)[..., :K]
         return moe_ref.round_bf16(q * s + b)
 
+    def ids_sorted_weights_not(logits, k):
+        ids, w = orig["topk_route"](logits, k)
+        return np.sort(ids, axis=1), w
+
+    def signed_nibbles(p):
+        return orig["unpack_u4"](p) - 8
+
+    def perm_token_major(ids):
+        n = np.asarray(ids).size
+        perm = np.arange(n, dtype=np.int32)
+        return perm, perm.copy()
+
     return {
+        "topk_ids_sorted_weights_not": ("topk_route", ids_sorted_weights_not),
+        "nibbles_signed": ("unpack_u4", signed_nibbles),
+        "permutation_not_grouped_by_expert": ("stable_permutation", perm_token_major),
         "dequant_scale_bias_swapped": ("dequant", scale_bias_swapped),
         "silu_is_sigmoid": ("silu", sigmoid_for_silu),
         "rms_norm_eps_outside_sqrt": ("rms_norm", rms_eps_outside),
